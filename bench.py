@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""KV page backup (D2H) / restore (H2D) throughput on one GB300 (or N replicas).
+
+Default workload: the Llama-8B-shaped pool (32 layers x {K,V} x 8 KV heads x
+head_dim 128 bf16, page 16 tokens, 4096 pages, layer-first NHD; 8 GiB) with a
+page-contiguous pinned host tier of 512 slots (1 GiB).  One step = back up 512
+seeded-random pages to slots 0..511, then restore all 512 into 512 other
+random pages: 1 GiB each way across the host link.  Inputs are synthetic
+(seeded random bytes; bf16 values are opaque bytes on this path).
+
+Printed (rank 0, one JSON line): device-timed throughput of the step
+(``value``), the same through the C ABI on the host clock (``e2e``), the host
+link's pinned-memcpy peak measured in the same run, per-direction GB/s and %
+of that peak, the roofline of the dominant kernel, SM clocks sampled during
+the timed region, and the CPU oracle timed on the host cores as a baseline.
+``--impl reference`` times the CPU oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "KV page backup/restore GB/s (D2H, H2D, 1 GB300) and % of measured host-link peak"
+GB = 1e9
+
+
+def parse():
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["llama8b", "mla_fp8", "trtllm_ipc"], default="llama8b")
+    p.add_argument("--mode", choices=["zero_copy", "staged"], default="zero_copy")
+    p.add_argument("--max-ctas", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for rel in ("hierarchical_kv_cache_backup_gb300/csrc/kvb_kernels.cu",
+                "hierarchical_kv_cache_backup_gb300/csrc/kvb_internal.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+    except OSError:
+        return None
+    if t.get("kernel_sha") != kernel_sha():
+        return None
+    return t.get(key)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not found"}
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"unavailable": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": max(pw), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(cpu_seconds: float, steps: int | None = None, n_sample: int = 512,
+                  pool_pages: int = 1024):
+    """Times the CPU oracle (as it stands) on the host cores: backup of n_sample
+    random pages of the Llama-8B geometry, then restore into n_sample others, on a
+    pool of ``pool_pages`` pages.  Returns (GB/s, threads, sample text, per-step s)."""
+    import oracle
+
+    g = wl.LLAMA8B.geom.with_(P=pool_pages)
+    og = oracle.geom(g.L, g.C, g.P, g.T, g.H, g.B)
+    pool = np.full(g.pool_bytes, 7, dtype=np.uint8)
+    host = np.full(n_sample * g.page_bytes, 3, dtype=np.uint8)
+    cores = len(os.sched_getaffinity(0))
+    r = wl.rng(wl.LLAMA8B.seed)
+    per_step = 2 * n_sample * g.page_bytes
+    times = []
+    used = 1
+    t_all = time.perf_counter()
+    k = 0
+    while True:
+        src = wl.distinct_pages(r, g.P, n_sample)
+        dst = wl.distinct_pages(r, g.P, n_sample, exclude=src)
+        slots = np.arange(n_sample, dtype=np.int32)
+        t0 = time.perf_counter()
+        used = oracle.backup(og, pool, host, src, slots, threads=cores)
+        oracle.restore(og, pool, host, slots, dst, threads=cores)
+        times.append(time.perf_counter() - t0)
+        k += 1
+        if steps is not None:
+            if k >= steps:
+                break
+        elif (time.perf_counter() - t_all >= cpu_seconds and k >= 2) or k >= 200:
+            break
+    total = sum(times)
+    sample = (f"{k} x (backup {n_sample} random pages + restore {n_sample}) of the Llama-8B "
+              f"geometry on a {pool_pages}-page host pool ({per_step / 2**20:.0f} MiB per step)")
+    return per_step * k / total / GB, used, sample, times
+
+
+def run_reference(args):
+    rank, _, ws = dist_env()
+    if rank != 0:
+        return
+    w = wl.LLAMA8B
+    # the reference arm: the oracle on the host cores, a bounded sample per step
+    n_sample = 64
+    oracle_sample(0, steps=max(1, args.warmup), n_sample=n_sample)
+    gbs, used, sample, times = oracle_sample(0, steps=max(1, args.steps), n_sample=n_sample)
+    ms = 1000 * statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    g = w.geom
+    return {"workload": f"{w.name}: L{g.L} x C{g.C} x H{g.H} x T{g.T} x {g.B} B per head vector, "
+                        f"{g.P} pages ({g.pool_bytes / 2**30:.1f} GiB) "
+                        f"{'page' if g.order else 'layer'}-first "
+                        f"{'HND' if g.dev_heads else 'NHD'}, host tier "
+                        f"{'HND' if g.host_heads else 'NHD'}",
+            "pages_per_op": w.n, "page_bytes": g.page_bytes,
+            "cache": "inputs larger than L2: 1 GiB+ per direction from random pages of a "
+                     "multi-GiB pool; no flush needed"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    from hierarchical_kv_cache_backup_gb300 import build as kbuild
+
+    kbuild.build_library()
+    from hierarchical_kv_cache_backup_gb300 import kvb
+
+    rank, local, ws = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mode = kvb.KV_MODE_STAGED if args.mode == "staged" else kvb.KV_MODE_ZERO_COPY
+    kvb.kv_config_set(mode, args.max_ctas, 0)
+
+    w = {"llama8b": wl.LLAMA8B, "mla_fp8": wl.MLA_FP8, "trtllm_ipc": wl.TRTLLM}[args.workload]
+    g = w.geom
+    lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B, g.order, g.dev_heads, g.elem_bytes)
+    alloc = torch.empty(w.pool_offset + g.pool_bytes, dtype=torch.uint8, device=dev)
+    wl.fill_random_(alloc, w.seed + 100 * rank)
+    host = torch.empty(w.host_slots * g.page_bytes, dtype=torch.uint8, pin_memory=True)
+    host.copy_(alloc[:host.numel()])
+    pool = kvb.kv_pool_register(lay, alloc.data_ptr(), w.pool_offset)
+    tier = kvb.kv_host_register(host.data_ptr(), host.numel(), w.host_slots, g.host_heads, lay)
+    s_a = torch.cuda.Stream(device=dev)
+    s_b = torch.cuda.Stream(device=dev)
+    R = 8
+    idsets = [wl.op_ids(w, seed=w.seed + 17 * k + 1000 * rank) for k in range(R)]
+
+    # ---- host-link peak, measured in this run: pinned cudaMemcpyAsync, 2 GiB, best of 10
+    link = {}
+    probe_n = 2 << 30
+    pin = torch.empty(probe_n, dtype=torch.uint8, pin_memory=True)
+    dbuf = alloc[:probe_n] if alloc.numel() >= probe_n else torch.empty(probe_n, dtype=torch.uint8,
+                                                                          device=dev)
+    pin2 = torch.empty(probe_n // 2, dtype=torch.uint8, pin_memory=True)
+    dbuf2 = torch.empty(probe_n // 2, dtype=torch.uint8, device=dev)
+
+    def best_of(fn, nbytes, reps=10):
+        ts = []
+        for i in range(reps + 3):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_a)
+            fn()
+            e1.record(s_a)
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) / 1000)
+        return nbytes / min(ts) / GB
+
+    with torch.cuda.stream(s_a):
+        link["d2h"] = best_of(lambda: pin.copy_(dbuf, non_blocking=True), probe_n)
+        link["h2d"] = best_of(lambda: dbuf.copy_(pin, non_blocking=True), probe_n)
+
+    def bidir():
+        ev = torch.cuda.Event()
+        ev.record(s_a)
+        s_b.wait_event(ev)
+        with torch.cuda.stream(s_a):
+            pin[:probe_n // 2].copy_(dbuf[:probe_n // 2], non_blocking=True)
+        with torch.cuda.stream(s_b):
+            dbuf2.copy_(pin2, non_blocking=True)
+        ev2 = torch.cuda.Event()
+        ev2.record(s_b)
+        s_a.wait_event(ev2)
+    link["bidir"] = best_of(bidir, probe_n)
+    del pin, pin2, dbuf2
+    torch.cuda.empty_cache()
+
+    # ---- one step of the workload (through the C ABI; ids are host arrays)
+    bytes_b = bytes_r = 0
+    if w is wl.LLAMA8B:
+        bytes_b = bytes_r = w.n * g.page_bytes
+    elif w is wl.MLA_FP8:
+        bytes_r = g.L * w.n * g.layer_page_bytes
+    else:
+        bytes_b = bytes_r = w.n * g.page_bytes
+
+    def step(k, evs=None):
+        ids = idsets[k % R]
+        if w is wl.LLAMA8B:
+            if evs:
+                evs[0].record(s_a)
+            kvb.kv_backup(pool, tier, ids.backup_src, ids.backup_slots, s_a.cuda_stream)
+            if evs:
+                evs[1].record(s_a)
+            f = kvb.kv_restore(pool, tier, ids.restore_slots, ids.restore_dst, -1, s_a.cuda_stream)
+            if evs:
+                evs[2].record(s_a)
+            return [f]   # same stream: the restore's fence follows the backup
+        if w is wl.MLA_FP8:
+            if evs:
+                evs[0].record(s_a)
+            f = None
+            for l in range(g.L):
+                f = kvb.kv_restore(pool, tier, ids.restore_slots, ids.restore_dst, l,
+                                   s_a.cuda_stream)
+            if evs:
+                evs[1].record(s_a)
+                evs[2].record(s_a)
+            return [f]
+        # trtllm: backup on stream A and restore on stream B at the same time
+        ev = torch.cuda.Event()
+        ev.record(s_a)
+        s_b.wait_event(ev)
+        if evs:
+            evs[0].record(s_a)
+        fb = kvb.kv_backup(pool, tier, ids.backup_src, ids.backup_slots, s_a.cuda_stream)
+        if evs:
+            evs[1].record(s_a)
+        fr = kvb.kv_restore(pool, tier, ids.restore_slots, ids.restore_dst, -1, s_b.cuda_stream)
+        ev2 = torch.cuda.Event()
+        ev2.record(s_b)
+        s_a.wait_event(ev2)
+        if evs:
+            evs[2].record(s_a)
+        return [fb, fr]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for k in range(args.warmup):
+        step(k)
+    barrier()
+
+    # ---- timed region: device clock (CUDA events on the launching stream)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    l0 = kvb.kv_launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(s_a)
+        for k in range(args.steps):
+            step(k, evs[k])
+        t_end.record(s_a)
+        barrier()
+    launches = kvb.kv_launch_count() - l0
+    elapsed = t_start.elapsed_time(t_end) / 1000
+    if dist is not None:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    b_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    r_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_bytes = bytes_b + bytes_r
+    value = ws * step_bytes * args.steps / elapsed / GB
+
+    # ---- end to end through the C ABI, host clock, fence wait every step
+    barrier()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        for f in step(k):
+            kvb.kv_fence_wait(f, 60_000_000_000)
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = ws * step_bytes * args.steps / e2e_s / GB
+
+    # ---- device-side layout-transform gather (staged half) against HBM
+    peaks, peak_src = measured_peaks()
+    hbm = None
+    if w is not wl.MLA_FP8:
+        n = w.n
+        buf = torch.empty(n * g.page_bytes, dtype=torch.uint8, device=dev)
+        ts = []
+        for i in range(13):
+            ids = idsets[i % R]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_a)
+            kvb.kv_device_gather(pool, buf.data_ptr(), buf.numel(), g.host_heads, ids.backup_src,
+                                 s_a.cuda_stream)
+            e1.record(s_a)
+            e1.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1) / 1000)
+        gb_s = 2 * n * g.page_bytes / statistics.median(ts) / GB
+        hbm = {"bound": "hbm", "kernel": "kv_move_kernel (device gather, pool -> device buffer "
+                                          "in host layout)",
+               "achieved": round(gb_s, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "frac": round(gb_s / peaks["hbm_gbs"], 4),
+               "traffic": recorded_traffic("device_gather_dram_bytes_per_launch"),
+               "algorithmic_bytes_per_launch": 2 * n * g.page_bytes,
+               "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
+        del buf
+
+    # ---- dominant kernel: the backup (D2H) move, or the restore for MLA
+    if w is wl.MLA_FP8:
+        dom_ms = statistics.mean(b_ms) / g.L
+        dom_bytes = w.n * g.layer_page_bytes
+        dom_peak, dom_dir = link["h2d"], "h2d"
+        kern = "kv_move_kernel (restore of one layer, zero-copy H2D)"
+    else:
+        dom_ms = statistics.mean(b_ms)
+        dom_bytes = bytes_b
+        dom_peak, dom_dir = link["d2h"], "d2h"
+        kern = "kv_move_kernel (backup, zero-copy D2H)" if mode == 0 else \
+            "kv_move_kernel + cudaMemcpyAsync (backup, staged D2H)"
+    achieved = dom_bytes / (dom_ms / 1000) / GB
+    roofline = {"bound": "host_link", "kernel": kern, "achieved": round(achieved, 2),
+                "peak": round(dom_peak, 2), "unit": "GB/s", "frac": round(achieved / dom_peak, 4),
+                "traffic": recorded_traffic("backup_dram_bytes_per_launch"),
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "peak_source": f"pinned cudaMemcpyAsync {dom_dir} of 2 GiB measured in this run, "
+                               "best of 10 (host link peak; not in MEASURED_PEAKS.json)"}
+    backup_gbs = bytes_b / (statistics.mean(b_ms) / 1000) / GB if bytes_b and w is not wl.MLA_FP8 \
+        else None
+    restore_gbs = bytes_r / (statistics.mean(r_ms if w is wl.LLAMA8B else b_ms) / 1000) / GB \
+        if w is not wl.TRTLLM else None
+    if w is wl.MLA_FP8:
+        restore_gbs = bytes_r / (statistics.mean(b_ms) / 1000) / GB
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * elapsed / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded random bytes; bf16/fp8 KV are opaque bytes)",
+        "config": dict(config_of(w), mode=args.mode,
+                       step=("backup n pages then restore n pages, one stream"
+                             if w is wl.LLAMA8B else
+                             "61 one-layer restores of 64 pages on a copy stream"
+                             if w is wl.MLA_FP8 else
+                             "backup n pages (stream A) while restoring n others (stream B)")),
+        "backup_gbs": round(backup_gbs, 2) if backup_gbs else None,
+        "restore_gbs": round(restore_gbs, 2) if restore_gbs else None,
+        "pages_per_s": round(ws * (w.n * (2 if bytes_b else 1)) * args.steps / elapsed, 1),
+        "host_link_peak_gbs": {k: round(v, 2) for k, v in link.items()},
+        "pct_of_host_link_peak": {
+            "d2h": round(100 * backup_gbs / link["d2h"], 2) if backup_gbs else None,
+            "h2d": round(100 * restore_gbs / link["h2d"], 2) if restore_gbs else None,
+            "step_vs_sequential_peak": round(
+                100 * value / ws / (step_bytes / ((bytes_b / link["d2h"] if bytes_b else 0) +
+                                                  bytes_r / link["h2d"])), 2)
+            if w is not wl.TRTLLM else round(100 * value / ws / link["bidir"], 2)},
+        "roofline": roofline,
+        "roofline_hbm": hbm,
+        "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": bytes_r +
+                8 * w.n * (2 if bytes_b else g.L), "d2h_bytes_per_step": bytes_b + 8,
+                "note": "host clock around kv_backup/kv_restore with host id arrays and a fence "
+                        "wait every step; payload crosses the host link inside the region"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        del alloc
+        torch.cuda.empty_cache()
+        gbs, used, sample, _ = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": used,
+                                "kind": "oracle", "sample": sample}
+    else:
+        line["cpu_baseline"] = None
+    kvb.kv_pool_close(pool)
+    kvb.kv_host_close(tier)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

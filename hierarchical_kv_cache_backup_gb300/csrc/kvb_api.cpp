@@ -1,0 +1,1009 @@
+// kvb_api.cpp -- host side of the KV backup / restore engine: the C ABI of
+// include/kvb.h.  Validation, handle and IPC-mapping registries, fences, and
+// the launch plan of each operation.  All data movement happens in the
+// kernels of kvb_kernels.cu (and, in STAGED mode, in copy-engine memcpys).
+//
+// Pages this follows (by title and section):
+//   [RFC] "[Feature] [RFC] [HiCache] Out-of-process HiCache data plane with
+//         device-memory IPC": §Device IPC data path, §Ownership, §Failure and
+//         lifecycle handling.
+//   [PR]  "[PP + HiCache] Add PP Prefetch Tickets for eager cross-stage
+//         storage prefetch": §PP Prefetch Ticket Path (layer-wise H2D).
+//   [LMC] "LMCacheRawCudaIPCWrapper深度解析": §共享与重建的完整链路,
+//         §发送端校验, §重建生命周期与引用计数, §为什么不做_share_cuda_回退.
+#include "kvb.h"
+#include "kvb_internal.h"
+
+#include <cuda.h>   // CUresult / CUdeviceptr types only; the function comes from the runtime
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <ctime>
+#include <mutex>
+#include <sched.h>
+#include <string>
+#include <unistd.h>
+#include <unordered_map>
+#include <vector>
+
+using namespace kvb;
+
+namespace {
+
+// ------------------------------------------------------------------ errors
+
+thread_local std::string t_err;
+
+kv_status fail(kv_status st, const char *fmt, ...) {
+    char buf[768];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return st;
+}
+
+kv_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(KV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- geometry
+
+struct Geo {
+    uint64_t L, C, P, T, H, B;
+    uint32_t order, heads;
+    uint64_t cb;   // chunk bytes: T*H*B (one page or slot, one layer, one component)
+    uint64_t pb;   // page bytes: L*C*cb
+};
+
+bool mul_ok(uint64_t a, uint64_t b, uint64_t lim, uint64_t *out) {
+    if (a != 0 && b > lim / a) return false;
+    *out = a * b;
+    return true;
+}
+
+// Layout checks shared by every entry point ([LMC] §发送端校验: reject, never guess).
+kv_status check_layout(const kv_layout *lay, Geo *g) {
+    if (lay == nullptr) return fail(KV_ERR_INVALID_ARG, "layout is NULL");
+    if (lay->num_layers == 0 || lay->num_comps == 0 || lay->num_pages == 0 ||
+        lay->page_tokens == 0 || lay->num_heads == 0 || lay->head_bytes == 0)
+        return fail(KV_ERR_LAYOUT,
+                    "layout has a zero dimension (L=%u C=%u P=%u T=%u H=%u B=%u)",
+                    lay->num_layers, lay->num_comps, lay->num_pages, lay->page_tokens,
+                    lay->num_heads, lay->head_bytes);
+    if (lay->order > KV_PAGE_FIRST || lay->heads > KV_HND || lay->reserved != 0)
+        return fail(KV_ERR_LAYOUT, "layout has unknown order %u / heads %u or reserved %u != 0",
+                    lay->order, lay->heads, lay->reserved);
+    if (lay->head_bytes % 16 != 0)
+        return fail(KV_ERR_ALIGNMENT, "head_bytes %u is not a multiple of 16", lay->head_bytes);
+    Geo r{lay->num_layers, lay->num_comps, lay->num_pages, lay->page_tokens, lay->num_heads,
+          lay->head_bytes, lay->order, lay->heads, 0, 0};
+    uint64_t th, lc, pool;
+    const uint64_t lim = 1ull << 62;
+    if (!mul_ok(r.T, r.H, lim, &th) || !mul_ok(th, r.B, lim, &r.cb) ||
+        !mul_ok(r.L, r.C, lim, &lc) || !mul_ok(lc, r.cb, lim, &r.pb) ||
+        !mul_ok(r.pb, r.P, lim, &pool))
+        return fail(KV_ERR_LAYOUT, "layout sizes overflow 64-bit byte offsets");
+    if (r.cb / 16 >= (1ull << 31))
+        return fail(KV_ERR_LAYOUT, "one (page, layer, component) chunk of %llu bytes is too large",
+                    (unsigned long long)r.cb);
+    *g = r;
+    return KV_OK;
+}
+
+bool same_slot_geometry(const Geo &a, const Geo &b) {
+    return a.L == b.L && a.C == b.C && a.T == b.T && a.H == b.H && a.B == b.B;
+}
+
+// --------------------------------------------------------------- handles
+
+struct PoolObj {
+    Geo g{};
+    kv_layout layout;
+    char *dev;           // device address of the pool's first byte
+    uint64_t nbytes;
+    int device;
+    uint64_t instance_id, generation;
+    bool imported;
+    std::string ipc_key; // handle bytes of the mapping (imported pools)
+};
+
+struct HostObj {
+    Geo g{};               // slot geometry (P unused)
+    uint32_t heads;      // head order of the tier
+    uint32_t num_slots;
+    char *host;
+    char *dev_view;      // device-visible address of `host`
+    uint64_t bytes;
+};
+
+struct Mapping {
+    void *base;
+    int refs;
+    int device;
+};
+
+constexpr int kRing = 4096;       // fence words / events per device
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kSeqMask = (1ull << 56) - 1;
+
+struct DevState {
+    bool init = false;
+    unsigned long long *words = nullptr;     // host view of the fence words
+    unsigned long long *words_dev = nullptr; // device view
+    uint32_t *err = nullptr;                 // sticky "kernel met a bad id" word
+    uint32_t *err_dev = nullptr;
+    cudaEvent_t ev[kRing] = {};
+    uint64_t slot_seq[kRing] = {};
+    int sms = 0;
+    char *staging = nullptr;                 // STAGED mode buffer, two halves
+    uint64_t staging_bytes = 0;
+    cudaEvent_t staging_free[2] = {nullptr, nullptr};
+    bool staging_used[2] = {false, false};
+};
+
+std::mutex g_mu;
+std::unordered_map<uint64_t, PoolObj *> g_pools;   // handle id -> object
+std::unordered_map<uint64_t, HostObj *> g_hosts;
+std::unordered_map<std::string, Mapping> g_maps;   // IPC handle bytes -> mapping
+std::unordered_map<uint64_t, uint64_t> g_floor;    // instance -> lowest live generation
+uint64_t g_next_handle = 1;                         // handle ids are never reused
+uint64_t g_next_seq = 1;
+DevState g_dev[kMaxDevices];
+kv_config g_cfg = {KV_MODE_ZERO_COPY, 0, 0};
+std::atomic<uint64_t> g_launches{0};
+
+constexpr uint64_t kDefaultStaging = 256ull << 20;
+
+uint64_t handle_id(const void *h) { return (uint64_t)(uintptr_t)h; }
+
+PoolObj *find_pool(kv_pool p) {
+    auto it = g_pools.find(handle_id(p));
+    return it == g_pools.end() ? nullptr : it->second;
+}
+
+HostObj *find_host(kv_host h) {
+    auto it = g_hosts.find(handle_id(h));
+    return it == g_hosts.end() ? nullptr : it->second;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    int want;
+    explicit DeviceGuard(int d) : want(d) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != want) cudaSetDevice(want);
+    }
+    ~DeviceGuard() {
+        if (prev >= 0 && prev != want) cudaSetDevice(prev);
+    }
+};
+
+typedef CUresult (*GetAddressRangeFn)(CUdeviceptr *, size_t *, CUdeviceptr);
+
+kv_status address_range(const void *p, uintptr_t *base, size_t *size) {
+    static GetAddressRangeFn fn = nullptr;
+    if (fn == nullptr) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || f == nullptr)
+            return fail(KV_ERR_CUDA, "cuMemGetAddressRange entry point unavailable");
+        fn = (GetAddressRangeFn)f;
+    }
+    CUdeviceptr b = 0;
+    size_t s = 0;
+    CUresult r = fn(&b, &s, (CUdeviceptr)(uintptr_t)p);
+    if (r != CUDA_SUCCESS)
+        return fail(KV_ERR_INVALID_ARG, "pointer %p is not inside a device allocation (CUresult %d)",
+                    p, (int)r);
+    *base = (uintptr_t)b;
+    *size = s;
+    return KV_OK;
+}
+
+kv_status init_device(int d) {
+    if (d < 0 || d >= kMaxDevices) return fail(KV_ERR_INVALID_ARG, "device %d out of range", d);
+    DevState &s = g_dev[d];
+    if (s.init) return KV_OK;
+    DeviceGuard guard(d);
+    void *mem = nullptr;
+    cudaError_t e = cudaHostAlloc(&mem, kRing * sizeof(unsigned long long) + 64,
+                                  cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(fence words)");
+    std::memset(mem, 0, kRing * sizeof(unsigned long long) + 64);
+    void *dmem = nullptr;
+    e = cudaHostGetDevicePointer(&dmem, mem, 0);
+    if (e != cudaSuccess) {
+        cudaFreeHost(mem);
+        return cuda_fail(e, "cudaHostGetDevicePointer(fence words)");
+    }
+    s.words = (unsigned long long *)mem;
+    s.words_dev = (unsigned long long *)dmem;
+    s.err = (uint32_t *)(s.words + kRing);
+    s.err_dev = (uint32_t *)(s.words_dev + kRing);
+    cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, d);
+    if (s.sms <= 0) s.sms = 1;
+    s.init = true;
+    return KV_OK;
+}
+
+// ------------------------------------------------------------------ fences
+
+unsigned long long load_acquire(const unsigned long long *p) {
+    return __atomic_load_n(p, __ATOMIC_ACQUIRE);
+}
+
+double now_ns() {
+    timespec ts;
+    clock_gettime(CLOCK_MONOTONIC, &ts);
+    return ts.tv_sec * 1e9 + ts.tv_nsec;
+}
+
+// Called with g_mu held, device current.  Enqueues the completion marker and
+// records the slot's event.
+kv_status issue_fence(int d, cudaStream_t stream, kv_fence *out) {
+    DevState &s = g_dev[d];
+    const uint64_t seq = g_next_seq;
+    if (seq > kSeqMask) return fail(KV_ERR_NO_MEMORY, "fence sequence space exhausted");
+    const int k = (int)(seq % kRing);
+    if (s.slot_seq[k] != 0 && load_acquire(&s.words[k]) < s.slot_seq[k]) {
+        // The op that last used this slot (kRing fences ago) is still running.
+        const double deadline = now_ns() + 30e9;
+        while (load_acquire(&s.words[k]) < s.slot_seq[k]) {
+            if (now_ns() > deadline)
+                return fail(KV_ERR_NO_MEMORY, "%d fences in flight: fence ring exhausted", kRing);
+            sched_yield();
+        }
+    }
+    if (s.ev[k] == nullptr) {
+        cudaError_t e = cudaEventCreateWithFlags(&s.ev[k], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            s.ev[k] = nullptr;
+            return cuda_fail(e, "cudaEventCreate(fence)");
+        }
+    }
+    cudaError_t e = launch_mark(s.words_dev + k, seq, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch of the completion marker");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    e = cudaEventRecord(s.ev[k], stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fence)");
+    s.slot_seq[k] = seq;
+    g_next_seq = seq + 1;
+    *out = ((uint64_t)d << 56) | seq;
+    return KV_OK;
+}
+
+// Decodes a fence; returns KV_OK with done set, or an error.
+kv_status fence_state(kv_fence f, bool *done, int *dev, int *slot) {
+    const int d = (int)(f >> 56);
+    const uint64_t seq = f & kSeqMask;
+    if (seq == 0 || d >= kMaxDevices) return fail(KV_ERR_INVALID_ARG, "invalid fence %llu",
+                                                  (unsigned long long)f);
+    unsigned long long *words;
+    uint64_t next;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_dev[d].init || seq >= g_next_seq)
+            return fail(KV_ERR_INVALID_ARG, "fence %llu was never issued", (unsigned long long)f);
+        words = g_dev[d].words;
+        next = g_next_seq;
+    }
+    const int k = (int)(seq % kRing);
+    *done = (next - seq > (uint64_t)kRing) || load_acquire(&words[k]) >= seq;
+    *dev = d;
+    *slot = k;
+    return KV_OK;
+}
+
+// -------------------------------------------------------------- validation
+
+struct DupStamp {
+    std::vector<uint32_t> stamp;
+    uint32_t epoch = 0;
+};
+thread_local DupStamp t_dup;
+
+kv_status check_ids(const char *what, const int32_t *ids, uint32_t n, uint64_t limit,
+                    bool no_dups) {
+    if (no_dups) {
+        if (t_dup.stamp.size() < limit) t_dup.stamp.assign(limit, 0u);
+        if (++t_dup.epoch == 0) {
+            std::fill(t_dup.stamp.begin(), t_dup.stamp.end(), 0u);
+            t_dup.epoch = 1;
+        }
+    }
+    for (uint32_t i = 0; i < n; ++i) {
+        const int32_t v = ids[i];
+        if (v < 0 || (uint64_t)v >= limit)
+            return fail(KV_ERR_OUT_OF_RANGE, "%s[%u] = %d is outside [0, %llu)", what, i, v,
+                        (unsigned long long)limit);
+        if (no_dups) {
+            if (t_dup.stamp[v] == t_dup.epoch)
+                return fail(KV_ERR_DUPLICATE, "%s[%u] = %d appears twice: one call may write a "
+                            "page or slot only once", what, i, v);
+            t_dup.stamp[v] = t_dup.epoch;
+        }
+    }
+    return KV_OK;
+}
+
+// kind 0 = backup (a = src pages, b = slots), 1 = restore (a = slots, b = dst pages)
+kv_status check_op(const Geo &g, uint64_t num_slots, int kind, const int32_t *a, const int32_t *b,
+                   uint32_t n, int32_t layer) {
+    if (kind != 0 && kind != 1) return fail(KV_ERR_INVALID_ARG, "unknown operation kind %d", kind);
+    if (n > 0 && (a == nullptr || b == nullptr))
+        return fail(KV_ERR_INVALID_ARG, "id arrays must be non-NULL when n = %u", n);
+    if (n > (1u << 30)) return fail(KV_ERR_INVALID_ARG, "n = %u is too large", n);
+    if (layer < -1 || (layer >= 0 && (uint64_t)layer >= g.L))
+        return fail(KV_ERR_OUT_OF_RANGE, "layer %d is outside [-1, %llu)", layer,
+                    (unsigned long long)g.L);
+    if (kind == 0) {
+        if (layer != -1) return fail(KV_ERR_INVALID_ARG, "backup always moves every layer");
+        kv_status st = check_ids("src_pages", a, n, g.P, false);
+        if (st != KV_OK) return st;
+        return check_ids("host_slots", b, n, num_slots, true);
+    }
+    kv_status st = check_ids("host_slots", a, n, num_slots, false);
+    if (st != KV_OK) return st;
+    return check_ids("dst_pages", b, n, g.P, true);
+}
+
+// ---------------------------------------------------------- launch planning
+
+Side pool_side(const PoolObj &p) {
+    const Geo &g = p.g;
+    Side s{};
+    s.base = (uint64_t)(uintptr_t)p.dev;
+    if (g.order == KV_PAGE_FIRST) {   // [P][L][C] chunks
+        s.s_id = g.L * g.C * g.cb;
+        s.s_l = g.C * g.cb;
+        s.s_c = g.cb;
+    } else {                          // [L][C][P] chunks
+        s.s_id = g.cb;
+        s.s_l = g.C * g.P * g.cb;
+        s.s_c = g.P * g.cb;
+    }
+    s.hnd = g.heads;
+    s.id_limit = (uint32_t)std::min<uint64_t>(g.P, 0xffffffffull);
+    return s;
+}
+
+Side host_side(const HostObj &h) {
+    const Geo &g = h.g;
+    Side s{};
+    s.base = (uint64_t)(uintptr_t)h.dev_view;
+    s.s_id = g.pb;                    // [S][L][C] chunks
+    s.s_l = g.C * g.cb;
+    s.s_c = g.cb;
+    s.hnd = h.heads;
+    s.id_limit = h.num_slots;
+    return s;
+}
+
+// Staging buffer in host layout for items 0..m-1, layers [l0, l0+nl).
+Side staging_side(char *base, const Geo &g, uint32_t heads, uint32_t nl, uint32_t l0,
+                  uint32_t m) {
+    Side s{};
+    s.s_id = (uint64_t)nl * g.C * g.cb;
+    s.s_l = g.C * g.cb;
+    s.s_c = g.cb;
+    s.base = (uint64_t)(uintptr_t)base - (uint64_t)l0 * s.s_l;   // index layers from l0
+    s.hnd = heads;
+    s.id_limit = m;
+    return s;
+}
+
+struct Plan {
+    MoveDesc d;
+    uint32_t max_items;   // items per launch
+};
+
+kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint32_t l0,
+               uint32_t *err_dev, bool iter_dst, Plan *out) {
+    MoveDesc d{};
+    d.src = src;
+    d.dst = dst;
+    d.nl = nl;
+    d.l0 = l0;
+    d.C = (uint32_t)g.C;
+    d.cb16 = (uint32_t)(g.cb / 16);
+    d.segs = (d.cb16 + kSegPieces - 1) / kSegPieces;
+    d.H = (uint32_t)g.H;
+    d.T = (uint32_t)g.T;
+    d.B16 = (uint32_t)(g.B / 16);
+    d.transpose = (src.hnd != dst.hnd && g.H > 1 && g.T > 1) ? 1u : 0u;
+    d.iter_dst = iter_dst ? 1u : 0u;
+    const uint64_t per_item = (uint64_t)nl * g.C * d.segs;
+    if (per_item == 0 || per_item > 0xffffffffull || (uint64_t)nl * g.C > 0xffffffffull)
+        return fail(KV_ERR_LAYOUT, "one page needs %llu warp segments: too large",
+                    (unsigned long long)per_item);
+    uint64_t m = 0xffffffffull / per_item;
+    out->max_items = (uint32_t)std::min<uint64_t>(m, (uint64_t)kMaxItems);
+    d.div_segs = make_fastdiv(d.segs);
+    d.div_lc = make_fastdiv(nl * d.C);
+    d.div_c = make_fastdiv(d.C);
+    d.div_b16 = make_fastdiv(d.B16);
+    d.div_T = make_fastdiv(d.T);
+    d.div_H = make_fastdiv(d.H);
+    d.err = err_dev;
+    out->d = d;
+    return KV_OK;
+}
+
+int default_ctas(const DevState &s, bool touches_host) {
+    if (g_cfg.max_ctas != 0) return (int)g_cfg.max_ctas;
+    return touches_host ? 2 * s.sms : 4 * s.sms;
+}
+
+// Launches the move for items [0, n) of (a, b) in slices of at most max_items.
+// b_is_index: the destination id of item i is i itself (a staging position).
+kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int ctas_cap,
+                    cudaStream_t stream, bool b_is_index) {
+    static thread_local MoveIds ids;
+    for (uint32_t i0 = 0; i0 < n; i0 += p.max_items) {
+        const uint32_t m = std::min(p.max_items, n - i0);
+        std::memcpy(ids.a, a + i0, m * sizeof(int32_t));
+        if (b_is_index)
+            for (uint32_t k = 0; k < m; ++k) ids.b[k] = (int32_t)(i0 + k);
+        else
+            std::memcpy(ids.b, b + i0, m * sizeof(int32_t));
+        p.d.n = m;
+        p.d.total_segs = m * p.d.nl * p.d.C * p.d.segs;
+        const uint32_t warps_needed = p.d.total_segs;
+        const uint32_t per_cta = kMoveThreads / 32;
+        const uint64_t need = (warps_needed + per_cta - 1) / per_cta;
+        const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
+        cudaError_t e = launch_move(p.d, ids, ctas, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    return KV_OK;
+}
+
+kv_status ensure_staging(DevState &s) {
+    const uint64_t want = g_cfg.staging_bytes ? g_cfg.staging_bytes : kDefaultStaging;
+    if (s.staging != nullptr && s.staging_bytes == want) return KV_OK;
+    if (s.staging != nullptr) {
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize (staging resize)");
+        cudaFree(s.staging);
+        s.staging = nullptr;
+        s.staging_used[0] = s.staging_used[1] = false;
+    }
+    void *p = nullptr;
+    cudaError_t e = cudaMalloc(&p, want);
+    if (e != cudaSuccess) return fail(KV_ERR_NO_MEMORY, "staging buffer of %llu bytes: %s",
+                                      (unsigned long long)want, cudaGetErrorString(e));
+    s.staging = (char *)p;
+    s.staging_bytes = want;
+    for (int h = 0; h < 2; ++h)
+        if (s.staging_free[h] == nullptr) {
+            e = cudaEventCreateWithFlags(&s.staging_free[h], cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(staging)");
+        }
+    return KV_OK;
+}
+
+// Copies between a host tier and the staging buffer, one memcpy per run of
+// consecutive slots.  `lb` = bytes per item moved (whole page or one layer),
+// `host_off` = byte offset of the moved part inside a slot.
+kv_status staged_copies(const HostObj &h, char *staging, const int32_t *slots, uint32_t m,
+                        uint64_t lb, uint64_t host_off, bool to_host, cudaStream_t stream) {
+    const uint64_t pb = h.g.pb;
+    uint32_t i = 0;
+    while (i < m) {
+        uint32_t j = i + 1;
+        while (j < m && slots[j] == slots[j - 1] + 1) ++j;
+        const uint32_t run = j - i;
+        char *hp = h.host + (uint64_t)slots[i] * pb + host_off;
+        char *sp = staging + (uint64_t)i * lb;
+        cudaError_t e;
+        if (lb == pb) {
+            e = to_host ? cudaMemcpyAsync(hp, sp, run * lb, cudaMemcpyDeviceToHost, stream)
+                        : cudaMemcpyAsync(sp, hp, run * lb, cudaMemcpyHostToDevice, stream);
+        } else {
+            e = to_host ? cudaMemcpy2DAsync(hp, pb, sp, lb, lb, run, cudaMemcpyDeviceToHost, stream)
+                        : cudaMemcpy2DAsync(sp, lb, hp, pb, lb, run, cudaMemcpyHostToDevice, stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "staged cudaMemcpyAsync");
+        i = j;
+    }
+    return KV_OK;
+}
+
+// Issues one backup (kind 0) or restore (kind 1).  g_mu held.
+kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, const int32_t *b,
+                uint32_t n, int32_t layer, void *stream_v, kv_fence *fence) {
+    if (fence == nullptr) return fail(KV_ERR_INVALID_ARG, "fence output pointer is NULL");
+    if (pool_h == nullptr || host_h == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "pool or host handle is NULL");
+    PoolObj *pool = find_pool(pool_h);
+    if (pool == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    HostObj *host = find_host(host_h);
+    if (host == nullptr) return fail(KV_ERR_CLOSED, "host handle is closed or unknown");
+    auto fl = g_floor.find(pool->instance_id);
+    if (fl != g_floor.end() && pool->generation < fl->second)
+        return fail(KV_ERR_STALE, "pool generation %llu of instance %llu is retired (floor %llu)",
+                    (unsigned long long)pool->generation, (unsigned long long)pool->instance_id,
+                    (unsigned long long)fl->second);
+    if (!same_slot_geometry(pool->g, host->g))
+        return fail(KV_ERR_LAYOUT, "pool and host tier have different page geometry");
+    kv_status st = check_op(pool->g, host->num_slots, kind, a, b, n, layer);
+    if (st != KV_OK) return st;
+
+    const int d = pool->device;
+    DeviceGuard guard(d);
+    st = init_device(d);
+    if (st != KV_OK) return st;
+    DevState &ds = g_dev[d];
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    const bool backup = kind == 0;
+    const uint32_t nl = layer < 0 ? (uint32_t)pool->g.L : 1u;
+    const uint32_t l0 = layer < 0 ? 0u : (uint32_t)layer;
+
+    if (n > 0 && g_cfg.mode == KV_MODE_ZERO_COPY) {
+        const Side ps = pool_side(*pool), hs = host_side(*host);
+        Plan p;
+        st = plan(pool->g, backup ? ps : hs, backup ? hs : ps, nl, l0, ds.err_dev,
+                  /*iter_dst=*/backup, &p);
+        if (st != KV_OK) return st;
+        st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false);
+        if (st != KV_OK) return st;
+    } else if (n > 0) {
+        st = ensure_staging(ds);
+        if (st != KV_OK) return st;
+        const int half = backup ? 0 : 1;
+        char *stg = ds.staging + (uint64_t)half * (ds.staging_bytes / 2);
+        const uint64_t half_bytes = ds.staging_bytes / 2;
+        const uint64_t layer_bytes = pool->g.C * pool->g.cb;        // one layer of one page
+        // layers per group: the whole range if one page fits, else as many as fit
+        const uint32_t gl = (uint32_t)std::min<uint64_t>(nl, half_bytes / layer_bytes);
+        if (gl == 0)
+            return fail(KV_ERR_NO_MEMORY, "staging half of %llu bytes holds no layer of %llu bytes",
+                        (unsigned long long)half_bytes, (unsigned long long)layer_bytes);
+        const uint64_t lb = (uint64_t)gl * layer_bytes;              // staged bytes per item
+        const uint64_t fit = half_bytes / lb;                         // items per staging fill
+        if (ds.staging_used[half]) {
+            cudaError_t e = cudaStreamWaitEvent(stream, ds.staging_free[half], 0);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(staging)");
+        }
+        const Side ps = pool_side(*pool);
+        static thread_local std::vector<int32_t> idx;
+        for (uint32_t la = l0; la < l0 + nl; la += gl) {
+            const uint32_t g_n = std::min(gl, l0 + nl - la);          // layers in this group
+            const uint64_t host_off = (uint64_t)la * layer_bytes;
+            const uint64_t gb = (uint64_t)g_n * layer_bytes;
+            for (uint32_t i0 = 0; i0 < n; i0 += (uint32_t)std::min<uint64_t>(fit, n)) {
+                const uint32_t m = (uint32_t)std::min<uint64_t>(fit, n - i0);
+                const Side ss = staging_side(stg, pool->g, host->heads, g_n, la, m);
+                Plan p;
+                st = plan(pool->g, backup ? ps : ss, backup ? ss : ps, g_n, la, ds.err_dev, backup,
+                          &p);
+                if (st != KV_OK) return st;
+                if (backup) {
+                    st = run_moves(p, a + i0, nullptr, m, default_ctas(ds, false), stream, true);
+                    if (st == KV_OK)
+                        st = staged_copies(*host, stg, b + i0, m, gb, host_off, true, stream);
+                } else {
+                    st = staged_copies(*host, stg, a + i0, m, gb, host_off, false, stream);
+                    if (st == KV_OK) {
+                        // staging item k -> dst page b[i0 + k]: a = staging index, b = page
+                        idx.resize(m);
+                        for (uint32_t k = 0; k < m; ++k) idx[k] = (int32_t)k;
+                        st = run_moves(p, idx.data(), b + i0, m, default_ctas(ds, false), stream,
+                                       false);
+                    }
+                }
+                if (st != KV_OK) return st;
+            }
+        }
+        cudaError_t e = cudaEventRecord(ds.staging_free[half], stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
+        ds.staging_used[half] = true;
+    }
+    return issue_fence(d, stream, fence);
+}
+
+// Device gather (kind 0) / scatter (kind 1) between the pool and a caller's
+// device buffer in host-tier layout.  g_mu held.
+kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t buf_heads, int kind,
+                       const int32_t *pages, uint32_t n, int32_t layer, void *stream_v,
+                       kv_fence *fence) {
+    if (fence == nullptr) return fail(KV_ERR_INVALID_ARG, "fence output pointer is NULL");
+    if (pool_h == nullptr) return fail(KV_ERR_INVALID_ARG, "pool handle is NULL");
+    PoolObj *pool = find_pool(pool_h);
+    if (pool == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    auto fl = g_floor.find(pool->instance_id);
+    if (fl != g_floor.end() && pool->generation < fl->second)
+        return fail(KV_ERR_STALE, "pool generation %llu of instance %llu is retired",
+                    (unsigned long long)pool->generation, (unsigned long long)pool->instance_id);
+    if (buf_heads > KV_HND) return fail(KV_ERR_LAYOUT, "unknown buffer head order %u", buf_heads);
+    if (n > 0 && (pages == nullptr || buf == nullptr))
+        return fail(KV_ERR_INVALID_ARG, "page list and buffer must be non-NULL when n = %u", n);
+    if (((uintptr_t)buf) % 16 != 0)
+        return fail(KV_ERR_ALIGNMENT, "buffer %p is not 16-byte aligned", buf);
+    const Geo &g = pool->g;
+    if (kind == 0 && layer != -1) return fail(KV_ERR_INVALID_ARG, "a gather moves every layer");
+    if (layer < -1 || (layer >= 0 && (uint64_t)layer >= g.L))
+        return fail(KV_ERR_OUT_OF_RANGE, "layer %d is outside [-1, %llu)", layer,
+                    (unsigned long long)g.L);
+    const uint32_t nl = layer < 0 ? (uint32_t)g.L : 1u;
+    const uint32_t l0 = layer < 0 ? 0u : (uint32_t)layer;
+    const uint64_t item = (uint64_t)nl * g.C * g.cb;
+    if (buf_bytes / item < n)
+        return fail(KV_ERR_OUT_OF_RANGE, "buffer of %llu bytes cannot hold %u items of %llu bytes",
+                    (unsigned long long)buf_bytes, n, (unsigned long long)item);
+    kv_status st = check_ids(kind == 0 ? "src_pages" : "dst_pages", pages, n, g.P, kind == 1);
+    if (st != KV_OK) return st;
+    const int d = pool->device;
+    DeviceGuard guard(d);
+    st = init_device(d);
+    if (st != KV_OK) return st;
+    DevState &ds = g_dev[d];
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    if (n > 0) {
+        cudaPointerAttributes attr;
+        cudaError_t e = cudaPointerGetAttributes(&attr, buf);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(buffer)");
+        if (attr.type != cudaMemoryTypeDevice || attr.device != d)
+            return fail(KV_ERR_INVALID_ARG, "buffer %p is not device memory of device %d", buf, d);
+        const Side ps = pool_side(*pool);
+        const Side bs = staging_side((char *)buf, g, buf_heads, nl, l0, n);
+        Plan p;
+        st = plan(g, kind == 0 ? ps : bs, kind == 0 ? bs : ps, nl, l0, ds.err_dev, kind == 0, &p);
+        if (st != KV_OK) return st;
+        if (kind == 0) {
+            st = run_moves(p, pages, nullptr, n, default_ctas(ds, false), stream, true);
+        } else {
+            static thread_local std::vector<int32_t> idx;
+            idx.resize(n);
+            for (uint32_t k = 0; k < n; ++k) idx[k] = (int32_t)k;
+            st = run_moves(p, idx.data(), pages, n, default_ctas(ds, false), stream, false);
+        }
+        if (st != KV_OK) return st;
+    }
+    return issue_fence(d, stream, fence);
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+uint32_t kv_abi_version(void) { return KVB_ABI_VERSION; }
+
+const char *kv_last_error(void) { return t_err.c_str(); }
+
+uint64_t kv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+kv_status kv_layout_page_bytes(const kv_layout *layout, uint64_t *out) {
+    if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output pointer is NULL");
+    Geo g{};
+    kv_status st = check_layout(layout, &g);
+    if (st != KV_OK) return st;
+    *out = g.pb;
+    return KV_OK;
+}
+
+kv_status kv_config_get(kv_config *out) {
+    if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output pointer is NULL");
+    std::lock_guard<std::mutex> lk(g_mu);
+    *out = g_cfg;
+    return KV_OK;
+}
+
+kv_status kv_config_set(const kv_config *cfg) {
+    if (cfg == nullptr) return fail(KV_ERR_INVALID_ARG, "config is NULL");
+    if (cfg->mode > KV_MODE_STAGED) return fail(KV_ERR_INVALID_ARG, "unknown mode %u", cfg->mode);
+    if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
+    if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
+        return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_cfg = *cfg;
+    return KV_OK;
+}
+
+kv_status kv_op_validate(const kv_layout *layout, uint32_t num_slots, int kind, const int32_t *a,
+                         const int32_t *b, uint32_t n, int32_t layer) {
+    Geo g{};
+    kv_status st = check_layout(layout, &g);
+    if (st != KV_OK) return st;
+    return check_op(g, num_slots, kind, a, b, n, layer);
+}
+
+kv_status kv_pool_register(const kv_layout *layout, void *base, uint64_t offset,
+                           uint64_t instance_id, uint64_t generation, kv_pool *out) {
+    if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output handle pointer is NULL");
+    Geo g{};
+    kv_status st = check_layout(layout, &g);
+    if (st != KV_OK) return st;
+    if (base == nullptr) return fail(KV_ERR_INVALID_ARG, "pool base is NULL");
+    char *start = (char *)base + offset;
+    if (((uintptr_t)start) % 16 != 0)
+        return fail(KV_ERR_ALIGNMENT, "pool start %p (base + %llu) is not 16-byte aligned",
+                    (void *)start, (unsigned long long)offset);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, start);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(pool)");
+    if (attr.type != cudaMemoryTypeDevice)
+        return fail(KV_ERR_INVALID_ARG, "pool start %p is not device memory", (void *)start);
+    uintptr_t ab;
+    size_t as;
+    {
+        DeviceGuard guard(attr.device);
+        st = address_range(start, &ab, &as);
+    }
+    if (st != KV_OK) return st;
+    const uint64_t nbytes = g.pb * g.P;
+    if ((uintptr_t)start + nbytes > ab + as || (uintptr_t)start + nbytes < (uintptr_t)start)
+        return fail(KV_ERR_OUT_OF_RANGE, "pool of %llu bytes at offset %llu overruns its "
+                    "allocation (%llu bytes from %p)", (unsigned long long)nbytes,
+                    (unsigned long long)((uintptr_t)start - ab), (unsigned long long)as,
+                    (void *)ab);
+    PoolObj *p = new (std::nothrow) PoolObj{g, *layout, start, nbytes, attr.device, instance_id,
+                                            generation, false, std::string()};
+    if (p == nullptr) return fail(KV_ERR_NO_MEMORY, "out of host memory");
+    std::lock_guard<std::mutex> lk(g_mu);
+    const uint64_t id = g_next_handle++;
+    g_pools[id] = p;
+    *out = (kv_pool)(uintptr_t)id;
+    return KV_OK;
+}
+
+kv_status kv_pool_export(kv_pool pool_h, kv_ipc_desc *out) {
+    if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output descriptor pointer is NULL");
+    std::lock_guard<std::mutex> lk(g_mu);
+    PoolObj *p = find_pool(pool_h);
+    if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    DeviceGuard guard(p->device);
+    uintptr_t ab;
+    size_t as;
+    kv_status st = address_range(p->dev, &ab, &as);
+    if (st != KV_OK) return st;
+    cudaIpcMemHandle_t h;
+    cudaError_t e = cudaIpcGetMemHandle(&h, (void *)ab);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaIpcGetMemHandle(allocation base)");
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, p->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    kv_ipc_desc dsc;
+    std::memset(&dsc, 0, sizeof dsc);
+    dsc.magic = KVB_IPC_MAGIC;
+    dsc.version = KVB_ABI_VERSION;
+    static_assert(sizeof(h.reserved) == sizeof(dsc.handle), "IPC handle size");
+    std::memcpy(dsc.handle, h.reserved, sizeof dsc.handle);
+    dsc.alloc_offset = (uint64_t)((uintptr_t)p->dev - ab);
+    dsc.nbytes = p->nbytes;
+    dsc.instance_id = p->instance_id;
+    dsc.generation = p->generation;
+    dsc.exporter_pid = (int64_t)getpid();
+    std::memcpy(dsc.device_uuid, prop.uuid.bytes, sizeof dsc.device_uuid);
+    dsc.layout = p->layout;
+    *out = dsc;
+    return KV_OK;
+}
+
+kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out) {
+    if (desc == nullptr || out == nullptr) return fail(KV_ERR_INVALID_ARG, "NULL argument");
+    if (desc->magic != KVB_IPC_MAGIC || desc->version != KVB_ABI_VERSION)
+        return fail(KV_ERR_INVALID_ARG, "descriptor magic/version %08x/%u not recognised",
+                    desc->magic, desc->version);
+    Geo g{};
+    kv_status st = check_layout(&desc->layout, &g);
+    if (st != KV_OK) return st;
+    if (desc->nbytes != g.pb * g.P)
+        return fail(KV_ERR_LAYOUT, "descriptor nbytes %llu != pool size %llu",
+                    (unsigned long long)desc->nbytes, (unsigned long long)(g.pb * g.P));
+    if (desc->alloc_offset % 16 != 0)
+        return fail(KV_ERR_ALIGNMENT, "alloc_offset %llu is not 16-byte aligned",
+                    (unsigned long long)desc->alloc_offset);
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+    int device = -1;
+    for (int i = 0; i < ndev && device < 0; ++i) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, i) == cudaSuccess &&
+            std::memcmp(prop.uuid.bytes, desc->device_uuid, 16) == 0)
+            device = i;
+    }
+    if (device < 0) return fail(KV_ERR_INVALID_ARG, "no visible device has the descriptor's UUID");
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto fl = g_floor.find(desc->instance_id);
+    if (fl != g_floor.end() && desc->generation < fl->second)
+        return fail(KV_ERR_STALE, "descriptor generation %llu of instance %llu is retired",
+                    (unsigned long long)desc->generation, (unsigned long long)desc->instance_id);
+    const std::string key((const char *)desc->handle, sizeof desc->handle);
+    auto it = g_maps.find(key);
+    void *base = nullptr;
+    if (it != g_maps.end()) {
+        base = it->second.base;
+    } else {
+        DeviceGuard guard(device);
+        cudaIpcMemHandle_t h;
+        std::memcpy(h.reserved, desc->handle, sizeof desc->handle);
+        e = cudaIpcOpenMemHandle(&base, h, cudaIpcMemLazyEnablePeerAccess);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaIpcOpenMemHandle");
+    }
+    char *start = (char *)base + desc->alloc_offset;
+    if (((uintptr_t)start) % 16 != 0) {
+        if (it == g_maps.end()) cudaIpcCloseMemHandle(base);
+        return fail(KV_ERR_ALIGNMENT, "imported pool start %p is not 16-byte aligned", (void *)start);
+    }
+    PoolObj *p = new (std::nothrow) PoolObj{g, desc->layout, start, desc->nbytes, device,
+                                            desc->instance_id, desc->generation, true, key};
+    if (p == nullptr) {
+        if (it == g_maps.end()) cudaIpcCloseMemHandle(base);
+        return fail(KV_ERR_NO_MEMORY, "out of host memory");
+    }
+    if (it != g_maps.end())
+        it->second.refs += 1;
+    else
+        g_maps[key] = Mapping{base, 1, device};
+    const uint64_t id = g_next_handle++;
+    g_pools[id] = p;
+    *out = (kv_pool)(uintptr_t)id;
+    return KV_OK;
+}
+
+kv_status kv_pool_close(kv_pool pool_h) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_pools.find(handle_id(pool_h));
+    if (it == g_pools.end()) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    PoolObj *p = it->second;
+    g_pools.erase(it);
+    kv_status st = KV_OK;
+    if (p->imported) {
+        auto m = g_maps.find(p->ipc_key);
+        if (m != g_maps.end() && --m->second.refs == 0) {
+            DeviceGuard guard(m->second.device);
+            cudaError_t e = cudaIpcCloseMemHandle(m->second.base);
+            g_maps.erase(m);
+            if (e != cudaSuccess) st = cuda_fail(e, "cudaIpcCloseMemHandle (mapping dropped)");
+        }
+    }
+    delete p;
+    return st;
+}
+
+kv_status kv_pool_retire(uint64_t instance_id, uint64_t min_generation) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    uint64_t &f = g_floor[instance_id];
+    f = std::max(f, min_generation);
+    return KV_OK;
+}
+
+kv_status kv_pool_info(kv_pool pool_h, kv_layout *layout, void **dev_ptr, uint64_t *nbytes) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    PoolObj *p = find_pool(pool_h);
+    if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    if (layout) *layout = p->layout;
+    if (dev_ptr) *dev_ptr = p->dev;
+    if (nbytes) *nbytes = p->nbytes;
+    return KV_OK;
+}
+
+kv_status kv_host_register(void *host, uint64_t bytes, uint32_t num_slots, uint32_t host_heads,
+                           const kv_layout *pool_layout, kv_host *out) {
+    if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output handle pointer is NULL");
+    Geo g{};
+    kv_status st = check_layout(pool_layout, &g);
+    if (st != KV_OK) return st;
+    if (host_heads > KV_HND) return fail(KV_ERR_LAYOUT, "unknown host head order %u", host_heads);
+    if (host == nullptr || num_slots == 0)
+        return fail(KV_ERR_INVALID_ARG, "host tier pointer is NULL or has no slots");
+    if (((uintptr_t)host) % 16 != 0)
+        return fail(KV_ERR_ALIGNMENT, "host tier %p is not 16-byte aligned", host);
+    uint64_t need;
+    if (!mul_ok(g.pb, num_slots, 1ull << 62, &need) || bytes < need)
+        return fail(KV_ERR_OUT_OF_RANGE, "host tier of %llu bytes cannot hold %u slots of %llu bytes",
+                    (unsigned long long)bytes, num_slots, (unsigned long long)g.pb);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, host);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(host tier)");
+    if (attr.type != cudaMemoryTypeHost)
+        return fail(KV_ERR_INVALID_ARG, "host tier %p is not page-locked host memory known to CUDA",
+                    host);
+    void *dv = attr.devicePointer;
+    if (dv == nullptr) {
+        e = cudaHostGetDevicePointer(&dv, host, 0);
+        if (e != cudaSuccess || dv == nullptr)
+            return fail(KV_ERR_INVALID_ARG, "host tier %p is not mapped into the device", host);
+    }
+    HostObj *h = new (std::nothrow) HostObj{g, host_heads, num_slots, (char *)host, (char *)dv, bytes};
+    if (h == nullptr) return fail(KV_ERR_NO_MEMORY, "out of host memory");
+    std::lock_guard<std::mutex> lk(g_mu);
+    const uint64_t id = g_next_handle++;
+    g_hosts[id] = h;
+    *out = (kv_host)(uintptr_t)id;
+    return KV_OK;
+}
+
+kv_status kv_host_close(kv_host host_h) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_hosts.find(handle_id(host_h));
+    if (it == g_hosts.end()) return fail(KV_ERR_CLOSED, "host handle is closed or unknown");
+    delete it->second;
+    g_hosts.erase(it);
+    return KV_OK;
+}
+
+kv_status kv_backup(kv_pool pool, kv_host host, const int32_t *src_pages,
+                    const int32_t *host_slots, uint32_t n, void *stream, kv_fence *fence) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue(pool, host, 0, src_pages, host_slots, n, -1, stream, fence);
+}
+
+kv_status kv_restore(kv_pool pool, kv_host host, const int32_t *host_slots,
+                     const int32_t *dst_pages, uint32_t n, int32_t layer, void *stream,
+                     kv_fence *fence) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue(pool, host, 1, host_slots, dst_pages, n, layer, stream, fence);
+}
+
+kv_status kv_device_gather(kv_pool pool, void *buf, uint64_t buf_bytes, uint32_t buf_heads,
+                           const int32_t *src_pages, uint32_t n, void *stream, kv_fence *fence) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue_device(pool, buf, buf_bytes, buf_heads, 0, src_pages, n, -1, stream, fence);
+}
+
+kv_status kv_device_scatter(kv_pool pool, const void *buf, uint64_t buf_bytes, uint32_t buf_heads,
+                            const int32_t *dst_pages, uint32_t n, int32_t layer, void *stream,
+                            kv_fence *fence) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue_device(pool, (void *)buf, buf_bytes, buf_heads, 1, dst_pages, n, layer, stream,
+                        fence);
+}
+
+kv_status kv_fence_query(kv_fence f) {
+    bool done = false;
+    int d = 0, k = 0;
+    kv_status st = fence_state(f, &done, &d, &k);
+    if (st != KV_OK) return st;
+    if (g_dev[d].err != nullptr && __atomic_load_n(g_dev[d].err, __ATOMIC_ACQUIRE) != 0)
+        return fail(KV_ERR_OUT_OF_RANGE, "a transfer kernel met an out-of-range id and skipped it");
+    return done ? KV_OK : KV_ERR_TIMEOUT;
+}
+
+kv_status kv_fence_wait(kv_fence f, uint64_t timeout_ns) {
+    const double deadline = now_ns() + (double)timeout_ns;
+    int spins = 0;
+    for (;;) {
+        kv_status st = kv_fence_query(f);
+        if (st != KV_ERR_TIMEOUT) return st;
+        if (now_ns() >= deadline)
+            return fail(KV_ERR_TIMEOUT, "fence %llu not complete after %llu ns",
+                        (unsigned long long)f, (unsigned long long)timeout_ns);
+        if (++spins < 64) {
+            sched_yield();
+        } else {
+            timespec ts{0, 20000};   // 20 us
+            nanosleep(&ts, nullptr);
+        }
+    }
+}
+
+kv_status kv_fence_stream_wait(kv_fence f, void *stream) {
+    bool done = false;
+    int d = 0, k = 0;
+    kv_status st = fence_state(f, &done, &d, &k);
+    if (st != KV_OK) return st;
+    if (done) return KV_OK;
+    std::lock_guard<std::mutex> lk(g_mu);
+    // The slot's event is this fence's, or a later one recorded only after this
+    // fence completed (issue_fence waits before reusing a slot): never too early.
+    DeviceGuard guard(d);
+    cudaError_t e = cudaStreamWaitEvent((cudaStream_t)stream, g_dev[d].ev[k], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fence)");
+    return KV_OK;
+}
+
+}  // extern "C"

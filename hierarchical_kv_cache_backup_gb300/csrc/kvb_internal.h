@@ -1,0 +1,67 @@
+// kvb_internal.h -- declarations shared by the host engine (kvb_api.cpp) and
+// the sm_103a kernels (kvb_kernels.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvb {
+
+// Invariant-divisor division by multiply-high and shift (Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication", PLDI
+// 1994, unsigned case with N = 32): for d >= 1, l = ceil(log2 d),
+// m = floor(2^32 (2^l - d) / d) + 1, and n / d = (umulhi(n, m) + n) >> l,
+// with the addition done in 64 bits.  Exact for every 32-bit n.
+struct FastDiv {
+    uint32_t d, m, s, pad;
+};
+FastDiv make_fastdiv(uint32_t d);   // host; d >= 1
+
+// One side of a move: where unit vectors of chunk (id, layer, comp) live.
+// A "chunk" is the T*H*B bytes of one (page or slot, layer, component).
+//   chunk address = base + id*s_id + layer*s_l + comp*s_c
+//   inside a chunk: NHD [T][H] or HND [H][T] vectors of B bytes.
+struct Side {
+    uint64_t base;      // device-visible address of the side's byte 0
+    uint64_t s_id;      // bytes between consecutive ids (pages or slots)
+    uint64_t s_l;       // bytes between consecutive layers
+    uint64_t s_c;       // bytes between components
+    uint32_t hnd;       // head order inside a chunk: 0 = NHD, 1 = HND
+    uint32_t id_limit;  // ids must be below this (checked again on the GPU)
+};
+
+// Kernel-parameter budget: the ids of one launch travel inside the launch
+// itself (sm_70+ accepts up to 32,764 bytes of parameters), so no device
+// buffer, copy or ring is needed for them.
+constexpr int kMaxItems = 2048;     // (a, b) id pairs per launch
+constexpr int kSegPieces = 256;     // 16-byte pieces a warp moves per segment (4 KiB)
+constexpr int kMoveThreads = 256;   // threads per CTA of the move kernel
+
+struct MoveDesc {
+    Side src, dst;
+    uint32_t n;          // items in this launch
+    uint32_t nl;         // layers per item
+    uint32_t l0;         // first layer
+    uint32_t C;          // components
+    uint32_t cb16;       // 16-byte pieces per chunk (T*H*B/16)
+    uint32_t segs;       // segments per chunk
+    uint32_t total_segs; // n * nl * C * segs (< 2^32)
+    uint32_t H, T, B16;  // heads, tokens, 16-byte pieces per head vector
+    uint32_t transpose;  // 1 when the two sides' head orders differ (H, T > 1)
+    uint32_t iter_dst;   // transpose only: 1 = walk destination order
+    FastDiv div_segs, div_lc, div_c, div_b16, div_T, div_H;
+    uint32_t *err;       // device-visible word set to 1 if a kernel meets a bad id
+};
+
+struct MoveIds {
+    int32_t a[kMaxItems];   // source ids (pages for backup, slots for restore)
+    int32_t b[kMaxItems];   // destination ids
+};
+
+// Launch the gather/scatter kernel on `stream` with `ctas` CTAs.
+cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
+// Launch the completion marker: stores `seq` to `word` (system scope, release)
+// once everything before it on `stream` has finished.
+cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream);
+
+}  // namespace kvb

@@ -1,0 +1,180 @@
+// kvb_kernels.cu -- sm_103a kernels of the KV backup / restore engine.
+//
+// kv_move: the one data-movement kernel.  It copies whole KV "chunks" (the
+// T*H*B bytes of one page-or-slot, layer and component) from a source side to
+// a destination side, optionally permuting the head order inside each chunk
+// (HND <-> NHD).  Both sides are described by strides (kvb_internal.h), so
+// the same kernel serves
+//   - backup, zero-copy : pool (HBM)          -> host tier (mapped pinned memory)
+//   - restore, zero-copy: host tier (mapped)  -> pool (HBM)
+//   - staged gather     : pool                -> device staging buffer (HBM only)
+//   - staged scatter    : device staging      -> pool
+// This is the BACKUP / RESTORE data movement of "[RFC][HiCache] Out-of-process
+// HiCache data plane with device-memory IPC" (§Device IPC data path), with
+// the layer restriction of "[PP + HiCache] Add PP Prefetch Tickets" (§PP
+// Prefetch Ticket Path, layer-wise H2D) and the HND pool of "LMCache
+// RawCudaIPCWrapper深度解析" (§在项目中的实际接入方式).  Payload moves as raw
+// 16-byte integer vectors: no float type touches it (§uint8字节往返).
+//
+// Work split: the op is a flat list of 4 KiB warp segments (chunk, segment);
+// warps stride over it.  A segment's id lookup and address math happen once;
+// then each lane issues eight independent 16-byte loads (4 KiB in flight per
+// warp) followed by eight stores, so consecutive lanes touch consecutive
+// 16-byte pieces: every warp-wide access covers 512 contiguous bytes, or B-byte
+// runs (B >= 16, usually 128-576) when a head permutation is fused in.
+#include "kvb_internal.h"
+
+namespace kvb {
+
+namespace {
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    const uint32_t t = __umulhi(n, f.m);
+    return (uint32_t)(((uint64_t)t + n) >> f.s);
+}
+
+// 16-byte load that bypasses L1 (each byte is read exactly once).
+__device__ __forceinline__ uint4 load16(const char *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// 16-byte streaming store (evict-first: the data is not read again soon).
+__device__ __forceinline__ void store16(char *p, const uint4 &v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Piece index on the other side of a head-order permutation.  q is a 16-byte
+// piece of a chunk laid out with head order `from_hnd`; returns the index of
+// the same piece in the other order.
+__device__ __forceinline__ uint32_t permute_piece(uint32_t q, uint32_t from_hnd,
+                                                  const MoveDesc &d) {
+    const uint32_t j = fdiv(q, d.div_b16);      // head vector within the chunk
+    const uint32_t r = q - j * d.B16;           // piece within the head vector
+    uint32_t h, t;
+    if (from_hnd) {                              // j = h*T + t
+        h = fdiv(j, d.div_T);
+        t = j - h * d.T;
+        return (t * d.H + h) * d.B16 + r;        // -> NHD
+    }
+    t = fdiv(j, d.div_H);                        // j = t*H + h
+    h = j - t * d.H;
+    return (h * d.T + t) * d.B16 + r;            // -> HND
+}
+
+constexpr int kUnroll = kSegPieces / 32;  // 16-byte pieces per lane per segment
+
+template <bool kTranspose>
+__global__ void __launch_bounds__(kMoveThreads, 4)
+    kv_move_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ MoveIds ids) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    const uint32_t lc_per_item = d.nl * d.C;
+
+    for (uint32_t w = warp; w < d.total_segs; w += nwarps) {
+        const uint32_t chunk = fdiv(w, d.div_segs);
+        const uint32_t seg = w - chunk * d.segs;
+        const uint32_t item = fdiv(chunk, d.div_lc);
+        const uint32_t lc = chunk - item * lc_per_item;
+        const uint32_t lr = fdiv(lc, d.div_c);
+        const uint32_t c = lc - lr * d.C;
+        const uint64_t l = d.l0 + lr;
+        const uint32_t ia = (uint32_t)ids.a[item];
+        const uint32_t ib = (uint32_t)ids.b[item];
+        if (ia >= d.src.id_limit || ib >= d.dst.id_limit) {
+            // Host validation makes this unreachable; never touch memory for a bad id.
+            if (lane == 0 && d.err != nullptr) *(volatile uint32_t *)d.err = 1u;
+            continue;
+        }
+        const char *sp = reinterpret_cast<const char *>(d.src.base + ia * d.src.s_id +
+                                                        l * d.src.s_l + c * d.src.s_c);
+        char *dp = reinterpret_cast<char *>(d.dst.base + ib * d.dst.s_id + l * d.dst.s_l +
+                                            c * d.dst.s_c);
+        const uint32_t q0 = seg * (uint32_t)kSegPieces;
+        const uint32_t qn = min((uint32_t)kSegPieces, d.cb16 - q0);
+
+        uint4 v[kUnroll];
+        if (!kTranspose) {
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint32_t k = u * 32u + lane;
+                if (k < qn) v[u] = load16(sp + (uint64_t)(q0 + k) * 16u);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint32_t k = u * 32u + lane;
+                if (k < qn) store16(dp + (uint64_t)(q0 + k) * 16u, v[u]);
+            }
+        } else if (d.iter_dst) {
+            // walk destination pieces in order: contiguous stores, B-byte-run loads
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint32_t k = u * 32u + lane;
+                if (k < qn) {
+                    const uint32_t qs = permute_piece(q0 + k, d.dst.hnd, d);
+                    v[u] = load16(sp + (uint64_t)qs * 16u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint32_t k = u * 32u + lane;
+                if (k < qn) store16(dp + (uint64_t)(q0 + k) * 16u, v[u]);
+            }
+        } else {
+            // walk source pieces in order: contiguous loads, B-byte-run stores
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint32_t k = u * 32u + lane;
+                if (k < qn) v[u] = load16(sp + (uint64_t)(q0 + k) * 16u);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const uint32_t k = u * 32u + lane;
+                if (k < qn) {
+                    const uint32_t qd = permute_piece(q0 + k, d.src.hnd, d);
+                    store16(dp + (uint64_t)qd * 16u, v[u]);
+                }
+            }
+        }
+    }
+}
+
+__global__ void kv_mark_kernel(unsigned long long *word, unsigned long long seq) {
+    if (threadIdx.x == 0) {
+        __threadfence_system();
+        asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(word), "l"(seq) : "memory");
+    }
+}
+
+}  // namespace
+
+FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{d, 0u, 0u, 0u};
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d) ++l;
+    const uint64_t two32 = 1ull << 32;
+    f.m = (uint32_t)((two32 * ((1ull << l) - d)) / d + 1ull);
+    f.s = l;
+    return f;
+}
+
+cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
+    if (d.transpose)
+        kv_move_kernel<true><<<ctas, kMoveThreads, 0, stream>>>(d, ids);
+    else
+        kv_move_kernel<false><<<ctas, kMoveThreads, 0, stream>>>(d, ids);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream) {
+    kv_mark_kernel<<<1, 32, 0, stream>>>(word, seq);
+    return cudaGetLastError();
+}
+
+}  // namespace kvb

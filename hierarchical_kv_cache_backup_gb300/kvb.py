@@ -1,0 +1,284 @@
+"""Thin ctypes binding of the C ABI in include/kvb.h (argument marshalling only).
+
+Every function has the C name.  Pointers are Python ints (``tensor.data_ptr()``),
+streams are ``torch.cuda.Stream.cuda_stream`` ints (or None for the legacy
+default stream), id lists are anything ``numpy.asarray(..., int32)`` accepts.
+A non-OK status raises :class:`KvError` carrying the status and the library's
+message; ``kv_fence_query`` returns its status instead (TIMEOUT = not yet).
+
+The library must have been built (``python -m hierarchical_kv_cache_backup_gb300.build``
+or ``__graft_entry__.build()``); importing this module without it fails loudly.
+There is no fallback path of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libkvb.so")
+
+KV_OK = 0
+KV_ERR_INVALID_ARG = 1
+KV_ERR_OUT_OF_RANGE = 2
+KV_ERR_DUPLICATE = 3
+KV_ERR_ALIGNMENT = 4
+KV_ERR_LAYOUT = 5
+KV_ERR_STALE = 6
+KV_ERR_TIMEOUT = 7
+KV_ERR_CUDA = 8
+KV_ERR_NO_MEMORY = 9
+KV_ERR_CLOSED = 10
+STATUS_NAMES = {v: k for k, v in dict(globals()).items() if k.startswith("KV_OK") or k.startswith("KV_ERR_")}
+
+KV_LAYER_FIRST, KV_PAGE_FIRST = 0, 1
+KV_NHD, KV_HND = 0, 1
+KV_MODE_ZERO_COPY, KV_MODE_STAGED = 0, 1
+KVB_IPC_MAGIC = 0x4B564231
+
+# the symbols include/kvb.h declares
+EXPORTS = ("kv_pool_register", "kv_pool_export", "kv_pool_import", "kv_pool_close",
+           "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
+           "kv_restore", "kv_device_gather", "kv_device_scatter", "kv_op_validate", "kv_fence_query", "kv_fence_wait",
+           "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
+           "kv_launch_count", "kv_last_error", "kv_abi_version")
+
+
+class KvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+
+
+class kv_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint32) for n in ("num_layers", "num_comps", "num_pages",
+                                               "page_tokens", "num_heads", "head_bytes", "order",
+                                               "heads", "elem_bytes", "reserved")]
+
+
+class kv_ipc_desc(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32),
+                ("handle", ctypes.c_uint8 * 64), ("alloc_offset", ctypes.c_uint64),
+                ("nbytes", ctypes.c_uint64), ("instance_id", ctypes.c_uint64),
+                ("generation", ctypes.c_uint64), ("exporter_pid", ctypes.c_int64),
+                ("device_uuid", ctypes.c_uint8 * 16), ("layout", kv_layout)]
+
+
+class kv_config(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_uint32), ("max_ctas", ctypes.c_uint32),
+                ("staging_bytes", ctypes.c_uint64)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                          "(python -m hierarchical_kv_cache_backup_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    u32, u64, i32, vp = ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int32, ctypes.c_void_p
+    st = ctypes.c_int
+    P = ctypes.POINTER
+    sig = {
+        "kv_pool_register": (st, [P(kv_layout), vp, u64, u64, u64, P(vp)]),
+        "kv_pool_export": (st, [vp, P(kv_ipc_desc)]),
+        "kv_pool_import": (st, [P(kv_ipc_desc), P(vp)]),
+        "kv_pool_close": (st, [vp]),
+        "kv_pool_retire": (st, [u64, u64]),
+        "kv_pool_info": (st, [vp, P(kv_layout), P(vp), P(u64)]),
+        "kv_host_register": (st, [vp, u64, u32, u32, P(kv_layout), P(vp)]),
+        "kv_host_close": (st, [vp]),
+        "kv_backup": (st, [vp, vp, vp, vp, u32, vp, P(u64)]),
+        "kv_restore": (st, [vp, vp, vp, vp, u32, i32, vp, P(u64)]),
+        "kv_device_gather": (st, [vp, vp, u64, u32, vp, u32, vp, P(u64)]),
+        "kv_device_scatter": (st, [vp, vp, u64, u32, vp, u32, i32, vp, P(u64)]),
+        "kv_op_validate": (st, [P(kv_layout), u32, ctypes.c_int, vp, vp, u32, i32]),
+        "kv_fence_query": (st, [u64]),
+        "kv_fence_wait": (st, [u64, u64]),
+        "kv_fence_stream_wait": (st, [u64, vp]),
+        "kv_config_get": (st, [P(kv_config)]),
+        "kv_config_set": (st, [P(kv_config)]),
+        "kv_layout_page_bytes": (st, [P(kv_layout), P(u64)]),
+        "kv_launch_count": (u64, []),
+        "kv_last_error": (ctypes.c_char_p, []),
+        "kv_abi_version": (u32, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int):
+    if status != KV_OK:
+        raise KvError(status, _lib.kv_last_error().decode(errors="replace"))
+
+
+def _ids(x):
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+    return a, (a.ctypes.data if a.size else None)
+
+
+def make_layout(L, C, P, T, H, B, order=KV_LAYER_FIRST, heads=KV_NHD, elem_bytes=2) -> kv_layout:
+    return kv_layout(L, C, P, T, H, B, order, heads, elem_bytes, 0)
+
+
+# ------------------------------------------------------------------- pools
+
+def kv_pool_register(layout: kv_layout, base: int, offset: int = 0, instance_id: int = 0,
+                     generation: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.kv_pool_register(ctypes.byref(layout), base, offset, instance_id, generation,
+                                 ctypes.byref(out)))
+    return out.value
+
+
+def kv_pool_export(pool: int) -> kv_ipc_desc:
+    d = kv_ipc_desc()
+    _check(_lib.kv_pool_export(pool, ctypes.byref(d)))
+    return d
+
+
+def kv_pool_import(desc: kv_ipc_desc) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.kv_pool_import(ctypes.byref(desc), ctypes.byref(out)))
+    return out.value
+
+
+def kv_pool_close(pool: int) -> None:
+    _check(_lib.kv_pool_close(pool))
+
+
+def kv_pool_retire(instance_id: int, min_generation: int) -> None:
+    _check(_lib.kv_pool_retire(instance_id, min_generation))
+
+
+def kv_pool_info(pool: int):
+    lay, ptr, nb = kv_layout(), ctypes.c_void_p(), ctypes.c_uint64()
+    _check(_lib.kv_pool_info(pool, ctypes.byref(lay), ctypes.byref(ptr), ctypes.byref(nb)))
+    return lay, ptr.value, nb.value
+
+
+def desc_to_bytes(d: kv_ipc_desc) -> bytes:
+    return ctypes.string_at(ctypes.addressof(d), ctypes.sizeof(d))
+
+
+def desc_from_bytes(b: bytes) -> kv_ipc_desc:
+    if len(b) != ctypes.sizeof(kv_ipc_desc):
+        raise ValueError(f"descriptor must be {ctypes.sizeof(kv_ipc_desc)} bytes, got {len(b)}")
+    return kv_ipc_desc.from_buffer_copy(b)
+
+
+# --------------------------------------------------------------- host tier
+
+def kv_host_register(host: int, nbytes: int, num_slots: int, host_heads: int,
+                     pool_layout: kv_layout) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.kv_host_register(host, nbytes, num_slots, host_heads, ctypes.byref(pool_layout),
+                                 ctypes.byref(out)))
+    return out.value
+
+
+def kv_host_close(host: int) -> None:
+    _check(_lib.kv_host_close(host))
+
+
+# -------------------------------------------------------------- operations
+
+def kv_backup(pool: int, host: int, src_pages, host_slots, stream=None) -> int:
+    a, pa = _ids(src_pages)
+    b, pb = _ids(host_slots)
+    if a.size != b.size:
+        raise ValueError("src_pages and host_slots differ in length")
+    f = ctypes.c_uint64()
+    _check(_lib.kv_backup(pool, host, pa, pb, a.size, stream, ctypes.byref(f)))
+    return f.value
+
+
+def kv_restore(pool: int, host: int, host_slots, dst_pages, layer: int = -1, stream=None) -> int:
+    a, pa = _ids(host_slots)
+    b, pb = _ids(dst_pages)
+    if a.size != b.size:
+        raise ValueError("host_slots and dst_pages differ in length")
+    f = ctypes.c_uint64()
+    _check(_lib.kv_restore(pool, host, pa, pb, a.size, layer, stream, ctypes.byref(f)))
+    return f.value
+
+
+def kv_device_gather(pool: int, buf: int, buf_bytes: int, buf_heads: int, src_pages,
+                     stream=None) -> int:
+    a, pa = _ids(src_pages)
+    f = ctypes.c_uint64()
+    _check(_lib.kv_device_gather(pool, buf, buf_bytes, buf_heads, pa, a.size, stream,
+                                 ctypes.byref(f)))
+    return f.value
+
+
+def kv_device_scatter(pool: int, buf: int, buf_bytes: int, buf_heads: int, dst_pages,
+                      layer: int = -1, stream=None) -> int:
+    a, pa = _ids(dst_pages)
+    f = ctypes.c_uint64()
+    _check(_lib.kv_device_scatter(pool, buf, buf_bytes, buf_heads, pa, a.size, layer, stream,
+                                  ctypes.byref(f)))
+    return f.value
+
+
+def kv_op_validate(layout: kv_layout, num_slots: int, kind: int, a, b, layer: int = -1) -> int:
+    """Returns the status (does not raise)."""
+    a_, pa = _ids(a)
+    b_, pb = _ids(b)
+    n = min(a_.size, b_.size)
+    return _lib.kv_op_validate(ctypes.byref(layout), num_slots, kind, pa, pb, n, layer)
+
+
+# ------------------------------------------------------------------ fences
+
+def kv_fence_query(fence: int) -> int:
+    return _lib.kv_fence_query(fence)
+
+
+def kv_fence_wait(fence: int, timeout_ns: int = 60_000_000_000) -> None:
+    _check(_lib.kv_fence_wait(fence, timeout_ns))
+
+
+def kv_fence_stream_wait(fence: int, stream=None) -> None:
+    _check(_lib.kv_fence_stream_wait(fence, stream))
+
+
+# --------------------------------------------------------------- utilities
+
+def kv_config_get() -> kv_config:
+    c = kv_config()
+    _check(_lib.kv_config_get(ctypes.byref(c)))
+    return c
+
+
+def kv_config_set(mode: int = KV_MODE_ZERO_COPY, max_ctas: int = 0, staging_bytes: int = 0):
+    _check(_lib.kv_config_set(ctypes.byref(kv_config(mode, max_ctas, staging_bytes))))
+
+
+def kv_layout_page_bytes(layout: kv_layout) -> int:
+    out = ctypes.c_uint64()
+    _check(_lib.kv_layout_page_bytes(ctypes.byref(layout), ctypes.byref(out)))
+    return out.value
+
+
+def kv_launch_count() -> int:
+    return _lib.kv_launch_count()
+
+
+def kv_last_error() -> str:
+    return _lib.kv_last_error().decode(errors="replace")
+
+
+def kv_abi_version() -> int:
+    return _lib.kv_abi_version()
+
+
+def library():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib

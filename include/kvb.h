@@ -1,0 +1,275 @@
+/*
+ * kvb.h -- C ABI of the GB300 paged KV-cache backup / restore engine.
+ *
+ * The engine moves KV-cache pages between a GPU KV pool (device memory) and a
+ * pinned host KV tier, in both directions, converting between the pool's
+ * layout and the host tier's page-contiguous layout on the way.  Payload is
+ * opaque bytes: fp16, bf16 and fp8_e4m3 KV all take the same path.
+ *
+ * Pages this interface restates (cited by title and section):
+ *   [RFC] "[Feature] [RFC] [HiCache] Out-of-process HiCache data plane with
+ *         device-memory IPC": §Device IPC data path (REGISTER_KV_POOL, BACKUP,
+ *         RESTORE descriptors; export / import / close of device memory;
+ *         export / import / wait of fences), §Ownership, §Failure and
+ *         lifecycle handling.
+ *   [PR]  "[PP + HiCache] Add PP Prefetch Tickets for eager cross-stage
+ *         storage prefetch": §PP Prefetch Ticket Path (layer-wise H2D ahead
+ *         of each layer's forward).
+ *   [LMC] "LMCacheRawCudaIPCWrapper深度解析：基于驱动级 CUDA IPC 共享 PyTorch
+ *         之外的 KV Cache": §共享与重建的完整链路 (allocation base + byte
+ *         offset), §uint8字节往返 (dtype-neutral bytes), §发送端校验 (reject,
+ *         never silently copy), §重建生命周期与引用计数 (refcounted mappings,
+ *         close logs but never throws), §在项目中的实际接入方式 (TRT-LLM pool
+ *         [NB, NL, 2, NH*BS*HS], kv_layout = HND).
+ *
+ * Conventions for every call:
+ *   - Status codes only.  Nothing aborts, throws or traps across this ABI.
+ *     A call that returns an error has had no side effect: validation runs
+ *     before anything is enqueued ([LMC] §发送端校验).  kv_last_error() gives
+ *     a readable message (thread-local) for the last failing call.
+ *   - Device pointers are plain CUDA device addresses; host pointers are
+ *     plain host addresses.  Streams are cudaStream_t values passed as void*
+ *     (NULL = the legacy default stream).
+ *   - Page IDs and host slots are int32 arrays in HOST memory.  The call
+ *     copies them before returning, so the caller may reuse them at once.
+ *   - Ownership ([RFC] §Ownership): the caller owns the device pool
+ *     allocation, its page allocator and page lifetimes, the pinned host
+ *     memory and the streams.  The library owns IPC mappings, staging
+ *     buffers, fence words and events.  Pool and host bytes named by an
+ *     operation must not be touched by the caller until its fence completes.
+ *
+ * Unit and layouts.  A unit is the B-byte head vector of (page p, layer l,
+ * component c, token t, head h); B = head_dim x element bytes.  With L layers,
+ * C components (2 = K,V; 1 = MLA latent), P pages, T tokens per page and H
+ * heads, the pool and the host tier are these row-major arrays of units:
+ *     KV_LAYER_FIRST + KV_NHD : [L][C][P][T][H]
+ *     KV_LAYER_FIRST + KV_HND : [L][C][P][H][T]
+ *     KV_PAGE_FIRST  + KV_NHD : [P][L][C][T][H]
+ *     KV_PAGE_FIRST  + KV_HND : [P][L][C][H][T]   (the TRT-LLM 6-D view
+ *                                [NB, NL, 2, NH, BS, HS] of [LMC])
+ *     host tier, NHD / HND    : [S][L][C][T][H] / [S][L][C][H][T]
+ * so one host slot holds one whole page contiguously (L*C*T*H*B bytes).
+ */
+#ifndef KVB_H
+#define KVB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVB_ABI_VERSION 1u
+
+#if defined(__GNUC__)
+#define KVB_API __attribute__((visibility("default")))
+#else
+#define KVB_API
+#endif
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,   /* null handle/pointer, bad enum, bad size     */
+    KV_ERR_OUT_OF_RANGE = 2,  /* page / slot / layer outside the pool / tier */
+    KV_ERR_DUPLICATE = 3,     /* one call writes one page or slot twice      */
+    KV_ERR_ALIGNMENT = 4,     /* B or the pool / host start not 16-B aligned */
+    KV_ERR_LAYOUT = 5,        /* layout invalid, or pool and tier disagree   */
+    KV_ERR_STALE = 6,         /* pool generation retired ([RFC] lifecycle)   */
+    KV_ERR_TIMEOUT = 7,       /* fence not complete (query) / not in time    */
+    KV_ERR_CUDA = 8,          /* a CUDA call failed; see kv_last_error()     */
+    KV_ERR_NO_MEMORY = 9,     /* library could not allocate its resources    */
+    KV_ERR_CLOSED = 10        /* handle already closed                       */
+} kv_status;
+
+typedef enum { KV_LAYER_FIRST = 0, KV_PAGE_FIRST = 1 } kv_order;
+typedef enum { KV_NHD = 0, KV_HND = 1 } kv_heads;
+
+/* Pool geometry (the `layout` argument of REGISTER_KV_POOL, [RFC] §Device IPC
+ * data path).  Fixed-size POD. */
+typedef struct {
+    uint32_t num_layers;   /* L                                               */
+    uint32_t num_comps;    /* C: 2 = K and V, 1 = MLA latent                  */
+    uint32_t num_pages;    /* P                                               */
+    uint32_t page_tokens;  /* T                                               */
+    uint32_t num_heads;    /* H                                               */
+    uint32_t head_bytes;   /* B = head_dim x element bytes; multiple of 16    */
+    uint32_t order;        /* kv_order of the device pool                     */
+    uint32_t heads;        /* kv_heads of the device pool                     */
+    uint32_t elem_bytes;   /* informational only: payload is opaque bytes     */
+    uint32_t reserved;     /* must be 0                                       */
+} kv_layout;
+
+typedef struct kv_pool_s *kv_pool;
+typedef struct kv_host_s *kv_host;
+typedef uint64_t kv_fence;   /* 0 is never a valid fence */
+
+/* IPC descriptor of a pool ([RFC] §Device IPC data path REGISTER_KV_POOL with
+ * instance_id / generation / device identity; [LMC] §共享与重建的完整链路
+ * sender step 5: handle of the allocation base, byte offset, size, device
+ * UUID).  Fixed-size POD: send its bytes over any channel. */
+typedef struct {
+    uint32_t magic;            /* KVB_IPC_MAGIC                                */
+    uint32_t version;          /* KVB_ABI_VERSION                              */
+    uint8_t handle[64];        /* cudaIpcMemHandle_t of the allocation base    */
+    uint64_t alloc_offset;     /* pool start minus allocation base, in bytes   */
+    uint64_t nbytes;           /* pool bytes: P x L x C x T x H x B            */
+    uint64_t instance_id;      /* exporter instance identity                   */
+    uint64_t generation;       /* pool generation                              */
+    int64_t exporter_pid;      /* exporter process identity                    */
+    uint8_t device_uuid[16];   /* device identity (resolved to an ordinal)     */
+    kv_layout layout;
+} kv_ipc_desc;
+#define KVB_IPC_MAGIC 0x4B564231u /* "KVB1" */
+
+/* Transfer modes.  ZERO_COPY: one kernel moves every byte between HBM and the
+ * mapped pinned host tier over the host link.  STAGED: a kernel gathers /
+ * scatters between the pool and a device staging buffer in host layout, and
+ * the copy engine moves the staging buffer to / from the host tier. */
+typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1 } kv_mode;
+
+typedef struct {
+    uint32_t mode;           /* kv_mode                                         */
+    uint32_t max_ctas;       /* CTA cap of the transfer kernel; 0 = default     */
+    uint64_t staging_bytes;  /* STAGED: device staging bytes; 0 = default       */
+} kv_config;
+
+/* ------------------------------------------------------------------ pools */
+
+/* REGISTER_KV_POOL ([RFC] §Device IPC data path).  Registers a pool the
+ * caller allocated: it starts `offset` bytes after device pointer `base`.
+ * Checks: layout valid (dims >= 1, B % 16 == 0, enums known, sizes fit in
+ * 64 bits), base+offset 16-B aligned, and the whole pool inside one device
+ * allocation of the current device.  The library does not own the memory.
+ * `instance_id` and `generation` identify the registering process and pool
+ * version ([RFC] §Failure and lifecycle handling).
+ * Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, CUDA, NO_MEMORY. */
+KVB_API kv_status kv_pool_register(const kv_layout *layout, void *base, uint64_t offset,
+                           uint64_t instance_id, uint64_t generation, kv_pool *out);
+
+/* Export ([RFC] DeviceMemoryIPC "export allocation"; [LMC] §共享与重建的完整链路
+ * sender steps 3-5): finds the allocation base of the pool start, takes the
+ * IPC handle of that base and records the pool's byte offset from it.  Fails
+ * (CUDA) for memory CUDA IPC cannot share; there is no alternate path
+ * ([LMC] §为什么不做_share_cuda_回退).  Errors: INVALID_ARG, CLOSED, CUDA. */
+KVB_API kv_status kv_pool_export(kv_pool pool, kv_ipc_desc *out);
+
+/* Import ([RFC] DeviceMemoryIPC "import allocation"; [LMC] §共享与重建的完整链路
+ * receiver steps 1-3): device UUID -> ordinal; one mapping per (process,
+ * allocation), refcounted by handle bytes; cudaIpcOpenMemHandle with lazy
+ * peer access when the allocation is not yet mapped; pool = mapped base +
+ * alloc_offset.  Must run in a process other than the exporter.  A
+ * descriptor whose generation is below the retired floor of its instance is
+ * refused with STALE.  Errors: INVALID_ARG, LAYOUT, ALIGNMENT, STALE, CUDA,
+ * NO_MEMORY. */
+KVB_API kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out);
+
+/* Close ([RFC] DeviceMemoryIPC "close mapping"; [LMC] §重建生命周期与引用计数):
+ * releases the handle; for an imported pool, drops one reference of its
+ * mapping and unmaps on the last one.  Teardown always completes: an unmap
+ * failure is reported (CUDA) after the handle is gone.  Closing twice gives
+ * CLOSED.  Operations still in flight on the pool must have completed. */
+KVB_API kv_status kv_pool_close(kv_pool pool);
+
+/* Retire every generation below `min_generation` of `instance_id` ([RFC]
+ * §Failure and lifecycle handling: a restarted scheduler's older generation
+ * must not be used).  Later backup / restore on such pools, and imports of
+ * such descriptors, fail with STALE.  Floors only rise. */
+KVB_API kv_status kv_pool_retire(uint64_t instance_id, uint64_t min_generation);
+
+/* Device address of the pool's first byte (base + offset, or mapped base +
+ * alloc_offset) and its byte size.  Either output may be NULL. */
+KVB_API kv_status kv_pool_info(kv_pool pool, kv_layout *layout, void **dev_ptr, uint64_t *nbytes);
+
+/* ------------------------------------------------------------- host tier */
+
+/* Registers the pinned host KV tier ([RFC] §Ownership: host KV physical
+ * allocation).  `host` must be page-locked host memory mapped into the
+ * device address space (cudaHostAlloc / torch pin_memory), 16-B aligned,
+ * holding `num_slots` slots of one page each (bytes >= num_slots x page
+ * bytes).  Slot geometry (L, C, T, H, B) comes from `pool_layout`; the
+ * tier's head order is `host_heads` (kv_heads).  Not owned by the library.
+ * Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, CUDA, NO_MEMORY. */
+KVB_API kv_status kv_host_register(void *host, uint64_t bytes, uint32_t num_slots, uint32_t host_heads,
+                           const kv_layout *pool_layout, kv_host *out);
+KVB_API kv_status kv_host_close(kv_host host);
+
+/* ------------------------------------------------------------ operations */
+
+/* BACKUP ([RFC] §Device IPC data path): for every i < n, every layer,
+ * component, token and head, host slot host_slots[i] receives the unit of
+ * page src_pages[i]; no other byte changes.  Enqueued on `stream` after
+ * earlier work on it; returns at once with a fence.  Checks, before
+ * enqueueing: handles live and not retired (CLOSED / STALE), pool and tier
+ * geometry equal (LAYOUT), ids in range (OUT_OF_RANGE), no slot written
+ * twice (DUPLICATE; repeated source pages are fine), arrays non-null when
+ * n > 0 (INVALID_ARG).  n = 0 enqueues only the fence.  Errors as listed and
+ * CUDA, NO_MEMORY. */
+KVB_API kv_status kv_backup(kv_pool pool, kv_host host, const int32_t *src_pages,
+                    const int32_t *host_slots, uint32_t n, void *stream, kv_fence *fence);
+
+/* RESTORE ([RFC] §Device IPC data path; layer-wise per [PR] §PP Prefetch
+ * Ticket Path): for every i < n, page dst_pages[i] receives the units of
+ * host slot host_slots[i] for every layer (layer = -1) or for that one layer
+ * (0 <= layer < L); no other byte changes.  Checks as kv_backup, with
+ * DUPLICATE for a destination page written twice and OUT_OF_RANGE for a
+ * layer outside [-1, L). */
+KVB_API kv_status kv_restore(kv_pool pool, kv_host host, const int32_t *host_slots,
+                     const int32_t *dst_pages, uint32_t n, int32_t layer, void *stream,
+                     kv_fence *fence);
+
+/* Device-side gather / scatter in host-tier layout (the first half of a
+ * STAGED transfer, exposed on its own for callers that move the result with
+ * their own engine: a NIC, storage, another process).  `buf` is DEVICE
+ * memory of the pool's device holding n items in the host tier's form with
+ * head order `buf_heads`: item i at byte i x (nl x C x T x H x B), where
+ * nl = L for a gather or a whole-page scatter and nl = 1 for a one-layer
+ * scatter.  kv_device_gather: item i <- page src_pages[i] (every layer).
+ * kv_device_scatter: page dst_pages[i] <- item i (every layer, or only
+ * `layer`).  Checks as kv_backup / kv_restore; buf must be 16-B aligned and
+ * buf_bytes >= n x item bytes (OUT_OF_RANGE); DUPLICATE for a page written
+ * twice by a scatter.  HBM-bound: one read and one write of every byte. */
+KVB_API kv_status kv_device_gather(kv_pool pool, void *buf, uint64_t buf_bytes, uint32_t buf_heads,
+                                   const int32_t *src_pages, uint32_t n, void *stream,
+                                   kv_fence *fence);
+KVB_API kv_status kv_device_scatter(kv_pool pool, const void *buf, uint64_t buf_bytes,
+                                    uint32_t buf_heads, const int32_t *dst_pages, uint32_t n,
+                                    int32_t layer, void *stream, kv_fence *fence);
+
+/* Host-side validation of an operation without a GPU (kind 0 = backup with
+ * a = src pages, b = slots; kind 1 = restore with a = slots, b = dst pages).
+ * Same checks and codes as kv_backup / kv_restore minus handle state. */
+KVB_API kv_status kv_op_validate(const kv_layout *layout, uint32_t num_slots, int kind,
+                         const int32_t *a, const int32_t *b, uint32_t n, int32_t layer);
+
+/* --------------------------------------------------------------- fences */
+
+/* DeviceSyncIPC wait/query ([RFC] §Device IPC data path).  A fence completes
+ * when every byte of its operation is in place.  Completion is a sequence
+ * number the GPU stores into a mapped pinned word after the operation, so
+ * the host learns of it without a CUDA call.
+ * kv_fence_query: OK when complete, TIMEOUT when not yet, INVALID_ARG for a
+ * fence never issued.  kv_fence_wait: polls until complete or until
+ * timeout_ns has passed (TIMEOUT).  kv_fence_stream_wait: makes `stream` wait
+ * for the fence on the GPU (the compute stream of a layer-wise restore). */
+KVB_API kv_status kv_fence_query(kv_fence fence);
+KVB_API kv_status kv_fence_wait(kv_fence fence, uint64_t timeout_ns);
+KVB_API kv_status kv_fence_stream_wait(kv_fence fence, void *stream);
+
+/* ------------------------------------------------------------ utilities */
+
+KVB_API kv_status kv_config_get(kv_config *out);
+/* Process-wide; applies to operations issued afterwards.  Errors: INVALID_ARG. */
+KVB_API kv_status kv_config_set(const kv_config *cfg);
+/* Bytes of one page (= one host slot) of a valid layout. */
+KVB_API kv_status kv_layout_page_bytes(const kv_layout *layout, uint64_t *out);
+/* Number of kernels this library has launched in this process. */
+KVB_API uint64_t kv_launch_count(void);
+/* Message of the last failing call on this thread ("" if none). */
+KVB_API const char *kv_last_error(void);
+KVB_API uint32_t kv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVB_H */

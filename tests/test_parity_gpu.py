@@ -1,0 +1,342 @@
+"""GPU parity: the CUDA path against the CPU oracle, byte for byte, over whole
+buffers (the pool's whole allocation and the whole host tier, so untouched
+bytes are checked too)."""
+import itertools
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from gpu_rig import Rig  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
+
+MODES = [kvb.KV_MODE_ZERO_COPY, kvb.KV_MODE_STAGED]
+LAYOUTS = [(o, d, h) for o in (wl.LAYER_FIRST, wl.PAGE_FIRST) for d in (wl.NHD, wl.HND)
+           for h in (wl.NHD, wl.HND)]
+
+
+@pytest.fixture(params=MODES, ids=["zero_copy", "staged"])
+def mode(request):
+    old = kvb.kv_config_get()
+    kvb.kv_config_set(request.param, 0, 4 << 20)   # small staging: forces several chunks
+    yield request.param
+    kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes)
+
+
+def run_backup(rig, src, slots, stream=None):
+    snap = rig.snapshot()
+    want = rig.expect_backup(snap, src, slots)
+    f = kvb.kv_backup(rig.pool, rig.hostt, src, slots, stream)
+    kvb.kv_fence_wait(f, 20_000_000_000)
+    rig.assert_equal(want)
+
+
+def run_restore(rig, slots, dst, layer=-1, stream=None):
+    snap = rig.snapshot()
+    want = rig.expect_restore(snap, slots, dst, layer)
+    f = kvb.kv_restore(rig.pool, rig.hostt, slots, dst, layer, stream)
+    kvb.kv_fence_wait(f, 20_000_000_000)
+    rig.assert_equal(want)
+
+
+@pytest.mark.parametrize("lay", LAYOUTS, ids=lambda t: "LF-PF"[3 * t[0]:3 * t[0] + 2] +
+                         "-" + "NH"[t[1]] + "-host" + "NH"[t[2]])
+def test_tiny_all_layouts(lay, mode):
+    """Tiny pool (2 layers x {K,V} x 2 heads x 16 tokens x 128 B), 8 random pages to 8 of 16
+    random slots, then restore into 8 other free pages, in every layout pairing."""
+    order, dev, host = lay
+    g = wl.TINY.geom.with_(order=order, dev_heads=dev, host_heads=host)
+    ids = wl.op_ids(wl.TINY)
+    rig = Rig(g, wl.TINY.host_slots, pool_offset=48, seed=wl.TINY.seed)
+    try:
+        run_backup(rig, ids.backup_src, ids.backup_slots)
+        run_restore(rig, ids.restore_slots, ids.restore_dst)
+        run_restore(rig, ids.restore_slots[:3], ids.backup_src[:3], layer=1)
+    finally:
+        rig.close()
+
+
+ODD = [  # geometries with ragged segment tails and non-power-of-two dims
+    dict(L=3, C=2, P=23, T=5, H=3, B=48),       # chunk 720 B: < one warp segment
+    dict(L=2, C=1, P=19, T=7, H=5, B=592),      # chunk 20,720 B: 5 segments + a ragged tail
+    dict(L=5, C=2, P=11, T=33, H=4, B=16),      # 16-byte heads, permutation of many tiny vectors
+    dict(L=1, C=1, P=9, T=1, H=1, B=4096 + 16), # one opaque run per page, ragged
+]
+
+
+@pytest.mark.parametrize("dims", ODD, ids=lambda d: "x".join(str(v) for v in d.values()))
+@pytest.mark.parametrize("lay", [(0, 0, 0), (0, 1, 0), (1, 1, 0), (1, 0, 1)],
+                         ids=["LF-N-hostN", "LF-H-hostN", "PF-H-hostN", "PF-N-hostH"])
+def test_odd_geometries(dims, lay, mode):
+    g = wl.Geometry(order=lay[0], dev_heads=lay[1], host_heads=lay[2], **dims)
+    r = np.random.default_rng(5)
+    S = g.P + 3
+    n = min(g.P - 1, 7)
+    rig = Rig(g, S, pool_offset=16 * 7, seed=77)
+    try:
+        src = r.permutation(g.P)[:n]
+        slots = r.permutation(S)[:n]
+        run_backup(rig, src, slots)
+        dst = r.permutation(g.P)[:n]
+        run_restore(rig, slots, dst)
+        run_restore(rig, slots[::-1].copy(), dst, layer=g.L - 1)
+    finally:
+        rig.close()
+
+
+def test_llama8b_shape_reduced(mode):
+    """Llama-8B page geometry (32 x {K,V} x 8 x 16 x 256 B) on a 256-page pool, 61 pages."""
+    g = wl.LLAMA8B.geom.with_(P=256)
+    r = np.random.default_rng(wl.LLAMA8B.seed)
+    rig = Rig(g, 80, seed=wl.LLAMA8B.seed)
+    try:
+        src = r.permutation(256)[:61]
+        slots = r.permutation(80)[:61]
+        run_backup(rig, src, slots)
+        dst = np.setdiff1d(np.arange(256), src)[r.permutation(256 - 61)[:61]]
+        run_restore(rig, slots, dst)
+    finally:
+        rig.close()
+
+
+def test_mla_layerwise_reduced(mode):
+    """MLA fp8 geometry (61 layers, 576 B latent, page 256) on a 96-page pool: a 16-page
+    prefix restored one layer per call on a side stream, then compared."""
+    g = wl.MLA_FP8.geom.with_(P=96)
+    r = np.random.default_rng(wl.MLA_FP8.seed)
+    rig = Rig(g, 16, seed=wl.MLA_FP8.seed)
+    try:
+        slots = np.arange(16)
+        dst = r.permutation(96)[:16]
+        snap = rig.snapshot()
+        want = rig.expect_restore(snap, slots, dst, -1)
+        s = torch.cuda.Stream()
+        fences = [kvb.kv_restore(rig.pool, rig.hostt, slots, dst, l, s.cuda_stream)
+                  for l in range(g.L)]
+        for f in fences:
+            kvb.kv_fence_wait(f, 20_000_000_000)
+        rig.assert_equal(want)
+    finally:
+        rig.close()
+
+
+def test_trtllm_reduced_at_offset(mode):
+    """TRT-LLM pool [NB, 40, 2, 8*32*128] bf16 (page-first HND) at offset 2 MiB + 48 inside
+    one allocation, host NHD: backup 25% and restore another 25% on two streams at once."""
+    g = wl.TRTLLM.geom.with_(P=64)
+    ids = wl.op_ids(wl.Workload("t", 3, g, n=16, host_slots=32, concurrent=True))
+    rig = Rig(g, 32, pool_offset=wl.TRTLLM.pool_offset, seed=wl.TRTLLM.seed)
+    try:
+        snap = rig.snapshot()
+        p1, h1 = rig.expect_backup(snap, ids.backup_src, ids.backup_slots)
+        p2, h2 = rig.expect_restore((p1, h1), ids.restore_slots, ids.restore_dst)
+        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        fa = kvb.kv_backup(rig.pool, rig.hostt, ids.backup_src, ids.backup_slots, sa.cuda_stream)
+        fb = kvb.kv_restore(rig.pool, rig.hostt, ids.restore_slots, ids.restore_dst, -1,
+                            sb.cuda_stream)
+        kvb.kv_fence_wait(fa, 20_000_000_000)
+        kvb.kv_fence_wait(fb, 20_000_000_000)
+        rig.assert_equal((p2, h2))
+    finally:
+        rig.close()
+
+
+@pytest.mark.parametrize("page_bytes,n,seq", [(4096, 1, True), (4096, 300, False),
+                                              (65536, 37, False), (1 << 20, 5, True)])
+def test_sweep_points(page_bytes, n, seq, mode):
+    g = wl.Geometry(L=1, C=1, P=512, T=1, H=1, B=page_bytes, elem_bytes=1)
+    r = np.random.default_rng(page_bytes + n)
+    rig = Rig(g, 2 * n, seed=9)
+    try:
+        src = np.arange(n) if seq else r.permutation(512)[:n]
+        run_backup(rig, src, np.arange(n))
+        dst = np.arange(n, 2 * n) if seq else r.permutation(512)[:n]
+        run_restore(rig, np.arange(n), dst)
+    finally:
+        rig.close()
+
+
+def test_more_items_than_one_launch(mode):
+    """n above the per-launch id budget (2048) splits into several launches."""
+    g = wl.Geometry(L=1, C=2, P=5000, T=2, H=1, B=16, elem_bytes=1)
+    r = np.random.default_rng(1)
+    rig = Rig(g, 4500, seed=3)
+    try:
+        src = r.permutation(5000)[:4500]
+        slots = r.permutation(4500)
+        run_backup(rig, src, slots)
+        run_restore(rig, slots[:4321], r.permutation(5000)[:4321])
+    finally:
+        rig.close()
+
+
+def test_empty_op_and_fence_order():
+    g = wl.TINY.geom
+    rig = Rig(g, 16, seed=1)
+    try:
+        snap = rig.snapshot()
+        f0 = kvb.kv_backup(rig.pool, rig.hostt, [], [])
+        kvb.kv_fence_wait(f0, 5_000_000_000)
+        assert kvb.kv_fence_query(f0) == kvb.KV_OK
+        rig.assert_equal(snap)
+        f1 = kvb.kv_backup(rig.pool, rig.hostt, [3], [4])
+        f2 = kvb.kv_restore(rig.pool, rig.hostt, [4], [9], 0)
+        assert f2 > f1 > f0
+        kvb.kv_fence_wait(f2, 5_000_000_000)
+        assert kvb.kv_fence_query(f1) == kvb.KV_OK
+    finally:
+        rig.close()
+
+
+def test_rejected_ops_have_no_side_effect():
+    g = wl.TINY.geom
+    rig = Rig(g, 16, seed=2)
+    try:
+        snap = rig.snapshot()
+        n0 = kvb.kv_launch_count()
+        cases = [
+            (lambda: kvb.kv_backup(rig.pool, rig.hostt, [1, 2], [3, 3]), kvb.KV_ERR_DUPLICATE),
+            (lambda: kvb.kv_backup(rig.pool, rig.hostt, [1, 64], [3, 4]), kvb.KV_ERR_OUT_OF_RANGE),
+            (lambda: kvb.kv_backup(rig.pool, rig.hostt, [1, 2], [3, 16]), kvb.KV_ERR_OUT_OF_RANGE),
+            (lambda: kvb.kv_restore(rig.pool, rig.hostt, [1, 2], [5, 5]), kvb.KV_ERR_DUPLICATE),
+            (lambda: kvb.kv_restore(rig.pool, rig.hostt, [1], [5], 2), kvb.KV_ERR_OUT_OF_RANGE),
+        ]
+        for fn, status in cases:
+            with pytest.raises(kvb.KvError) as e:
+                fn()
+            assert e.value.status == status, kvb.kv_last_error()
+        assert kvb.kv_launch_count() == n0
+        rig.assert_equal(snap)
+    finally:
+        rig.close()
+
+
+def test_pool_and_tier_geometry_must_agree():
+    g = wl.TINY.geom
+    rig = Rig(g, 16, seed=4)
+    other = Rig(g.with_(T=8), 16, seed=5)
+    try:
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_backup(rig.pool, other.hostt, [1], [1])
+        assert e.value.status == kvb.KV_ERR_LAYOUT
+    finally:
+        rig.close()
+        other.close()
+
+
+def test_register_checks_on_device():
+    g = wl.TINY.geom
+    t = torch.empty(g.pool_bytes + 100, dtype=torch.uint8, device="cuda")
+    lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B)
+    with pytest.raises(kvb.KvError) as e:       # pool overruns the allocation
+        kvb.kv_pool_register(lay, t.data_ptr(), 112)
+    assert e.value.status == kvb.KV_ERR_OUT_OF_RANGE
+    p = kvb.kv_pool_register(lay, t.data_ptr(), 96)
+    kvb.kv_pool_close(p)
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_pool_close(p)
+    assert e.value.status == kvb.KV_ERR_CLOSED
+    h = torch.empty(g.page_bytes * 2, dtype=torch.uint8)   # pageable: refused
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_host_register(h.data_ptr(), h.numel(), 2, 0, lay)
+    assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    hp = torch.empty(g.page_bytes * 2, dtype=torch.uint8, pin_memory=True)
+    with pytest.raises(kvb.KvError) as e:       # device memory is not a host tier
+        kvb.kv_host_register(t.data_ptr(), t.numel(), 1, 0, lay)
+    assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    kvb.kv_host_close(kvb.kv_host_register(hp.data_ptr(), hp.numel(), 2, 0, lay))
+
+
+def test_retired_generation_is_refused():
+    g = wl.TINY.geom
+    t = torch.zeros(g.pool_bytes, dtype=torch.uint8, device="cuda")
+    hp = torch.zeros(g.page_bytes * 2, dtype=torch.uint8, pin_memory=True)
+    lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B)
+    p = kvb.kv_pool_register(lay, t.data_ptr(), 0, instance_id=4242, generation=3)
+    h = kvb.kv_host_register(hp.data_ptr(), hp.numel(), 2, 0, lay)
+    try:
+        kvb.kv_fence_wait(kvb.kv_backup(p, h, [0], [0]), 5_000_000_000)
+        kvb.kv_pool_retire(4242, 4)
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_backup(p, h, [0], [0])
+        assert e.value.status == kvb.KV_ERR_STALE
+    finally:
+        kvb.kv_pool_close(p)
+        kvb.kv_host_close(h)
+
+
+def test_fence_stream_wait_orders_compute_after_restore():
+    """A compute stream that waits on a layer's fence sees that layer restored."""
+    g = wl.MLA_FP8.geom.with_(P=8, L=4)
+    rig = Rig(g, 2, seed=6)
+    try:
+        copy_s, comp_s = torch.cuda.Stream(), torch.cuda.Stream()
+        f = kvb.kv_restore(rig.pool, rig.hostt, [0, 1], [5, 2], 3, copy_s.cuda_stream)
+        kvb.kv_fence_stream_wait(f, comp_s.cuda_stream)
+        lb = g.layer_page_bytes
+        with torch.cuda.stream(comp_s):
+            # layer-first pool: page p of layer l starts at (l*C*P + p) * T*H*B
+            got = rig.alloc[(3 * 8 + 5) * lb:(3 * 8 + 6) * lb].clone()
+        comp_s.synchronize()
+        want = rig.host[0 * g.page_bytes + 3 * lb:0 * g.page_bytes + 4 * lb]
+        assert torch.equal(got.cpu(), want)
+    finally:
+        rig.close()
+
+
+@pytest.mark.parametrize("wname", ["llama8b", "trtllm_ipc", "mla_fp8"])
+def test_device_gather_scatter(wname):
+    """Device gather into / scatter out of a device buffer in host-tier layout equals the
+    oracle's backup into / restore out of a host tier whose slots are 0..n-1."""
+    import oracle
+    from gpu_rig import oracle_geom
+
+    w = {x.name: x for x in wl.WORKLOADS}[wname]
+    g = w.geom.with_(P=40)
+    n = 9
+    r = np.random.default_rng(w.seed)
+    rig = Rig(g, n, pool_offset=w.pool_offset, seed=w.seed)
+    buf = torch.empty(n * g.page_bytes + 32, dtype=torch.uint8, device="cuda")
+    try:
+        src = r.permutation(g.P)[:n]
+        snap = rig.snapshot()
+        want_host = np.zeros(n * g.page_bytes, dtype=np.uint8)
+        oracle.backup(oracle_geom(g), snap[0], want_host, src, np.arange(n),
+                      pool_offset=rig.offset)
+        f = kvb.kv_device_gather(rig.pool, buf.data_ptr(), buf.numel(), g.host_heads, src)
+        kvb.kv_fence_wait(f, 10_000_000_000)
+        assert np.array_equal(buf[:n * g.page_bytes].cpu().numpy(), want_host)
+        # scatter back into other pages, whole page and one layer
+        dst = r.permutation(g.P)[:n]
+        src_host = r.integers(0, 256, n * g.page_bytes, dtype=np.uint8)
+        buf[:n * g.page_bytes].copy_(torch.from_numpy(src_host))
+        snap = rig.snapshot()
+        want_pool = snap[0].copy()
+        oracle.restore(oracle_geom(g), want_pool, src_host, np.arange(n), dst,
+                       pool_offset=rig.offset)
+        f = kvb.kv_device_scatter(rig.pool, buf.data_ptr(), buf.numel(), g.host_heads, dst)
+        kvb.kv_fence_wait(f, 10_000_000_000)
+        rig.assert_equal((want_pool, snap[1]))
+        layer = g.L - 2
+        one_layer = np.ascontiguousarray(src_host.reshape(n, g.L, -1)[:, layer]).reshape(-1)
+        buf[:one_layer.size].copy_(torch.from_numpy(one_layer))
+        oracle.restore(oracle_geom(g), want_pool, src_host, np.arange(n), src, layer=layer,
+                       pool_offset=rig.offset)
+        f = kvb.kv_device_scatter(rig.pool, buf.data_ptr(), one_layer.size, g.host_heads, src,
+                                  layer)
+        kvb.kv_fence_wait(f, 10_000_000_000)
+        rig.assert_equal((want_pool, snap[1]))
+        with pytest.raises(kvb.KvError) as e:   # buffer too small for n items
+            kvb.kv_device_gather(rig.pool, buf.data_ptr(), g.page_bytes * (n - 1), 0, src)
+        assert e.value.status == kvb.KV_ERR_OUT_OF_RANGE
+        with pytest.raises(kvb.KvError) as e:   # host memory is not a device buffer
+            kvb.kv_device_gather(rig.pool, rig.host.data_ptr(), rig.host.numel(), 0, src[:1])
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    finally:
+        rig.close()
