@@ -230,12 +230,22 @@ def test_pool_and_tier_geometry_must_agree():
         other.close()
 
 
+def _segment_end(ptr):
+    """End address of the CUDA allocation (caching-allocator segment) holding ptr."""
+    for seg in torch.cuda.memory_snapshot():
+        if seg["address"] <= ptr < seg["address"] + seg["total_size"]:
+            return seg["address"] + seg["total_size"]
+    raise AssertionError("pointer not in any segment")
+
+
 def test_register_checks_on_device():
     g = wl.TINY.geom
     t = torch.empty(g.pool_bytes + 100, dtype=torch.uint8, device="cuda")
     lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B)
-    with pytest.raises(kvb.KvError) as e:       # pool overruns the allocation
-        kvb.kv_pool_register(lay, t.data_ptr(), 112)
+    end = _segment_end(t.data_ptr())
+    over = end - g.pool_bytes + 16 - t.data_ptr()      # pool would end 16 B past the segment
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_pool_register(lay, t.data_ptr(), over)
     assert e.value.status == kvb.KV_ERR_OUT_OF_RANGE
     p = kvb.kv_pool_register(lay, t.data_ptr(), 96)
     kvb.kv_pool_close(p)
