@@ -57,7 +57,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
         log = None
         if src.endswith(".cu"):
             cmd += ["-Xptxas", "-v"]
-            log = open(os.path.join(BUILD, "ptxas.log"), "w")
+            log = open(os.path.join(BUILD, os.path.basename(src) + ".ptxas.log"), "w")
         procs.append((subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
                                        text=True), cmd, log))
         objs.append(obj)

@@ -49,7 +49,10 @@ kv_status fail(kv_status st, const char *fmt, ...) {
 }
 
 kv_status cuda_fail(cudaError_t e, const char *what) {
-    return fail(KV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    kv_status st = fail(KV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+                        cudaGetErrorString(e));
+    (void)cudaGetLastError();   // a non-sticky error must not resurface at a later launch
+    return st;
 }
 
 // ---------------------------------------------------------------- geometry

@@ -165,6 +165,7 @@ FastDiv make_fastdiv(uint32_t d) {
 }
 
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
+    (void)cudaGetLastError();   // report this launch's error, not an earlier call's
     if (d.transpose)
         kv_move_kernel<true><<<ctas, kMoveThreads, 0, stream>>>(d, ids);
     else
@@ -173,6 +174,7 @@ cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStr
 }
 
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream) {
+    (void)cudaGetLastError();
     kv_mark_kernel<<<1, 32, 0, stream>>>(word, seq);
     return cudaGetLastError();
 }
