@@ -677,6 +677,87 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
 
 }  // namespace
 
+// ------------------------------------------- staged backup with no allocation
+
+namespace kvb {
+
+int set_last_error(int status, const char *msg) { return fail((kv_status)status, "%s", msg); }
+
+int pool_device_of(const void *pool_handle, int *device) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    PoolObj *p = find_pool((kv_pool)pool_handle);
+    if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    *device = p->device;
+    return KV_OK;
+}
+
+int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_handle,
+                                  const int32_t *src, const int32_t *slots, uint32_t n,
+                                  void *staging, uint64_t staging_bytes, cudaStream_t stream) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (pool_handle == nullptr || host_handle == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "pool or host handle is NULL");
+    PoolObj *pool = find_pool((kv_pool)pool_handle);
+    if (pool == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    HostObj *host = find_host((kv_host)host_handle);
+    if (host == nullptr) return fail(KV_ERR_CLOSED, "host handle is closed or unknown");
+    auto fl = g_floor.find(pool->instance_id);
+    if (fl != g_floor.end() && pool->generation < fl->second)
+        return fail(KV_ERR_STALE, "pool generation %llu of instance %llu is retired",
+                    (unsigned long long)pool->generation, (unsigned long long)pool->instance_id);
+    if (!same_slot_geometry(pool->g, host->g))
+        return fail(KV_ERR_LAYOUT, "pool and host tier have different page geometry");
+    if (n > 0 && (src == nullptr || slots == nullptr))
+        return fail(KV_ERR_INVALID_ARG, "id arrays must be non-NULL when n = %u", n);
+    const Geo &g = pool->g;
+    if (n > (uint32_t)kMaxItems)
+        return fail(KV_ERR_OUT_OF_RANGE, "n = %u exceeds the %d pages one allocation-free backup "
+                    "may move", n, kMaxItems);
+    if ((uint64_t)n * g.pb > staging_bytes)
+        return fail(KV_ERR_OUT_OF_RANGE, "%u pages of %llu bytes exceed the %llu-byte static "
+                    "staging area of the allocation-free backup", n, (unsigned long long)g.pb,
+                    (unsigned long long)staging_bytes);
+    // range checks, then duplicate slots by sorting a stack copy (no heap)
+    int32_t sorted[kMaxItems];
+    for (uint32_t i = 0; i < n; ++i) {
+        if (src[i] < 0 || (uint64_t)src[i] >= g.P)
+            return fail(KV_ERR_OUT_OF_RANGE, "src_pages[%u] = %d is outside [0, %llu)", i, src[i],
+                        (unsigned long long)g.P);
+        if (slots[i] < 0 || (uint32_t)slots[i] >= host->num_slots)
+            return fail(KV_ERR_OUT_OF_RANGE, "host_slots[%u] = %d is outside [0, %u)", i, slots[i],
+                        host->num_slots);
+        sorted[i] = slots[i];
+    }
+    std::sort(sorted, sorted + n);
+    for (uint32_t i = 1; i < n; ++i)
+        if (sorted[i] == sorted[i - 1])
+            return fail(KV_ERR_DUPLICATE, "host slot %d appears twice: one call may write a slot "
+                        "only once", sorted[i]);
+    if (n == 0) return KV_OK;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, pool->device);
+    const Side ps = pool_side(*pool);
+    const Side ss = staging_side((char *)staging, g, host->heads, (uint32_t)g.L, 0, n);
+    Plan p;
+    kv_status st = plan(g, ps, ss, (uint32_t)g.L, 0, nullptr, true, &p);
+    if (st != KV_OK) return st;
+    MoveIds ids;   // on the stack: the ids travel inside the launch
+    std::memcpy(ids.a, src, n * sizeof(int32_t));
+    for (uint32_t k = 0; k < n; ++k) ids.b[k] = (int32_t)k;
+    p.d.n = n;
+    p.d.total_segs = n * p.d.nl * p.d.C * p.d.segs;
+    const uint32_t per_cta = kMoveThreads / 32;
+    const uint64_t need = (p.d.total_segs + per_cta - 1) / per_cta;
+    const int cap = g_cfg.max_ctas ? (int)g_cfg.max_ctas : 4 * std::max(sms, 1);
+    const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)cap));
+    cudaError_t e = launch_move(p.d, ids, ctas, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return staged_copies(*host, (char *)staging, slots, n, g.pb, 0, true, stream);
+}
+
+}  // namespace kvb
+
 // =================================================================== C ABI
 
 extern "C" {

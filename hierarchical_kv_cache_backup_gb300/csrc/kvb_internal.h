@@ -64,4 +64,17 @@ cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStr
 // once everything before it on `stream` has finished.
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream);
 
+// ---- support for kv_backup_staged_noalloc (kvb_noalloc.cu) ----------------
+// Records `msg` as this thread's last error and returns `status`.
+int set_last_error(int status, const char *msg);
+// Device of a live pool handle, or an error status.
+int pool_device_of(const void *pool_handle, int *device);
+// Validates a staged backup into a caller-supplied device staging area of
+// `staging_bytes` and enqueues it on `stream`: the gather kernel (pool ->
+// staging, host layout) and copy-engine copies (staging -> host tier).  Uses
+// no heap, no CUDA allocation and no library fence; returns a kv_status.
+int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_handle,
+                                  const int32_t *src_pages, const int32_t *host_slots, uint32_t n,
+                                  void *staging, uint64_t staging_bytes, cudaStream_t stream);
+
 }  // namespace kvb

@@ -41,7 +41,8 @@ KVB_IPC_MAGIC = 0x4B564231
 # the symbols include/kvb.h declares
 EXPORTS = ("kv_pool_register", "kv_pool_export", "kv_pool_import", "kv_pool_close",
            "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
-           "kv_restore", "kv_device_gather", "kv_device_scatter", "kv_op_validate", "kv_fence_query", "kv_fence_wait",
+           "kv_restore", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
+           "kv_op_validate", "kv_fence_query", "kv_fence_wait",
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version")
 
@@ -92,6 +93,7 @@ def _load():
         "kv_restore": (st, [vp, vp, vp, vp, u32, i32, vp, P(u64)]),
         "kv_device_gather": (st, [vp, vp, u64, u32, vp, u32, vp, P(u64)]),
         "kv_device_scatter": (st, [vp, vp, u64, u32, vp, u32, i32, vp, P(u64)]),
+        "kv_backup_staged_noalloc": (st, [vp, vp, vp, vp, u32, vp]),
         "kv_op_validate": (st, [P(kv_layout), u32, ctypes.c_int, vp, vp, u32, i32]),
         "kv_fence_query": (st, [u64]),
         "kv_fence_wait": (st, [u64, u64]),
@@ -225,6 +227,15 @@ def kv_device_scatter(pool: int, buf: int, buf_bytes: int, buf_heads: int, dst_p
     _check(_lib.kv_device_scatter(pool, buf, buf_bytes, buf_heads, pa, a.size, layer, stream,
                                   ctypes.byref(f)))
     return f.value
+
+
+def kv_backup_staged_noalloc(pool: int, host: int, src_pages, host_slots, stream=None) -> None:
+    """Allocation-free staged backup (see include/kvb.h); ordered on ``stream``, no fence."""
+    a, pa = _ids(src_pages)
+    b, pb = _ids(host_slots)
+    if a.size != b.size:
+        raise ValueError("src_pages and host_slots differ in length")
+    _check(_lib.kv_backup_staged_noalloc(pool, host, pa, pb, a.size, stream))
 
 
 def kv_op_validate(layout: kv_layout, num_slots: int, kind: int, a, b, layer: int = -1) -> int:

@@ -236,6 +236,31 @@ KVB_API kv_status kv_device_scatter(kv_pool pool, const void *buf, uint64_t buf_
                                     uint32_t buf_heads, const int32_t *dst_pages, uint32_t n,
                                     int32_t layer, void *stream, kv_fence *fence);
 
+/* Staged backup that allocates nothing.  No counterpart on the pages: this
+ * entry point exists for callers that cannot allocate GPU memory when they
+ * back pages up (an engine whose allocator owns all of HBM, an out-of-memory
+ * or teardown path, a runtime that forbids allocation calls while it records
+ * work).  Same result as kv_backup: host slot host_slots[i] receives page
+ * src_pages[i].  It stages through one static device array of
+ * KVB_NOALLOC_STAGING_BYTES that is part of the library (every GPU that loads
+ * the library's device code holds it until the process exits), so the call
+ * makes no cudaMalloc, cudaFree, pinned or event allocation and returns no
+ * fence: the work is ordered on `stream`, and the caller waits on that stream
+ * (or an event of its own) before reading the host slots.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array.  Nothing in it needs to
+ *     start at zero (each call writes every byte it later reads), but calls
+ *     whose work overlaps on the GPU (different streams, not ordered) race on
+ *     it and corrupt each other's output: order them on one stream.
+ *   - Limits: n <= 2048 and n x page bytes <= KVB_NOALLOC_STAGING_BYTES, else
+ *     OUT_OF_RANGE with a message naming the limit.  Other checks and codes
+ *     as kv_backup. */
+#define KVB_NOALLOC_STAGING_BYTES (32ull << 20)
+KVB_API kv_status kv_backup_staged_noalloc(kv_pool pool, kv_host host, const int32_t *src_pages,
+                                           const int32_t *host_slots, uint32_t n, void *stream);
+
 /* Host-side validation of an operation without a GPU (kind 0 = backup with
  * a = src pages, b = slots; kind 1 = restore with a = slots, b = dst pages).
  * Same checks and codes as kv_backup / kv_restore minus handle state. */
