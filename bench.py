@@ -422,6 +422,40 @@ def run_ours(args):
                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
         del buf
 
+    # ---- small-op latency: the tiny workload (8 pages of 16 KiB) through the C ABI
+    latency = None
+    if w is wl.LLAMA8B:
+        t = wl.TINY
+        tg = t.geom
+        tlay = kvb.make_layout(tg.L, tg.C, tg.P, tg.T, tg.H, tg.B, tg.order, tg.dev_heads,
+                               tg.elem_bytes)
+        talloc = torch.empty(tg.pool_bytes, dtype=torch.uint8, device=dev)
+        wl.fill_random_(talloc, t.seed)
+        thost = torch.empty(t.host_slots * tg.page_bytes, dtype=torch.uint8, pin_memory=True)
+        tpool = kvb.kv_pool_register(tlay, talloc.data_ptr(), 0)
+        ttier = kvb.kv_host_register(thost.data_ptr(), thost.numel(), t.host_slots, 0, tlay)
+        tids = wl.op_ids(t)
+        lat_b, lat_r = [], []
+        for i in range(250):
+            t0 = time.perf_counter()
+            kvb.kv_fence_wait(kvb.kv_backup(tpool, ttier, tids.backup_src, tids.backup_slots,
+                                            s_a.cuda_stream), 10_000_000_000)
+            t1 = time.perf_counter()
+            kvb.kv_fence_wait(kvb.kv_restore(tpool, ttier, tids.restore_slots, tids.restore_dst,
+                                             -1, s_a.cuda_stream), 10_000_000_000)
+            t2 = time.perf_counter()
+            if i >= 50:
+                lat_b.append(t1 - t0)
+                lat_r.append(t2 - t1)
+        latency = {"workload": "tiny: 8 pages x 16 KiB (128 KiB) per op, host clock from the "
+                               "C-ABI call to the fence wait returning",
+                   "backup_us_median": round(1e6 * statistics.median(lat_b), 1),
+                   "restore_us_median": round(1e6 * statistics.median(lat_r), 1),
+                   "backup_us_p99": round(1e6 * sorted(lat_b)[int(0.99 * len(lat_b))], 1)}
+        kvb.kv_pool_close(tpool)
+        kvb.kv_host_close(ttier)
+        del talloc, thost
+
     # ---- dominant kernel: the backup (D2H) move, or the restore for MLA
     if w is wl.MLA_FP8:
         dom_ms = statistics.mean(b_ms) / g.L
@@ -478,6 +512,7 @@ def run_ours(args):
                 "note": "host clock around kv_backup/kv_restore with host id arrays and a fence "
                         "wait every step; payload crosses the host link inside the region"},
         "gpu_launches": launches,
+        "latency_small_ops": latency,
         "clocks": clk.summary(),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -139,8 +139,11 @@ struct DevState {
     bool init = false;
     unsigned long long *words = nullptr;     // host view of the fence words
     unsigned long long *words_dev = nullptr; // device view
+    unsigned long long *status = nullptr;    // host view: status[k] == seq -> op gave up
+    unsigned long long *status_dev = nullptr;
     uint32_t *err = nullptr;                 // sticky "kernel met a bad id" word
     uint32_t *err_dev = nullptr;
+    uint32_t *counters = nullptr;            // device: finished-CTA counters, one per slot
     cudaEvent_t ev[kRing] = {};
     uint64_t slot_seq[kRing] = {};
     int sms = 0;
@@ -162,6 +165,7 @@ kv_config g_cfg = {KV_MODE_ZERO_COPY, 0, 0};
 std::atomic<uint64_t> g_launches{0};
 
 constexpr uint64_t kDefaultStaging = 256ull << 20;
+constexpr uint64_t kMaxReadyTimeoutNs = 60ull * 1000 * 1000 * 1000;   // gate waits at most 60 s
 
 uint64_t handle_id(const void *h) { return (uint64_t)(uintptr_t)h; }
 
@@ -216,21 +220,33 @@ kv_status init_device(int d) {
     DevState &s = g_dev[d];
     if (s.init) return KV_OK;
     DeviceGuard guard(d);
+    // mapped pinned table: kRing fence words, kRing status words, the error word
+    const size_t table = 2 * kRing * sizeof(unsigned long long) + 64;
     void *mem = nullptr;
-    cudaError_t e = cudaHostAlloc(&mem, kRing * sizeof(unsigned long long) + 64,
-                                  cudaHostAllocMapped | cudaHostAllocPortable);
+    cudaError_t e = cudaHostAlloc(&mem, table, cudaHostAllocMapped | cudaHostAllocPortable);
     if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(fence words)");
-    std::memset(mem, 0, kRing * sizeof(unsigned long long) + 64);
+    std::memset(mem, 0, table);
     void *dmem = nullptr;
     e = cudaHostGetDevicePointer(&dmem, mem, 0);
     if (e != cudaSuccess) {
         cudaFreeHost(mem);
         return cuda_fail(e, "cudaHostGetDevicePointer(fence words)");
     }
+    void *cnt = nullptr;
+    e = cudaMalloc(&cnt, kRing * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(cnt, 0, kRing * sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        if (cnt) cudaFree(cnt);
+        cudaFreeHost(mem);
+        return cuda_fail(e, "cudaMalloc(completion counters)");
+    }
     s.words = (unsigned long long *)mem;
     s.words_dev = (unsigned long long *)dmem;
-    s.err = (uint32_t *)(s.words + kRing);
-    s.err_dev = (uint32_t *)(s.words_dev + kRing);
+    s.status = s.words + kRing;
+    s.status_dev = s.words_dev + kRing;
+    s.err = (uint32_t *)(s.words + 2 * kRing);
+    s.err_dev = (uint32_t *)(s.words_dev + 2 * kRing);
+    s.counters = (uint32_t *)cnt;
     cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, d);
     if (s.sms <= 0) s.sms = 1;
     s.init = true;
@@ -249,9 +265,19 @@ double now_ns() {
     return ts.tv_sec * 1e9 + ts.tv_nsec;
 }
 
-// Called with g_mu held, device current.  Enqueues the completion marker and
-// records the slot's event.
-kv_status issue_fence(int d, cudaStream_t stream, kv_fence *out) {
+// Fences.  An operation first reserves the next sequence number and its ring
+// slot (waiting, bounded, if the slot's previous op is still in flight); its
+// last kernel then stores the number into the slot's mapped word -- fused into
+// the move kernel, or by kv_mark_kernel after copy-engine work -- and
+// commit_fence records the slot's event and publishes the fence.  Both run
+// with g_mu held and the device current, so a failed operation simply never
+// commits and its number is reused.
+struct FenceSlot {
+    uint64_t seq;
+    int k;
+};
+
+kv_status reserve_fence(int d, FenceSlot *out) {
     DevState &s = g_dev[d];
     const uint64_t seq = g_next_seq;
     if (seq > kSeqMask) return fail(KV_ERR_NO_MEMORY, "fence sequence space exhausted");
@@ -272,19 +298,36 @@ kv_status issue_fence(int d, cudaStream_t stream, kv_fence *out) {
             return cuda_fail(e, "cudaEventCreate(fence)");
         }
     }
-    cudaError_t e = launch_mark(s.words_dev + k, seq, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "launch of the completion marker");
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    e = cudaEventRecord(s.ev[k], stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fence)");
-    s.slot_seq[k] = seq;
-    g_next_seq = seq + 1;
-    *out = ((uint64_t)d << 56) | seq;
+    out->seq = seq;
+    out->k = k;
     return KV_OK;
 }
 
+kv_status commit_fence(int d, const FenceSlot &f, bool need_mark, cudaStream_t stream,
+                       kv_fence *out) {
+    DevState &s = g_dev[d];
+    if (need_mark) {
+        cudaError_t e = launch_mark(s.words_dev + f.k, f.seq, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "launch of the completion marker");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    cudaError_t e = cudaEventRecord(s.ev[f.k], stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fence)");
+    s.slot_seq[f.k] = f.seq;
+    g_next_seq = f.seq + 1;
+    *out = ((uint64_t)d << 56) | f.seq;
+    return KV_OK;
+}
+
+kv_status issue_fence(int d, cudaStream_t stream, kv_fence *out) {
+    FenceSlot f;
+    kv_status st = reserve_fence(d, &f);
+    if (st != KV_OK) return st;
+    return commit_fence(d, f, true, stream, out);
+}
+
 // Decodes a fence; returns KV_OK with done set, or an error.
-kv_status fence_state(kv_fence f, bool *done, int *dev, int *slot) {
+kv_status fence_state(kv_fence f, bool *done, int *dev, int *slot, bool *aborted) {
     const int d = (int)(f >> 56);
     const uint64_t seq = f & kSeqMask;
     if (seq == 0 || d >= kMaxDevices) return fail(KV_ERR_INVALID_ARG, "invalid fence %llu",
@@ -299,7 +342,9 @@ kv_status fence_state(kv_fence f, bool *done, int *dev, int *slot) {
         next = g_next_seq;
     }
     const int k = (int)(seq % kRing);
-    *done = (next - seq > (uint64_t)kRing) || load_acquire(&words[k]) >= seq;
+    const bool recycled = next - seq > (uint64_t)kRing;
+    *done = recycled || load_acquire(&words[k]) >= seq;
+    *aborted = !recycled && *done && load_acquire(&g_dev[d].status[k]) == seq;
     *dev = d;
     *slot = k;
     return KV_OK;
@@ -440,18 +485,36 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
     return KV_OK;
 }
 
+// CTAs of a move kernel.  Host-link moves saturate the link with few CTAs
+// (measured on GB300: 16 CTAs of 256 threads reach the D2H peak, 32 the H2D
+// peak, and 64 + 64 give the best D2H + H2D mix, while more CTAs per direction
+// lose bidirectional throughput), so they are capped at kLinkCtas and leave
+// the other SMs to compute.  HBM-only moves use 4 CTAs per SM.
+constexpr int kLinkCtas = 64;
+
 int default_ctas(const DevState &s, bool touches_host) {
     if (g_cfg.max_ctas != 0) return (int)g_cfg.max_ctas;
-    return touches_host ? 2 * s.sms : 4 * s.sms;
+    return touches_host ? std::min(kLinkCtas, 4 * s.sms) : 4 * s.sms;
 }
 
 // Launches the move for items [0, n) of (a, b) in slices of at most max_items.
 // b_is_index: the destination id of item i is i itself (a staging position).
+// fence: when non-null, the last slice's kernel completes that fence itself.
 kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int ctas_cap,
-                    cudaStream_t stream, bool b_is_index) {
+                    cudaStream_t stream, bool b_is_index, const DevState *ds = nullptr,
+                    const FenceSlot *fence = nullptr) {
     static thread_local MoveIds ids;
     for (uint32_t i0 = 0; i0 < n; i0 += p.max_items) {
         const uint32_t m = std::min(p.max_items, n - i0);
+        const bool last = i0 + m >= n;
+        if (last && fence != nullptr) {
+            p.d.fence_word = ds->words_dev + fence->k;
+            p.d.fence_seq = fence->seq;
+            p.d.fence_count = ds->counters + fence->k;
+        } else {
+            p.d.fence_word = nullptr;
+            p.d.fence_count = nullptr;
+        }
         std::memcpy(ids.a, a + i0, m * sizeof(int32_t));
         if (b_is_index)
             for (uint32_t k = 0; k < m; ++k) ids.b[k] = (int32_t)(i0 + k);
@@ -522,8 +585,13 @@ kv_status staged_copies(const HostObj &h, char *staging, const int32_t *slots, u
 }
 
 // Issues one backup (kind 0) or restore (kind 1).  g_mu held.
+// `ready` (device-visible, or NULL): BACKUP's ready_fence -- the move starts
+// only once *ready >= ready_value, waited for on the GPU for at most
+// ready_timeout_ns; on time-out nothing moves and the fence reports ABORTED.
 kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, const int32_t *b,
-                uint32_t n, int32_t layer, void *stream_v, kv_fence *fence) {
+                uint32_t n, int32_t layer, void *stream_v, kv_fence *fence,
+                const unsigned long long *ready = nullptr, uint64_t ready_value = 0,
+                uint64_t ready_timeout_ns = 0) {
     if (fence == nullptr) return fail(KV_ERR_INVALID_ARG, "fence output pointer is NULL");
     if (pool_h == nullptr || host_h == nullptr)
         return fail(KV_ERR_INVALID_ARG, "pool or host handle is NULL");
@@ -550,15 +618,30 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     const bool backup = kind == 0;
     const uint32_t nl = layer < 0 ? (uint32_t)pool->g.L : 1u;
     const uint32_t l0 = layer < 0 ? 0u : (uint32_t)layer;
+    FenceSlot fs;
+    st = reserve_fence(d, &fs);
+    if (st != KV_OK) return st;
+    if (ready != nullptr) {
+        cudaError_t e = launch_gate(ready, ready_value, ready_timeout_ns, ds.status_dev + fs.k,
+                                    fs.seq, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "launch of the ready-fence gate");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    bool fused = false;
 
-    if (n > 0 && g_cfg.mode == KV_MODE_ZERO_COPY) {
+    if (n > 0 && (g_cfg.mode == KV_MODE_ZERO_COPY || ready != nullptr)) {
         const Side ps = pool_side(*pool), hs = host_side(*host);
         Plan p;
         st = plan(pool->g, backup ? ps : hs, backup ? hs : ps, nl, l0, ds.err_dev,
                   /*iter_dst=*/backup, &p);
         if (st != KV_OK) return st;
-        st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false);
+        if (ready != nullptr) {
+            p.d.skip_word = ds.status_dev + fs.k;
+            p.d.skip_tag = fs.seq;
+        }
+        st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false, &ds, &fs);
         if (st != KV_OK) return st;
+        fused = true;
     } else if (n > 0) {
         st = ensure_staging(ds);
         if (st != KV_OK) return st;
@@ -611,7 +694,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
         ds.staging_used[half] = true;
     }
-    return issue_fence(d, stream, fence);
+    return commit_fence(d, fs, !fused, stream, fence);
 }
 
 // Device gather (kind 0) / scatter (kind 1) between the pool and a caller's
@@ -662,15 +745,20 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
         Plan p;
         st = plan(g, kind == 0 ? ps : bs, kind == 0 ? bs : ps, nl, l0, ds.err_dev, kind == 0, &p);
         if (st != KV_OK) return st;
+        FenceSlot fs;
+        st = reserve_fence(d, &fs);
+        if (st != KV_OK) return st;
         if (kind == 0) {
-            st = run_moves(p, pages, nullptr, n, default_ctas(ds, false), stream, true);
+            st = run_moves(p, pages, nullptr, n, default_ctas(ds, false), stream, true, &ds, &fs);
         } else {
             static thread_local std::vector<int32_t> idx;
             idx.resize(n);
             for (uint32_t k = 0; k < n; ++k) idx[k] = (int32_t)k;
-            st = run_moves(p, idx.data(), pages, n, default_ctas(ds, false), stream, false);
+            st = run_moves(p, idx.data(), pages, n, default_ctas(ds, false), stream, false, &ds,
+                           &fs);
         }
         if (st != KV_OK) return st;
+        return commit_fence(d, fs, false, stream, fence);
     }
     return issue_fence(d, stream, fence);
 }
@@ -1026,6 +1114,32 @@ kv_status kv_backup(kv_pool pool, kv_host host, const int32_t *src_pages,
     return issue(pool, host, 0, src_pages, host_slots, n, -1, stream, fence);
 }
 
+kv_status kv_backup_when_ready(kv_pool pool, kv_host host, const int32_t *src_pages,
+                               const int32_t *host_slots, uint32_t n, const uint64_t *ready_word,
+                               uint64_t ready_value, uint64_t ready_timeout_ns, void *stream,
+                               kv_fence *fence) {
+    if (ready_word == nullptr) return fail(KV_ERR_INVALID_ARG, "ready_word is NULL");
+    if (((uintptr_t)ready_word) % 8 != 0)
+        return fail(KV_ERR_ALIGNMENT, "ready_word %p is not 8-byte aligned", (const void *)ready_word);
+    if (ready_timeout_ns > kMaxReadyTimeoutNs)
+        return fail(KV_ERR_INVALID_ARG, "ready_timeout_ns %llu exceeds the %llu ns limit",
+                    (unsigned long long)ready_timeout_ns, (unsigned long long)kMaxReadyTimeoutNs);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, ready_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(ready_word)");
+    const void *dev_word = nullptr;
+    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
+        dev_word = ready_word;
+    else if (attr.type == cudaMemoryTypeHost)
+        dev_word = attr.devicePointer;
+    if (dev_word == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "ready_word %p is not visible to the GPU (use device or "
+                    "pinned mapped host memory)", (const void *)ready_word);
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue(pool, host, 0, src_pages, host_slots, n, -1, stream, fence,
+                 (const unsigned long long *)dev_word, ready_value, ready_timeout_ns);
+}
+
 kv_status kv_restore(kv_pool pool, kv_host host, const int32_t *host_slots,
                      const int32_t *dst_pages, uint32_t n, int32_t layer, void *stream,
                      kv_fence *fence) {
@@ -1048,10 +1162,13 @@ kv_status kv_device_scatter(kv_pool pool, const void *buf, uint64_t buf_bytes, u
 }
 
 kv_status kv_fence_query(kv_fence f) {
-    bool done = false;
+    bool done = false, aborted = false;
     int d = 0, k = 0;
-    kv_status st = fence_state(f, &done, &d, &k);
+    kv_status st = fence_state(f, &done, &d, &k, &aborted);
     if (st != KV_OK) return st;
+    if (aborted)
+        return fail(KV_ERR_ABORTED, "fence %llu: the ready fence was not reached in time; the "
+                    "operation moved nothing", (unsigned long long)f);
     if (g_dev[d].err != nullptr && __atomic_load_n(g_dev[d].err, __ATOMIC_ACQUIRE) != 0)
         return fail(KV_ERR_OUT_OF_RANGE, "a transfer kernel met an out-of-range id and skipped it");
     return done ? KV_OK : KV_ERR_TIMEOUT;
@@ -1076,9 +1193,9 @@ kv_status kv_fence_wait(kv_fence f, uint64_t timeout_ns) {
 }
 
 kv_status kv_fence_stream_wait(kv_fence f, void *stream) {
-    bool done = false;
+    bool done = false, aborted = false;
     int d = 0, k = 0;
-    kv_status st = fence_state(f, &done, &d, &k);
+    kv_status st = fence_state(f, &done, &d, &k, &aborted);
     if (st != KV_OK) return st;
     if (done) return KV_OK;
     std::lock_guard<std::mutex> lk(g_mu);

@@ -51,18 +51,40 @@ struct MoveDesc {
     uint32_t iter_dst;   // transpose only: 1 = walk destination order
     FastDiv div_segs, div_lc, div_c, div_b16, div_T, div_H;
     uint32_t *err;       // device-visible word set to 1 if a kernel meets a bad id
+    // Completion, fused: when fence_word is set, the last CTA to finish stores
+    // fence_seq there (system scope, release) once every CTA's bytes are
+    // visible; fence_count is a zeroed device counter that CTA resets.
+    unsigned long long *fence_word;
+    unsigned long long fence_seq;
+    uint32_t *fence_count;
+    // Gating: when skip_word is set and *skip_word == skip_tag (written by the
+    // ready-fence gate that ran before this kernel), no byte is moved.
+    const unsigned long long *skip_word;
+    unsigned long long skip_tag;
 };
 
-struct MoveIds {
-    int32_t a[kMaxItems];   // source ids (pages for backup, slots for restore)
-    int32_t b[kMaxItems];   // destination ids
+// Ids of one launch, inside the kernel's parameter block.  Launches use the
+// smallest capacity that holds their items (64, 512 or kMaxItems), so small
+// operations do not ship 16 KiB of parameters.
+template <int kCap>
+struct IdsT {
+    int32_t a[kCap];   // source ids (pages for backup, slots for restore)
+    int32_t b[kCap];   // destination ids
 };
+using MoveIds = IdsT<kMaxItems>;
 
 // Launch the gather/scatter kernel on `stream` with `ctas` CTAs.
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
 // Launch the completion marker: stores `seq` to `word` (system scope, release)
 // once everything before it on `stream` has finished.
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream);
+// Launch the ready-fence gate: one thread waits until *word >= value or until
+// timeout_ns has passed on the GPU's global timer (and at most a bounded
+// number of polls); on time-out it stores `tag` to *status, which makes the
+// gated kernels that follow on `stream` skip their work.
+cudaError_t launch_gate(const unsigned long long *word, unsigned long long value,
+                        unsigned long long timeout_ns, unsigned long long *status,
+                        unsigned long long tag, cudaStream_t stream);
 
 // ---- support for kv_backup_staged_noalloc (kvb_noalloc.cu) ----------------
 // Records `msg` as this thread's last error and returns `status`.

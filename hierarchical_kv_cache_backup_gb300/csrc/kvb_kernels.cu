@@ -69,15 +69,50 @@ __device__ __forceinline__ uint32_t permute_piece(uint32_t q, uint32_t from_hnd,
 
 constexpr int kUnroll = kSegPieces / 32;  // 16-byte pieces per lane per segment
 
-template <bool kTranspose>
+// Completion of a grid, fused into its last CTA: every thread makes its own
+// stores visible system-wide, the CTA counts itself done, and the CTA that
+// finishes last publishes the sequence number for the host (and resets the
+// counter for the fence slot's next use).
+__device__ __forceinline__ void complete_grid(const MoveDesc &d) {
+    __threadfence_system();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned int done;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(done)
+                     : "l"(d.fence_count)
+                     : "memory");
+        if (done == gridDim.x - 1) {
+            *d.fence_count = 0u;
+            __threadfence_system();
+            asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.fence_word),
+                         "l"(d.fence_seq)
+                         : "memory");
+        }
+    }
+}
+
+template <bool kTranspose, int kCap>
 __global__ void __launch_bounds__(kMoveThreads, 4)
-    kv_move_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ MoveIds ids) {
+    kv_move_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ IdsT<kCap> ids) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const uint32_t lc_per_item = d.nl * d.C;
 
-    for (uint32_t w = warp; w < d.total_segs; w += nwarps) {
+    bool skip = false;
+    if (d.skip_word != nullptr) {   // gated op: the gate decided once, before this launch
+        __shared__ int s_skip;
+        if (threadIdx.x == 0) {
+            unsigned long long v;
+            asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(d.skip_word));
+            s_skip = (v == d.skip_tag);
+        }
+        __syncthreads();
+        skip = s_skip != 0;
+    }
+
+    for (uint32_t w = skip ? d.total_segs : warp; w < d.total_segs; w += nwarps) {
         const uint32_t chunk = fdiv(w, d.div_segs);
         const uint32_t seg = w - chunk * d.segs;
         const uint32_t item = fdiv(chunk, d.div_lc);
@@ -143,12 +178,42 @@ __global__ void __launch_bounds__(kMoveThreads, 4)
             }
         }
     }
+    if (d.fence_word != nullptr) complete_grid(d);
 }
 
 __global__ void kv_mark_kernel(unsigned long long *word, unsigned long long seq) {
     if (threadIdx.x == 0) {
         __threadfence_system();
         asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(word), "l"(seq) : "memory");
+    }
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Ready-fence gate: bounded wait, never a trap.  The poll count is capped too,
+// so the wait ends even if the global timer were not advancing.
+__global__ void kv_gate_kernel(const unsigned long long *word, unsigned long long value,
+                               unsigned long long timeout_ns, unsigned long long *status,
+                               unsigned long long tag) {
+    if (threadIdx.x != 0) return;
+    const unsigned long long t0 = global_ns();
+    const unsigned long long max_polls = timeout_ns / 32ull + 4096ull;
+    unsigned int sleep_ns = 32;
+    for (unsigned long long polls = 0;; ++polls) {
+        unsigned long long v;
+        asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(word) : "memory");
+        if (v >= value) return;
+        if (global_ns() - t0 >= timeout_ns || polls >= max_polls) {
+            asm volatile("st.relaxed.sys.global.u64 [%0], %1;" ::"l"(status), "l"(tag) : "memory");
+            __threadfence_system();
+            return;
+        }
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 4096) sleep_ns <<= 1;
     }
 }
 
@@ -164,18 +229,39 @@ FastDiv make_fastdiv(uint32_t d) {
     return f;
 }
 
+template <int kCap>
+static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
+    IdsT<kCap> p;
+    for (uint32_t i = 0; i < d.n; ++i) {
+        p.a[i] = ids.a[i];
+        p.b[i] = ids.b[i];
+    }
+    if (d.transpose)
+        kv_move_kernel<true, kCap><<<ctas, kMoveThreads, 0, stream>>>(d, p);
+    else
+        kv_move_kernel<false, kCap><<<ctas, kMoveThreads, 0, stream>>>(d, p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
     (void)cudaGetLastError();   // report this launch's error, not an earlier call's
-    if (d.transpose)
-        kv_move_kernel<true><<<ctas, kMoveThreads, 0, stream>>>(d, ids);
-    else
-        kv_move_kernel<false><<<ctas, kMoveThreads, 0, stream>>>(d, ids);
-    return cudaGetLastError();
+    if (d.n > (uint32_t)kMaxItems) return cudaErrorInvalidValue;
+    if (d.n <= 64) return launch_cap<64>(d, ids, ctas, stream);
+    if (d.n <= 512) return launch_cap<512>(d, ids, ctas, stream);
+    return launch_cap<kMaxItems>(d, ids, ctas, stream);
 }
 
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream) {
     (void)cudaGetLastError();
     kv_mark_kernel<<<1, 32, 0, stream>>>(word, seq);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate(const unsigned long long *word, unsigned long long value,
+                        unsigned long long timeout_ns, unsigned long long *status,
+                        unsigned long long tag, cudaStream_t stream) {
+    (void)cudaGetLastError();
+    kv_gate_kernel<<<1, 32, 0, stream>>>(word, value, timeout_ns, status, tag);
     return cudaGetLastError();
 }
 

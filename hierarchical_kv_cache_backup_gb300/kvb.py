@@ -31,6 +31,7 @@ KV_ERR_TIMEOUT = 7
 KV_ERR_CUDA = 8
 KV_ERR_NO_MEMORY = 9
 KV_ERR_CLOSED = 10
+KV_ERR_ABORTED = 11
 STATUS_NAMES = {v: k for k, v in dict(globals()).items() if k.startswith("KV_OK") or k.startswith("KV_ERR_")}
 
 KV_LAYER_FIRST, KV_PAGE_FIRST = 0, 1
@@ -41,7 +42,7 @@ KVB_IPC_MAGIC = 0x4B564231
 # the symbols include/kvb.h declares
 EXPORTS = ("kv_pool_register", "kv_pool_export", "kv_pool_import", "kv_pool_close",
            "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
-           "kv_restore", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
+           "kv_restore", "kv_backup_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version")
@@ -91,6 +92,7 @@ def _load():
         "kv_host_close": (st, [vp]),
         "kv_backup": (st, [vp, vp, vp, vp, u32, vp, P(u64)]),
         "kv_restore": (st, [vp, vp, vp, vp, u32, i32, vp, P(u64)]),
+        "kv_backup_when_ready": (st, [vp, vp, vp, vp, u32, vp, u64, u64, vp, P(u64)]),
         "kv_device_gather": (st, [vp, vp, u64, u32, vp, u32, vp, P(u64)]),
         "kv_device_scatter": (st, [vp, vp, u64, u32, vp, u32, i32, vp, P(u64)]),
         "kv_backup_staged_noalloc": (st, [vp, vp, vp, vp, u32, vp]),
@@ -198,6 +200,18 @@ def kv_backup(pool: int, host: int, src_pages, host_slots, stream=None) -> int:
         raise ValueError("src_pages and host_slots differ in length")
     f = ctypes.c_uint64()
     _check(_lib.kv_backup(pool, host, pa, pb, a.size, stream, ctypes.byref(f)))
+    return f.value
+
+
+def kv_backup_when_ready(pool: int, host: int, src_pages, host_slots, ready_word: int,
+                         ready_value: int, ready_timeout_ns: int, stream=None) -> int:
+    a, pa = _ids(src_pages)
+    b, pb = _ids(host_slots)
+    if a.size != b.size:
+        raise ValueError("src_pages and host_slots differ in length")
+    f = ctypes.c_uint64()
+    _check(_lib.kv_backup_when_ready(pool, host, pa, pb, a.size, ready_word, ready_value,
+                                     ready_timeout_ns, stream, ctypes.byref(f)))
     return f.value
 
 

@@ -79,7 +79,8 @@ typedef enum {
     KV_ERR_TIMEOUT = 7,       /* fence not complete (query) / not in time    */
     KV_ERR_CUDA = 8,          /* a CUDA call failed; see kv_last_error()     */
     KV_ERR_NO_MEMORY = 9,     /* library could not allocate its resources    */
-    KV_ERR_CLOSED = 10        /* handle already closed                       */
+    KV_ERR_CLOSED = 10,       /* handle already closed                       */
+    KV_ERR_ABORTED = 11       /* op gave up: its ready fence never arrived   */
 } kv_status;
 
 typedef enum { KV_LAYER_FIRST = 0, KV_PAGE_FIRST = 1 } kv_order;
@@ -208,6 +209,22 @@ KVB_API kv_status kv_host_close(kv_host host);
 KVB_API kv_status kv_backup(kv_pool pool, kv_host host, const int32_t *src_pages,
                     const int32_t *host_slots, uint32_t n, void *stream, kv_fence *fence);
 
+/* BACKUP with its ready_fence ([RFC] §Device IPC data path: BACKUP(operation_id,
+ * source_pages, cache_keys, ready_fence); §Ownership: the scheduler publishes
+ * which source pages are safe to back up).  As kv_backup, but on the GPU the
+ * copy waits until the 64-bit word `ready_word` holds a value >= ready_value
+ * -- a word the scheduler, another process or the host sets when the pages
+ * are ready.  `ready_word` must be 8-B aligned device memory or page-locked
+ * host memory mapped into the device.  The wait is bounded: after
+ * ready_timeout_ns (<= 60 s, GPU global timer) it gives up, the operation moves
+ * no byte and its fence completes with KV_ERR_ABORTED (fail closed); nothing
+ * traps or hangs.  Always the zero-copy path.  Errors: as kv_backup, plus
+ * INVALID_ARG / ALIGNMENT for the ready word or timeout. */
+KVB_API kv_status kv_backup_when_ready(kv_pool pool, kv_host host, const int32_t *src_pages,
+                                       const int32_t *host_slots, uint32_t n,
+                                       const uint64_t *ready_word, uint64_t ready_value,
+                                       uint64_t ready_timeout_ns, void *stream, kv_fence *fence);
+
 /* RESTORE ([RFC] §Device IPC data path; layer-wise per [PR] §PP Prefetch
  * Ticket Path): for every i < n, page dst_pages[i] receives the units of
  * host slot host_slots[i] for every layer (layer = -1) or for that one layer
@@ -273,9 +290,10 @@ KVB_API kv_status kv_op_validate(const kv_layout *layout, uint32_t num_slots, in
  * when every byte of its operation is in place.  Completion is a sequence
  * number the GPU stores into a mapped pinned word after the operation, so
  * the host learns of it without a CUDA call.
- * kv_fence_query: OK when complete, TIMEOUT when not yet, INVALID_ARG for a
- * fence never issued.  kv_fence_wait: polls until complete or until
- * timeout_ns has passed (TIMEOUT).  kv_fence_stream_wait: makes `stream` wait
+ * kv_fence_query: OK when complete, TIMEOUT when not yet, ABORTED when the
+ * operation completed by giving up (kv_backup_when_ready whose ready fence
+ * never arrived), INVALID_ARG for a fence never issued.  kv_fence_wait: polls
+ * until complete or until timeout_ns has passed (TIMEOUT).  kv_fence_stream_wait: makes `stream` wait
  * for the fence on the GPU (the compute stream of a layer-wise restore). */
 KVB_API kv_status kv_fence_query(kv_fence fence);
 KVB_API kv_status kv_fence_wait(kv_fence fence, uint64_t timeout_ns);

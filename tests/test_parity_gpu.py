@@ -2,6 +2,7 @@
 buffers (the pool's whole allocation and the whole host tier, so untouched
 bytes are checked too)."""
 import itertools
+import time
 
 import numpy as np
 import pytest
@@ -348,5 +349,99 @@ def test_device_gather_scatter(wname):
         with pytest.raises(kvb.KvError) as e:   # host memory is not a device buffer
             kvb.kv_device_gather(rig.pool, rig.host.data_ptr(), rig.host.numel(), 0, src[:1])
         assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    finally:
+        rig.close()
+
+
+def _ready_word(device):
+    if device == "host":
+        return torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    return torch.zeros(1, dtype=torch.int64, device="cuda")
+
+
+@pytest.mark.parametrize("where", ["host", "device"])
+def test_backup_when_ready_waits_for_its_ready_fence(where):
+    """BACKUP's ready_fence: nothing moves until the word reaches the value; then the
+    result equals the oracle's backup."""
+    g = wl.TINY.geom
+    ids = wl.op_ids(wl.TINY)
+    rig = Rig(g, 16, seed=21)
+    word = _ready_word(where)
+    side = torch.cuda.Stream()
+    try:
+        snap = rig.snapshot()
+        want = rig.expect_backup(snap, ids.backup_src, ids.backup_slots)
+        s = torch.cuda.Stream()
+        f = kvb.kv_backup_when_ready(rig.pool, rig.hostt, ids.backup_src, ids.backup_slots,
+                                     word.data_ptr(), 7, 20_000_000_000, s.cuda_stream)
+        assert kvb.kv_fence_query(f) == kvb.KV_ERR_TIMEOUT          # still waiting
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_fence_wait(f, 50_000_000)
+        assert e.value.status == kvb.KV_ERR_TIMEOUT
+        assert np.array_equal(rig.host.numpy(), snap[1])           # nothing moved yet
+        if where == "host":
+            word[0] = 7
+        else:
+            with torch.cuda.stream(side):
+                word.fill_(9)
+        kvb.kv_fence_wait(f, 20_000_000_000)
+        rig.assert_equal(want)
+    finally:
+        rig.close()
+
+
+def test_backup_when_ready_gives_up_and_moves_nothing():
+    g = wl.LLAMA8B.geom.with_(P=64)
+    rig = Rig(g, 8, seed=22)
+    word = _ready_word("host")
+    try:
+        snap = rig.snapshot()
+        t0 = time.perf_counter()
+        f = kvb.kv_backup_when_ready(rig.pool, rig.hostt, [5, 9, 1], [0, 3, 7], word.data_ptr(),
+                                     1, 300_000_000)
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_fence_wait(f, 20_000_000_000)
+        assert e.value.status == kvb.KV_ERR_ABORTED, kvb.kv_last_error()
+        assert time.perf_counter() - t0 >= 0.25
+        assert kvb.kv_fence_query(f) == kvb.KV_ERR_ABORTED
+        rig.assert_equal(snap)                                      # fail closed
+        # the engine keeps working: the next backup lands normally
+        want = rig.expect_backup(snap, [5, 9, 1], [0, 3, 7])
+        kvb.kv_fence_wait(kvb.kv_backup(rig.pool, rig.hostt, [5, 9, 1], [0, 3, 7]),
+                          20_000_000_000)
+        rig.assert_equal(want)
+        with pytest.raises(kvb.KvError) as e:                      # bounded timeouts only
+            kvb.kv_backup_when_ready(rig.pool, rig.hostt, [1], [1], word.data_ptr(), 1,
+                                     61_000_000_000)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+        pageable = torch.zeros(1, dtype=torch.int64)
+        with pytest.raises(kvb.KvError) as e:                      # not visible to the GPU
+            kvb.kv_backup_when_ready(rig.pool, rig.hostt, [1], [1], pageable.data_ptr(), 1,
+                                     1_000_000)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    finally:
+        rig.close()
+
+
+def test_many_small_ops_reuse_fence_slots():
+    """More operations than fence slots (4096): slots and the fused completion counters
+    are reused correctly; every fence completes in order of issue on one stream."""
+    g = wl.Geometry(L=1, C=1, P=64, T=1, H=1, B=16, elem_bytes=1)
+    rig = Rig(g, 64, seed=23)
+    try:
+        snap = rig.snapshot()
+        r = np.random.default_rng(8)
+        fences = []
+        host = snap[1].copy()
+        import oracle
+        from gpu_rig import oracle_geom
+        for k in range(4500):
+            src = r.integers(0, 64, 3)
+            slots = r.permutation(64)[:3]
+            fences.append(kvb.kv_backup(rig.pool, rig.hostt, src, slots))
+            oracle.backup(oracle_geom(g), snap[0], host, src, slots, pool_offset=0)
+        kvb.kv_fence_wait(fences[-1], 60_000_000_000)
+        assert all(kvb.kv_fence_query(f) == kvb.KV_OK for f in fences[-100:])
+        rig.assert_equal((snap[0], host))
     finally:
         rig.close()
