@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--workload", choices=["llama8b", "mla_fp8", "trtllm_ipc"], default="llama8b")
     p.add_argument("--mode", choices=["zero_copy", "staged"], default="zero_copy")
     p.add_argument("--max-ctas", type=int, default=0)
+    p.add_argument("--no-bulk", action="store_true",
+                   help="HBM-only moves use the register kernel instead of bulk copies")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -58,6 +60,22 @@ def parse():
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def dist_max(x: float, dist, device=None) -> float:
+    """Max of a per-rank time over all ranks (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, steps: int, ranks: int, max_elapsed_s: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return ranks * bytes_per_rank_step * steps / max_elapsed_s / GB
 
 
 def measured_peaks():
@@ -244,7 +262,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     mode = kvb.KV_MODE_STAGED if args.mode == "staged" else kvb.KV_MODE_ZERO_COPY
-    kvb.kv_config_set(mode, args.max_ctas, 0)
+    kvb.kv_config_set(mode, args.max_ctas, 0, kvb.KV_CFG_NO_BULK if args.no_bulk else 0)
 
     w = {"llama8b": wl.LLAMA8B, "mla_fp8": wl.MLA_FP8, "trtllm_ipc": wl.TRTLLM}[args.workload]
     g = w.geom
@@ -372,15 +390,11 @@ def run_ours(args):
         t_end.record(s_a)
         barrier()
     launches = kvb.kv_launch_count() - l0
-    elapsed = t_start.elapsed_time(t_end) / 1000
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = dist_max(t_start.elapsed_time(t_end) / 1000, dist, dev)
     b_ms = [e[0].elapsed_time(e[1]) for e in evs]
     r_ms = [e[1].elapsed_time(e[2]) for e in evs]
     step_bytes = bytes_b + bytes_r
-    value = ws * step_bytes * args.steps / elapsed / GB
+    value = job_gbs(step_bytes, args.steps, ws, elapsed)
 
     # ---- end to end through the C ABI, host clock, fence wait every step
     barrier()
@@ -388,12 +402,8 @@ def run_ours(args):
     for k in range(args.steps):
         for f in step(k):
             kvb.kv_fence_wait(f, 60_000_000_000)
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = ws * step_bytes * args.steps / e2e_s / GB
+    e2e_s = dist_max(time.perf_counter() - t0, dist, dev)
+    e2e = job_gbs(step_bytes, args.steps, ws, e2e_s)
 
     # ---- device-side layout-transform gather (staged half) against HBM
     peaks, peak_src = measured_peaks()
@@ -413,8 +423,9 @@ def run_ours(args):
             if i >= 3:
                 ts.append(e0.elapsed_time(e1) / 1000)
         gb_s = 2 * n * g.page_bytes / statistics.median(ts) / GB
-        hbm = {"bound": "hbm", "kernel": "kv_move_kernel (device gather, pool -> device buffer "
-                                          "in host layout)",
+        hbm = {"bound": "hbm", "kernel": ("kv_move_kernel" if args.no_bulk or g.dev_heads != g.host_heads
+                                          else "kv_bulk_kernel") +
+                         " (device gather, pool -> device buffer in host layout)",
                "achieved": round(gb_s, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                "frac": round(gb_s / peaks["hbm_gbs"], 4),
                "traffic": recorded_traffic("device_gather_dram_bytes_per_launch"),

@@ -161,7 +161,7 @@ std::unordered_map<uint64_t, uint64_t> g_floor;    // instance -> lowest live ge
 uint64_t g_next_handle = 1;                         // handle ids are never reused
 uint64_t g_next_seq = 1;
 DevState g_dev[kMaxDevices];
-kv_config g_cfg = {KV_MODE_ZERO_COPY, 0, 0};
+kv_config g_cfg = {KV_MODE_ZERO_COPY, 0, 0, 0, 0};
 std::atomic<uint64_t> g_launches{0};
 
 constexpr uint64_t kDefaultStaging = 256ull << 20;
@@ -451,10 +451,13 @@ Side staging_side(char *base, const Geo &g, uint32_t heads, uint32_t nl, uint32_
 struct Plan {
     MoveDesc d;
     uint32_t max_items;   // items per launch
+    bool bulk = false;    // launch the bulk-copy kernel
 };
 
+// bulk: plan for the bulk-copy kernel (identity chunks, kBulkBytes segments)
+// instead of the register kernel (kSegPieces x 16-byte warp segments).
 kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint32_t l0,
-               uint32_t *err_dev, bool iter_dst, Plan *out) {
+               uint32_t *err_dev, bool iter_dst, Plan *out, bool bulk = false) {
     MoveDesc d{};
     d.src = src;
     d.dst = dst;
@@ -462,7 +465,8 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
     d.l0 = l0;
     d.C = (uint32_t)g.C;
     d.cb16 = (uint32_t)(g.cb / 16);
-    d.segs = (d.cb16 + kSegPieces - 1) / kSegPieces;
+    d.segs = bulk ? (uint32_t)((g.cb + kBulkBytes - 1) / kBulkBytes)
+                  : (d.cb16 + kSegPieces - 1) / kSegPieces;
     d.H = (uint32_t)g.H;
     d.T = (uint32_t)g.T;
     d.B16 = (uint32_t)(g.B / 16);
@@ -472,8 +476,13 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
     if (per_item == 0 || per_item > 0xffffffffull || (uint64_t)nl * g.C > 0xffffffffull)
         return fail(KV_ERR_LAYOUT, "one page needs %llu warp segments: too large",
                     (unsigned long long)per_item);
-    uint64_t m = 0xffffffffull / per_item;
+    // keep every launch's segment count below 2^31 so no grid-stride index wraps
+    uint64_t m = 0x7fffffffull / per_item;
+    if (m == 0)
+        return fail(KV_ERR_LAYOUT, "one page needs %llu segments: too large",
+                    (unsigned long long)per_item);
     out->max_items = (uint32_t)std::min<uint64_t>(m, (uint64_t)kMaxItems);
+    out->bulk = bulk;
     d.div_segs = make_fastdiv(d.segs);
     d.div_lc = make_fastdiv(nl * d.C);
     d.div_c = make_fastdiv(d.C);
@@ -492,9 +501,17 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
 // the other SMs to compute.  HBM-only moves use 4 CTAs per SM.
 constexpr int kLinkCtas = 64;
 
-int default_ctas(const DevState &s, bool touches_host) {
+int default_ctas(const DevState &s, bool touches_host, bool bulk = false) {
     if (g_cfg.max_ctas != 0) return (int)g_cfg.max_ctas;
+    if (bulk) return 3 * s.sms;   // 3 x 64 KiB rings fit one SM's shared memory
     return touches_host ? std::min(kLinkCtas, 4 * s.sms) : 4 * s.sms;
+}
+
+// HBM-only moves of identity chunks go through the bulk-copy kernel unless
+// the caller turned it off (KV_CFG_NO_BULK).
+bool use_bulk(const Geo &g, const Side &a, const Side &b) {
+    const bool transpose = a.hnd != b.hnd && g.H > 1 && g.T > 1;
+    return !transpose && (g_cfg.flags & KV_CFG_NO_BULK) == 0;
 }
 
 // Launches the move for items [0, n) of (a, b) in slices of at most max_items.
@@ -522,11 +539,11 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
             std::memcpy(ids.b, b + i0, m * sizeof(int32_t));
         p.d.n = m;
         p.d.total_segs = m * p.d.nl * p.d.C * p.d.segs;
-        const uint32_t warps_needed = p.d.total_segs;
-        const uint32_t per_cta = kMoveThreads / 32;
-        const uint64_t need = (warps_needed + per_cta - 1) / per_cta;
+        const uint32_t per_cta = p.bulk ? 1u : (uint32_t)(kMoveThreads / 32);   // segments in flight
+        const uint64_t need = ((uint64_t)p.d.total_segs + per_cta - 1) / per_cta;
         const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
-        cudaError_t e = launch_move(p.d, ids, ctas, stream);
+        cudaError_t e = p.bulk ? launch_bulk(p.d, ids, ctas, stream)
+                               : launch_move(p.d, ids, ctas, stream);
         if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -669,12 +686,14 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             for (uint32_t i0 = 0; i0 < n; i0 += (uint32_t)std::min<uint64_t>(fit, n)) {
                 const uint32_t m = (uint32_t)std::min<uint64_t>(fit, n - i0);
                 const Side ss = staging_side(stg, pool->g, host->heads, g_n, la, m);
+                const bool bulk = use_bulk(pool->g, ps, ss);
                 Plan p;
                 st = plan(pool->g, backup ? ps : ss, backup ? ss : ps, g_n, la, ds.err_dev, backup,
-                          &p);
+                          &p, bulk);
                 if (st != KV_OK) return st;
+                const int ctas = default_ctas(ds, false, bulk);
                 if (backup) {
-                    st = run_moves(p, a + i0, nullptr, m, default_ctas(ds, false), stream, true);
+                    st = run_moves(p, a + i0, nullptr, m, ctas, stream, true);
                     if (st == KV_OK)
                         st = staged_copies(*host, stg, b + i0, m, gb, host_off, true, stream);
                 } else {
@@ -683,8 +702,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                         // staging item k -> dst page b[i0 + k]: a = staging index, b = page
                         idx.resize(m);
                         for (uint32_t k = 0; k < m; ++k) idx[k] = (int32_t)k;
-                        st = run_moves(p, idx.data(), b + i0, m, default_ctas(ds, false), stream,
-                                       false);
+                        st = run_moves(p, idx.data(), b + i0, m, ctas, stream, false);
                     }
                 }
                 if (st != KV_OK) return st;
@@ -742,20 +760,22 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
             return fail(KV_ERR_INVALID_ARG, "buffer %p is not device memory of device %d", buf, d);
         const Side ps = pool_side(*pool);
         const Side bs = staging_side((char *)buf, g, buf_heads, nl, l0, n);
+        const bool bulk = use_bulk(g, ps, bs);
         Plan p;
-        st = plan(g, kind == 0 ? ps : bs, kind == 0 ? bs : ps, nl, l0, ds.err_dev, kind == 0, &p);
+        st = plan(g, kind == 0 ? ps : bs, kind == 0 ? bs : ps, nl, l0, ds.err_dev, kind == 0, &p,
+                  bulk);
         if (st != KV_OK) return st;
         FenceSlot fs;
         st = reserve_fence(d, &fs);
         if (st != KV_OK) return st;
+        const int ctas = default_ctas(ds, false, bulk);
         if (kind == 0) {
-            st = run_moves(p, pages, nullptr, n, default_ctas(ds, false), stream, true, &ds, &fs);
+            st = run_moves(p, pages, nullptr, n, ctas, stream, true, &ds, &fs);
         } else {
             static thread_local std::vector<int32_t> idx;
             idx.resize(n);
             for (uint32_t k = 0; k < n; ++k) idx[k] = (int32_t)k;
-            st = run_moves(p, idx.data(), pages, n, default_ctas(ds, false), stream, false, &ds,
-                           &fs);
+            st = run_moves(p, idx.data(), pages, n, ctas, stream, false, &ds, &fs);
         }
         if (st != KV_OK) return st;
         return commit_fence(d, fs, false, stream, fence);
@@ -878,6 +898,8 @@ kv_status kv_config_set(const kv_config *cfg) {
     if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
     if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
         return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
+    if ((cfg->flags & ~(uint32_t)KV_CFG_NO_BULK) != 0 || cfg->reserved != 0)
+        return fail(KV_ERR_INVALID_ARG, "unknown config flags %#x or reserved != 0", cfg->flags);
     std::lock_guard<std::mutex> lk(g_mu);
     g_cfg = *cfg;
     return KV_OK;

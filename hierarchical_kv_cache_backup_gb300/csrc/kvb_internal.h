@@ -36,6 +36,12 @@ struct Side {
 constexpr int kMaxItems = 2048;     // (a, b) id pairs per launch
 constexpr int kSegPieces = 256;     // 16-byte pieces a warp moves per segment (4 KiB)
 constexpr int kMoveThreads = 256;   // threads per CTA of the move kernel
+// Bulk-copy (TMA) variant for HBM-only moves whose two sides share a head
+// order: one warp per CTA, lane 0 streams each chunk through a ring of
+// kBulkStages shared-memory buffers of kBulkBytes with cp.async.bulk.
+constexpr int kBulkStages = 4;
+constexpr uint32_t kBulkBytes = 16384;
+constexpr int kBulkThreads = 32;
 
 struct MoveDesc {
     Side src, dst;
@@ -75,6 +81,9 @@ using MoveIds = IdsT<kMaxItems>;
 
 // Launch the gather/scatter kernel on `stream` with `ctas` CTAs.
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
+// Launch the bulk-copy variant (identity chunks only; d.segs / d.div_segs /
+// d.total_segs count kBulkBytes segments).  `ctas` CTAs of kBulkThreads.
+cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
 // Launch the completion marker: stores `seq` to `word` (system scope, release)
 // once everything before it on `stream` has finished.
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream);

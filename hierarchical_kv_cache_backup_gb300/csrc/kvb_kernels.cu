@@ -181,17 +181,150 @@ __global__ void __launch_bounds__(kMoveThreads, 4)
     if (d.fence_word != nullptr) complete_grid(d);
 }
 
-__global__ void kv_mark_kernel(unsigned long long *word, unsigned long long seq) {
-    if (threadIdx.x == 0) {
-        __threadfence_system();
-        asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(word), "l"(seq) : "memory");
-    }
-}
+// ----------------------------------------------------------- bulk (TMA) path
 
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Bounded wait for an mbarrier phase: gives up after ~2 s of GPU time.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t polls = 0; polls < (1u << 30); ++polls) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((polls & 255u) == 255u && global_ns() - t0 > 2000000000ull) return false;
+    }
+    return false;
+}
+
+struct BulkSeg {
+    const char *src;
+    char *dst;
+    uint32_t bytes;
+    bool ok;
+};
+
+__device__ __forceinline__ BulkSeg bulk_segment(const MoveDesc &d, const int32_t *ia_arr,
+                                                const int32_t *ib_arr, uint32_t w) {
+    const uint32_t chunk = fdiv(w, d.div_segs);
+    const uint32_t seg = w - chunk * d.segs;
+    const uint32_t item = fdiv(chunk, d.div_lc);
+    const uint32_t lc = chunk - item * (d.nl * d.C);
+    const uint32_t lr = fdiv(lc, d.div_c);
+    const uint32_t c = lc - lr * d.C;
+    const uint64_t l = d.l0 + lr;
+    const uint32_t ia = (uint32_t)ia_arr[item];
+    const uint32_t ib = (uint32_t)ib_arr[item];
+    BulkSeg r;
+    r.ok = ia < d.src.id_limit && ib < d.dst.id_limit;
+    const uint64_t off = (uint64_t)seg * kBulkBytes;
+    const uint64_t cb = (uint64_t)d.cb16 * 16u;
+    r.bytes = (uint32_t)min((uint64_t)kBulkBytes, cb - off);
+    r.src = reinterpret_cast<const char *>(d.src.base + ia * d.src.s_id + l * d.src.s_l +
+                                           c * d.src.s_c + off);
+    r.dst = reinterpret_cast<char *>(d.dst.base + ib * d.dst.s_id + l * d.dst.s_l +
+                                     c * d.dst.s_c + off);
+    return r;
+}
+
+template <int kCap>
+__global__ void __launch_bounds__(kBulkThreads)
+    kv_bulk_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ IdsT<kCap> ids) {
+    extern __shared__ __align__(128) unsigned char ring[];   // kBulkStages x kBulkBytes
+    __shared__ __align__(8) unsigned long long bar[kBulkStages];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBulkStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+        const uint32_t first = blockIdx.x, step = gridDim.x;
+        uint32_t parity = 0;          // bit s: phase parity expected next on stage s
+        bool failed = false;
+        // prologue: fill every stage
+        for (int s = 0; s < kBulkStages; ++s) {
+            const uint32_t w = first + s * step;
+            if (w >= d.total_segs) break;
+            const BulkSeg g = bulk_segment(d, ids.a, ids.b, w);
+            const uint32_t b = smem_addr(&bar[s]);
+            const uint32_t buf = smem_addr(ring + s * kBulkBytes);
+            const uint32_t bytes = g.ok ? g.bytes : 0u;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b),
+                         "r"(bytes) : "memory");
+            if (bytes)
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                    "[%0], [%1], %2, [%3];" ::"r"(buf), "l"(g.src), "r"(bytes), "r"(b)
+                    : "memory");
+        }
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t w = first + i * step;
+            if (w >= d.total_segs) break;
+            const int s = (int)(i % kBulkStages);
+            const uint32_t b = smem_addr(&bar[s]);
+            const uint32_t buf = smem_addr(ring + s * kBulkBytes);
+            if (!mbar_wait(b, (parity >> s) & 1u)) {
+                failed = true;
+                break;
+            }
+            parity ^= 1u << s;
+            const BulkSeg g = bulk_segment(d, ids.a, ids.b, w);
+            if (g.ok) {
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                 g.dst), "r"(buf), "r"(g.bytes)
+                             : "memory");
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            } else if (d.err != nullptr) {
+                *(volatile uint32_t *)d.err = 1u;   // unreachable after host validation
+            }
+            const uint32_t wn = w + kBulkStages * step;   // refill this stage
+            if (wn < d.total_segs) {
+                // the store must have finished reading this stage first
+                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                const BulkSeg gn = bulk_segment(d, ids.a, ids.b, wn);
+                const uint32_t bytes = gn.ok ? gn.bytes : 0u;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b),
+                             "r"(bytes) : "memory");
+                if (bytes)
+                    asm volatile(
+                        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                        "[%0], [%1], %2, [%3];" ::"r"(buf), "l"(gn.src), "r"(bytes), "r"(b)
+                        : "memory");
+            }
+        }
+        if (failed) {
+            // Never leave while a load may still be writing this CTA's shared
+            // memory: wait (bounded) for every stage, then report.
+            for (int s = 0; s < kBulkStages; ++s)
+                mbar_wait(smem_addr(&bar[s]), (parity >> s) & 1u);
+            if (d.err != nullptr) *(volatile uint32_t *)d.err = 2u;
+        }
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // every store complete
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    if (d.fence_word != nullptr) complete_grid(d);
+}
+
+__global__ void kv_mark_kernel(unsigned long long *word, unsigned long long seq) {
+    if (threadIdx.x == 0) {
+        __threadfence_system();
+        asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(word), "l"(seq) : "memory");
+    }
 }
 
 // Ready-fence gate: bounded wait, never a trap.  The poll count is capped too,
@@ -241,6 +374,34 @@ static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, c
     else
         kv_move_kernel<false, kCap><<<ctas, kMoveThreads, 0, stream>>>(d, p);
     return cudaGetLastError();
+}
+
+template <int kCap>
+static cudaError_t launch_bulk_cap(const MoveDesc &d, const MoveIds &ids, int ctas,
+                                   cudaStream_t stream) {
+    static bool attr_set = false;   // per instantiation; set once (host calls are serialised)
+    const int smem = kBulkStages * (int)kBulkBytes;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kv_bulk_kernel<kCap>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    IdsT<kCap> p;
+    for (uint32_t i = 0; i < d.n; ++i) {
+        p.a[i] = ids.a[i];
+        p.b[i] = ids.b[i];
+    }
+    kv_bulk_kernel<kCap><<<ctas, kBulkThreads, smem, stream>>>(d, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
+    (void)cudaGetLastError();
+    if (d.n > (uint32_t)kMaxItems || d.transpose) return cudaErrorInvalidValue;
+    if (d.n <= 64) return launch_bulk_cap<64>(d, ids, ctas, stream);
+    if (d.n <= 512) return launch_bulk_cap<512>(d, ids, ctas, stream);
+    return launch_bulk_cap<kMaxItems>(d, ids, ctas, stream);
 }
 
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {

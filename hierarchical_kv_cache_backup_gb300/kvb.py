@@ -37,6 +37,7 @@ STATUS_NAMES = {v: k for k, v in dict(globals()).items() if k.startswith("KV_OK"
 KV_LAYER_FIRST, KV_PAGE_FIRST = 0, 1
 KV_NHD, KV_HND = 0, 1
 KV_MODE_ZERO_COPY, KV_MODE_STAGED = 0, 1
+KV_CFG_NO_BULK = 1
 KVB_IPC_MAGIC = 0x4B564231
 
 # the symbols include/kvb.h declares
@@ -70,7 +71,8 @@ class kv_ipc_desc(ctypes.Structure):
 
 class kv_config(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_uint32), ("max_ctas", ctypes.c_uint32),
-                ("staging_bytes", ctypes.c_uint64)]
+                ("staging_bytes", ctypes.c_uint64), ("flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
 
 
 def _load():
@@ -282,8 +284,9 @@ def kv_config_get() -> kv_config:
     return c
 
 
-def kv_config_set(mode: int = KV_MODE_ZERO_COPY, max_ctas: int = 0, staging_bytes: int = 0):
-    _check(_lib.kv_config_set(ctypes.byref(kv_config(mode, max_ctas, staging_bytes))))
+def kv_config_set(mode: int = KV_MODE_ZERO_COPY, max_ctas: int = 0, staging_bytes: int = 0,
+                  flags: int = 0):
+    _check(_lib.kv_config_set(ctypes.byref(kv_config(mode, max_ctas, staging_bytes, flags, 0))))
 
 
 def kv_layout_page_bytes(layout: kv_layout) -> int:

@@ -129,10 +129,15 @@ typedef struct {
  * the copy engine moves the staging buffer to / from the host tier. */
 typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1 } kv_mode;
 
+/* kv_config.flags */
+#define KV_CFG_NO_BULK 1u   /* HBM-only moves use the register kernel, not bulk copies */
+
 typedef struct {
     uint32_t mode;           /* kv_mode                                         */
     uint32_t max_ctas;       /* CTA cap of the transfer kernel; 0 = default     */
     uint64_t staging_bytes;  /* STAGED: device staging bytes; 0 = default       */
+    uint32_t flags;          /* KV_CFG_* bits                                   */
+    uint32_t reserved;       /* must be 0                                       */
 } kv_config;
 
 /* ------------------------------------------------------------------ pools */
