@@ -144,6 +144,9 @@ struct DevState {
     uint32_t *err = nullptr;                 // sticky "kernel met a bad id" word
     uint32_t *err_dev = nullptr;
     uint32_t *counters = nullptr;            // device: finished-CTA counters, one per slot
+    uint32_t *aux = nullptr;                 // device: per-slot layer counters, kRing each of
+                                             // done / published / work / lock (progressive)
+    bool wait_value = false;                 // GPU-side waits on fence words supported
     cudaEvent_t ev[kRing] = {};
     uint64_t slot_seq[kRing] = {};
     int sms = 0;
@@ -215,6 +218,36 @@ kv_status address_range(const void *p, uintptr_t *base, size_t *size) {
     return KV_OK;
 }
 
+// Driver entry points fetched through the runtime (no link-time libcuda).
+typedef CUresult (*StreamWaitValue64Fn)(CUstream, CUdeviceptr, cuuint64_t, unsigned int);
+typedef CUresult (*DeviceGetFn)(CUdevice *, int);
+typedef CUresult (*DeviceGetAttributeFn)(int *, CUdevice_attribute, CUdevice);
+
+void *driver_fn(const char *name) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return f;
+}
+
+StreamWaitValue64Fn g_wait_value64 = nullptr;
+
+// GPU-side waits on a 64-bit word (a stream waits until fence word >= seq)
+// need the driver's 64-bit stream memory operations.
+bool stream_wait_value_supported(int ordinal) {
+    auto get = (DeviceGetFn)driver_fn("cuDeviceGet");
+    auto attr = (DeviceGetAttributeFn)driver_fn("cuDeviceGetAttribute");
+    g_wait_value64 = (StreamWaitValue64Fn)driver_fn("cuStreamWaitValue64");
+    if (get == nullptr || attr == nullptr || g_wait_value64 == nullptr) return false;
+    CUdevice dev;
+    int v = 0;
+    if (get(&dev, ordinal) != CUDA_SUCCESS) return false;
+    if (attr(&v, CU_DEVICE_ATTRIBUTE_CAN_USE_64_BIT_STREAM_MEM_OPS, dev) != CUDA_SUCCESS) return false;
+    return v != 0;
+}
+
 kv_status init_device(int d) {
     if (d < 0 || d >= kMaxDevices) return fail(KV_ERR_INVALID_ARG, "device %d out of range", d);
     DevState &s = g_dev[d];
@@ -233,13 +266,15 @@ kv_status init_device(int d) {
         return cuda_fail(e, "cudaHostGetDevicePointer(fence words)");
     }
     void *cnt = nullptr;
-    e = cudaMalloc(&cnt, kRing * sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaMemset(cnt, 0, kRing * sizeof(uint32_t));
+    e = cudaMalloc(&cnt, 5 * kRing * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(cnt, 0, 5 * kRing * sizeof(uint32_t));
     if (e != cudaSuccess) {
         if (cnt) cudaFree(cnt);
         cudaFreeHost(mem);
         return cuda_fail(e, "cudaMalloc(completion counters)");
     }
+    s.aux = (uint32_t *)cnt + kRing;
+    s.wait_value = stream_wait_value_supported(d);
     s.words = (unsigned long long *)mem;
     s.words_dev = (unsigned long long *)dmem;
     s.status = s.words + kRing;
@@ -300,6 +335,35 @@ kv_status reserve_fence(int d, FenceSlot *out) {
     }
     out->seq = seq;
     out->k = k;
+    return KV_OK;
+}
+
+// Reserves `count` consecutive sequence numbers (count <= kRing / 2), each
+// slot free; returns the first.  Nothing is committed.
+kv_status reserve_fence_range(int d, uint32_t count, uint64_t *seq0) {
+    DevState &s = g_dev[d];
+    const uint64_t first = g_next_seq;
+    if (first + count > kSeqMask) return fail(KV_ERR_NO_MEMORY, "fence sequence space exhausted");
+    for (uint32_t j = 0; j < count; ++j) {
+        const int k = (int)((first + j) % kRing);
+        if (s.slot_seq[k] != 0 && load_acquire(&s.words[k]) < s.slot_seq[k]) {
+            const double deadline = now_ns() + 30e9;
+            while (load_acquire(&s.words[k]) < s.slot_seq[k]) {
+                if (now_ns() > deadline)
+                    return fail(KV_ERR_NO_MEMORY, "%d fences in flight: fence ring exhausted",
+                                kRing);
+                sched_yield();
+            }
+        }
+        if (s.ev[k] == nullptr) {
+            cudaError_t e = cudaEventCreateWithFlags(&s.ev[k], cudaEventDisableTiming);
+            if (e != cudaSuccess) {
+                s.ev[k] = nullptr;
+                return cuda_fail(e, "cudaEventCreate(fence)");
+            }
+        }
+    }
+    *seq0 = first;
     return KV_OK;
 }
 
@@ -452,6 +516,7 @@ struct Plan {
     MoveDesc d;
     uint32_t max_items;   // items per launch
     bool bulk = false;    // launch the bulk-copy kernel
+    int threads = kMoveThreads;   // CTA size of the register kernel
 };
 
 // bulk: plan for the bulk-copy kernel (identity chunks, kBulkBytes segments)
@@ -494,17 +559,50 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
     return KV_OK;
 }
 
-// CTAs of a move kernel.  Host-link moves saturate the link with few CTAs
+// CTAs of a move kernel.  Host-link moves saturate the link with few threads
 // (measured on GB300: 16 CTAs of 256 threads reach the D2H peak, 32 the H2D
 // peak, and 64 + 64 give the best D2H + H2D mix, while more CTAs per direction
-// lose bidirectional throughput), so they are capped at kLinkCtas and leave
-// the other SMs to compute.  HBM-only moves use 4 CTAs per SM.
-constexpr int kLinkCtas = 64;
+// lose bidirectional throughput).  By default they run the same 16,384
+// threads as 16 CTAs of 1024, one per SM: whole SMs stay free for compute
+// kernels beside them, where 64 small CTAs would sit on 64 SMs and keep large
+// compute CTAs off all of them.  HBM-only moves use 4 CTAs of 256 per SM.
+constexpr int kLinkCtas = 64;       // CTAs of kMoveThreads
+constexpr int kLinkWideCtas = 16;   // CTAs of kWideThreads
+// Progressive layer restores exist to run beside each layer's forward: 8 wide
+// CTAs (8 SMs) still reach 98% of the H2D peak and cut the time of a 61-layer
+// restore pipelined with a per-layer GEMM from 4.26 ms (16 CTAs) to 3.54 ms.
+constexpr int kOverlapWideCtas = 8;
+
+int link_threads() { return g_cfg.cta_threads ? (int)g_cfg.cta_threads : kWideThreads; }
+
+// Turns a plan into a progressive multi-layer plan for n items (one launch).
+kv_status plan_layer_major(Plan &p, uint32_t n, const DevState &ds, uint64_t seq0) {
+    MoveDesc &d = p.d;
+    const uint64_t pls = (uint64_t)n * d.C * d.segs;
+    if (n > p.max_items || pls * d.nl > 0x7fffffffull || pls == 0)
+        return fail(KV_ERR_OUT_OF_RANGE, "%u pages x %u layers is too large for one progressive "
+                    "restore", n, d.nl);
+    d.layer_major = 1;
+    d.per_layer_segs = (uint32_t)pls;
+    d.div_pls = make_fastdiv((uint32_t)pls);
+    d.div_cs = make_fastdiv(d.C * d.segs);
+    d.lay_words = ds.words_dev;
+    d.lay_seq0 = seq0;
+    d.lay_ring = kRing;
+    const uint32_t k_last = (uint32_t)((seq0 + d.nl - 1) % kRing);
+    d.lay_done = ds.aux;                        // done[k] for each layer's slot k
+    d.lay_published = ds.aux + kRing + k_last;
+    d.lay_work = ds.aux + 2 * kRing + k_last;
+    d.lay_lock = ds.aux + 3 * kRing + k_last;
+    return KV_OK;
+}
 
 int default_ctas(const DevState &s, bool touches_host, bool bulk = false) {
     if (g_cfg.max_ctas != 0) return (int)g_cfg.max_ctas;
     if (bulk) return 3 * s.sms;   // 3 x 64 KiB rings fit one SM's shared memory
-    return touches_host ? std::min(kLinkCtas, 4 * s.sms) : 4 * s.sms;
+    if (!touches_host) return 4 * s.sms;
+    return link_threads() == kWideThreads ? std::min(kLinkWideCtas, s.sms)
+                                          : std::min(kLinkCtas, 4 * s.sms);
 }
 
 // HBM-only moves of identity chunks go through the bulk-copy kernel unless
@@ -539,11 +637,11 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
             std::memcpy(ids.b, b + i0, m * sizeof(int32_t));
         p.d.n = m;
         p.d.total_segs = m * p.d.nl * p.d.C * p.d.segs;
-        const uint32_t per_cta = p.bulk ? 1u : (uint32_t)(kMoveThreads / 32);   // segments in flight
+        const uint32_t per_cta = p.bulk ? 1u : (uint32_t)(p.threads / 32);   // segments in flight
         const uint64_t need = ((uint64_t)p.d.total_segs + per_cta - 1) / per_cta;
         const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
         cudaError_t e = p.bulk ? launch_bulk(p.d, ids, ctas, stream)
-                               : launch_move(p.d, ids, ctas, stream);
+                               : launch_move(p.d, ids, ctas, p.threads, stream);
         if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -656,6 +754,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             p.d.skip_word = ds.status_dev + fs.k;
             p.d.skip_tag = fs.seq;
         }
+        p.threads = link_threads();
         st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false, &ds, &fs);
         if (st != KV_OK) return st;
         fused = true;
@@ -858,7 +957,7 @@ int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_hand
     const uint64_t need = (p.d.total_segs + per_cta - 1) / per_cta;
     const int cap = g_cfg.max_ctas ? (int)g_cfg.max_ctas : 4 * std::max(sms, 1);
     const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)cap));
-    cudaError_t e = launch_move(p.d, ids, ctas, stream);
+    cudaError_t e = launch_move(p.d, ids, ctas, kMoveThreads, stream);
     if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
     g_launches.fetch_add(1, std::memory_order_relaxed);
     return staged_copies(*host, (char *)staging, slots, n, g.pb, 0, true, stream);
@@ -898,8 +997,12 @@ kv_status kv_config_set(const kv_config *cfg) {
     if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
     if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
         return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
-    if ((cfg->flags & ~(uint32_t)KV_CFG_NO_BULK) != 0 || cfg->reserved != 0)
-        return fail(KV_ERR_INVALID_ARG, "unknown config flags %#x or reserved != 0", cfg->flags);
+    if ((cfg->flags & ~(uint32_t)KV_CFG_NO_BULK) != 0)
+        return fail(KV_ERR_INVALID_ARG, "unknown config flags %#x", cfg->flags);
+    if (cfg->cta_threads != 0 && cfg->cta_threads != (uint32_t)kMoveThreads &&
+        cfg->cta_threads != (uint32_t)kWideThreads)
+        return fail(KV_ERR_INVALID_ARG, "cta_threads must be 0, %d or %d", kMoveThreads,
+                    kWideThreads);
     std::lock_guard<std::mutex> lk(g_mu);
     g_cfg = *cfg;
     return KV_OK;
@@ -1162,6 +1265,89 @@ kv_status kv_backup_when_ready(kv_pool pool, kv_host host, const int32_t *src_pa
                  (const unsigned long long *)dev_word, ready_value, ready_timeout_ns);
 }
 
+kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_slots,
+                            const int32_t *dst_pages, uint32_t n, uint32_t first_layer,
+                            uint32_t num_layers, void *stream_v, kv_fence *fences) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (fences == nullptr) return fail(KV_ERR_INVALID_ARG, "fence output array is NULL");
+    if (pool_h == nullptr || host_h == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "pool or host handle is NULL");
+    PoolObj *pool = find_pool(pool_h);
+    if (pool == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    HostObj *host = find_host(host_h);
+    if (host == nullptr) return fail(KV_ERR_CLOSED, "host handle is closed or unknown");
+    auto fl = g_floor.find(pool->instance_id);
+    if (fl != g_floor.end() && pool->generation < fl->second)
+        return fail(KV_ERR_STALE, "pool generation %llu of instance %llu is retired",
+                    (unsigned long long)pool->generation, (unsigned long long)pool->instance_id);
+    if (!same_slot_geometry(pool->g, host->g))
+        return fail(KV_ERR_LAYOUT, "pool and host tier have different page geometry");
+    if (num_layers == 0 || num_layers > kRing / 2 || (uint64_t)first_layer + num_layers > pool->g.L)
+        return fail(KV_ERR_OUT_OF_RANGE, "layers [%u, %u + %u) are not inside [0, %llu) or exceed "
+                    "%d", first_layer, first_layer, num_layers, (unsigned long long)pool->g.L,
+                    kRing / 2);
+    if (n > (uint32_t)kMaxItems)
+        return fail(KV_ERR_OUT_OF_RANGE, "n = %u exceeds the %d pages of one progressive restore",
+                    n, kMaxItems);
+    kv_status st = check_op(pool->g, host->num_slots, 1, host_slots, dst_pages, n, -1);
+    if (st != KV_OK) return st;
+    const int d = pool->device;
+    DeviceGuard guard(d);
+    st = init_device(d);
+    if (st != KV_OK) return st;
+    DevState &ds = g_dev[d];
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    uint64_t seq0 = 0;
+    st = reserve_fence_range(d, num_layers, &seq0);
+    if (st != KV_OK) return st;
+    if (n > 0) {
+        // Counters of this call, zeroed in stream order.  The last slot's previous
+        // user must have fully finished (its kernel may still be fetching tickets
+        // after publishing its last fence): wait for that op's event first.
+        const uint32_t k0 = (uint32_t)(seq0 % kRing);
+        const uint32_t k_last = (uint32_t)((seq0 + num_layers - 1) % kRing);
+        cudaError_t e = cudaSuccess;
+        if (ds.slot_seq[k_last] != 0) e = cudaStreamWaitEvent(stream, ds.ev[k_last], 0);
+        const uint32_t first_run = std::min<uint32_t>(num_layers, kRing - k0);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(ds.aux + k0, 0, first_run * sizeof(uint32_t), stream);
+        if (e == cudaSuccess && first_run < num_layers)
+            e = cudaMemsetAsync(ds.aux, 0, (num_layers - first_run) * sizeof(uint32_t), stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(ds.aux + kRing + k_last, 0, sizeof(uint32_t), stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(ds.aux + 2 * kRing + k_last, 0, sizeof(uint32_t), stream);
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(ds.aux + 3 * kRing + k_last, 0, sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "zeroing the layer counters");
+        const Side ps = pool_side(*pool), hs = host_side(*host);
+        Plan p;
+        st = plan(pool->g, hs, ps, num_layers, first_layer, ds.err_dev, false, &p);
+        if (st == KV_OK) st = plan_layer_major(p, n, ds, seq0);
+        p.threads = link_threads();
+        const int ctas = g_cfg.max_ctas ? (int)g_cfg.max_ctas
+                         : p.threads == kWideThreads ? std::min(kOverlapWideCtas, ds.sms)
+                                                     : default_ctas(ds, true);
+        if (st == KV_OK) st = run_moves(p, host_slots, dst_pages, n, ctas, stream, false);
+        if (st != KV_OK) return st;
+    } else {
+        for (uint32_t j = 0; j < num_layers; ++j) {   // nothing to move: mark every layer
+            cudaError_t e = launch_mark(ds.words_dev + (seq0 + j) % kRing, seq0 + j, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "launch of the completion marker");
+            g_launches.fetch_add(1, std::memory_order_relaxed);
+        }
+    }
+    for (uint32_t j = 0; j < num_layers; ++j) {
+        const int k = (int)((seq0 + j) % kRing);
+        cudaError_t e = cudaEventRecord(ds.ev[k], stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(fence)");
+        ds.slot_seq[k] = seq0 + j;
+        fences[j] = ((uint64_t)d << 56) | (seq0 + j);
+    }
+    g_next_seq = seq0 + num_layers;
+    return KV_OK;
+}
+
 kv_status kv_restore(kv_pool pool, kv_host host, const int32_t *host_slots,
                      const int32_t *dst_pages, uint32_t n, int32_t layer, void *stream,
                      kv_fence *fence) {
@@ -1221,10 +1407,21 @@ kv_status kv_fence_stream_wait(kv_fence f, void *stream) {
     if (st != KV_OK) return st;
     if (done) return KV_OK;
     std::lock_guard<std::mutex> lk(g_mu);
-    // The slot's event is this fence's, or a later one recorded only after this
-    // fence completed (issue_fence waits before reusing a slot): never too early.
     DeviceGuard guard(d);
-    cudaError_t e = cudaStreamWaitEvent((cudaStream_t)stream, g_dev[d].ev[k], 0);
+    DevState &ds = g_dev[d];
+    if (ds.wait_value) {
+        // Wait on the GPU for the fence word itself: right for fences that a
+        // kernel publishes before it ends (progressive layers), and slot reuse
+        // only ever raises the word, so it is never early.
+        CUresult r = g_wait_value64((CUstream)stream, (CUdeviceptr)(uintptr_t)(ds.words_dev + k),
+                                    (cuuint64_t)(f & kSeqMask), CU_STREAM_WAIT_VALUE_GEQ);
+        if (r != CUDA_SUCCESS)
+            return fail(KV_ERR_CUDA, "cuStreamWaitValue64(fence word) failed (CUresult %d)", (int)r);
+        return KV_OK;
+    }
+    // The slot's event is this fence's, or a later one recorded only after this
+    // fence completed (slots are reused only then): never too early.
+    cudaError_t e = cudaStreamWaitEvent((cudaStream_t)stream, ds.ev[k], 0);
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(fence)");
     return KV_OK;
 }

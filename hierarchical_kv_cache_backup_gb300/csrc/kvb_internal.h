@@ -35,7 +35,8 @@ struct Side {
 // buffer, copy or ring is needed for them.
 constexpr int kMaxItems = 2048;     // (a, b) id pairs per launch
 constexpr int kSegPieces = 256;     // 16-byte pieces a warp moves per segment (4 KiB)
-constexpr int kMoveThreads = 256;   // threads per CTA of the move kernel
+constexpr int kMoveThreads = 256;   // threads per CTA of the move kernel (HBM-only moves)
+constexpr int kWideThreads = 1024;  // wide CTAs: host-link moves packed onto few SMs
 // Bulk-copy (TMA) variant for HBM-only moves whose two sides share a head
 // order: one warp per CTA, lane 0 streams each chunk through a ring of
 // kBulkStages shared-memory buffers of kBulkBytes with cp.async.bulk.
@@ -67,6 +68,19 @@ struct MoveDesc {
     // ready-fence gate that ran before this kernel), no byte is moved.
     const unsigned long long *skip_word;
     unsigned long long skip_tag;
+    // Progressive layers (layer_major = 1): segments run layer by layer and
+    // layer j's fence (sequence seq0 + j, ring slot (seq0 + j) % ring) is
+    // published as soon as layers 0..j are all in place.
+    uint32_t layer_major;
+    uint32_t per_layer_segs;        // n * C * segs
+    FastDiv div_pls, div_cs;        // per_layer_segs, C * segs
+    unsigned long long *lay_words;  // fence words (device view of the ring)
+    unsigned long long lay_seq0;
+    uint32_t lay_ring;
+    uint32_t *lay_done;             // per-slot finished-segment counters (zeroed before launch)
+    uint32_t *lay_published;        // layers published so far (zeroed before launch)
+    uint32_t *lay_work;             // next segment ticket (zeroed before launch)
+    uint32_t *lay_lock;             // publisher lock (zeroed before launch)
 };
 
 // Ids of one launch, inside the kernel's parameter block.  Launches use the
@@ -79,8 +93,10 @@ struct IdsT {
 };
 using MoveIds = IdsT<kMaxItems>;
 
-// Launch the gather/scatter kernel on `stream` with `ctas` CTAs.
-cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
+// Launch the gather/scatter kernel on `stream` with `ctas` CTAs of `threads`
+// threads (kMoveThreads or kWideThreads).
+cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int threads,
+                        cudaStream_t stream);
 // Launch the bulk-copy variant (identity chunks only; d.segs / d.div_segs /
 // d.total_segs count kBulkBytes segments).  `ctas` CTAs of kBulkThreads.
 cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);

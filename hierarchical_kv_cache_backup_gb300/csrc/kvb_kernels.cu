@@ -92,14 +92,67 @@ __device__ __forceinline__ void complete_grid(const MoveDesc &d) {
     }
 }
 
-template <bool kTranspose, int kCap>
-__global__ void __launch_bounds__(kMoveThreads, 4)
+// Progressive layers: called by lane 0 of a warp once its `count` segments of
+// layer `lr` are visible device-wide.  The warp that completes a layer tries
+// to become the publisher (a lock that is tried, never waited on): the
+// publisher stores the fence word of every complete layer of the prefix in
+// layer order, so layer j's word is never visible before layer j-1's.  After
+// releasing, it looks again for a layer that completed while it held the lock
+// (that layer's completer gave up when it found the lock taken); the sequential
+// fences on both sides guarantee one of the two sees the other.  No loop
+// waits: each round publishes at least one layer or returns.  Restores write
+// device memory read by kernels on the GPU, so device scope suffices for the
+// data; the fence words are stored at system scope for the host.
+__device__ __forceinline__ void publish_layers(const MoveDesc &d, uint32_t lr, uint32_t count) {
+    const uint32_t slot = (uint32_t)((d.lay_seq0 + lr) % d.lay_ring);
+    unsigned int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(prev)
+                 : "l"(d.lay_done + slot), "r"(count)
+                 : "memory");
+    if (prev + count != d.per_layer_segs) return;
+    __threadfence();
+    for (;;) {
+        if (atomicCAS(d.lay_lock, 0u, 1u) != 0u) return;   // the holder will look again
+        __threadfence();
+        uint32_t p = *(volatile uint32_t *)d.lay_published;
+        while (p < d.nl) {
+            const uint32_t sp = (uint32_t)((d.lay_seq0 + p) % d.lay_ring);
+            unsigned int dn;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(dn) : "l"(d.lay_done + sp)
+                         : "memory");
+            if (dn != d.per_layer_segs) break;
+            __threadfence_system();
+            asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.lay_words + sp),
+                         "l"(d.lay_seq0 + p)
+                         : "memory");
+            ++p;
+        }
+        *(volatile uint32_t *)d.lay_published = p;
+        __threadfence();
+        atomicExch(d.lay_lock, 0u);
+        __threadfence();
+        if (p >= d.nl) return;
+        const uint32_t sp = (uint32_t)((d.lay_seq0 + p) % d.lay_ring);
+        unsigned int dn;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(dn) : "l"(d.lay_done + sp)
+                     : "memory");
+        if (dn != d.per_layer_segs) return;   // its completer will publish it
+    }
+}
+
+// kThreads = kMoveThreads (4 CTAs per SM, for HBM-only moves) or kWideThreads
+// (one 32-warp CTA per SM: host-link moves packed onto as few SMs as possible,
+// leaving whole SMs to whatever computes beside them).
+template <bool kTranspose, int kCap, int kThreads>
+__global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
     kv_move_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ IdsT<kCap> ids) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const uint32_t lc_per_item = d.nl * d.C;
 
+    uint32_t cur_layer = 0xffffffffu, cur_count = 0;   // progressive: this warp's tally
     bool skip = false;
     if (d.skip_word != nullptr) {   // gated op: the gate decided once, before this launch
         __shared__ int s_skip;
@@ -112,21 +165,51 @@ __global__ void __launch_bounds__(kMoveThreads, 4)
         skip = s_skip != 0;
     }
 
-    for (uint32_t w = skip ? d.total_segs : warp; w < d.total_segs; w += nwarps) {
-        const uint32_t chunk = fdiv(w, d.div_segs);
-        const uint32_t seg = w - chunk * d.segs;
-        const uint32_t item = fdiv(chunk, d.div_lc);
-        const uint32_t lc = chunk - item * lc_per_item;
-        const uint32_t lr = fdiv(lc, d.div_c);
-        const uint32_t c = lc - lr * d.C;
+    // Progressive layers take segments from a ticket counter in order, so a warp
+    // slowed by whatever else shares its SM does less of the work instead of
+    // holding back every later layer's publication; other moves use a static
+    // grid stride.
+    uint32_t w = skip ? d.total_segs : warp;
+    if (d.layer_major) {
+        uint32_t t = 0;
+        if (lane == 0) t = atomicAdd(d.lay_work, 1u);
+        w = __shfl_sync(0xffffffffu, t, 0);
+    }
+    for (; w < d.total_segs;) {
+        uint32_t seg, item, lr, c;
+        if (d.layer_major) {   // layer, then item, component, segment
+            lr = fdiv(w, d.div_pls);
+            const uint32_t rem = w - lr * d.per_layer_segs;
+            item = fdiv(rem, d.div_cs);
+            const uint32_t rem2 = rem - item * (d.C * d.segs);
+            c = fdiv(rem2, d.div_segs);
+            seg = rem2 - c * d.segs;
+        } else {               // item, then layer, component, segment
+            const uint32_t chunk = fdiv(w, d.div_segs);
+            seg = w - chunk * d.segs;
+            item = fdiv(chunk, d.div_lc);
+            const uint32_t lc = chunk - item * lc_per_item;
+            lr = fdiv(lc, d.div_c);
+            c = lc - lr * d.C;
+        }
+        if (d.layer_major && lr != cur_layer) {
+            // a warp walks layers in increasing order: flush the previous layer's tally
+            if (cur_count != 0) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) publish_layers(d, cur_layer, cur_count);
+            }
+            cur_layer = lr;
+            cur_count = 0;
+        }
+        ++cur_count;
         const uint64_t l = d.l0 + lr;
         const uint32_t ia = (uint32_t)ids.a[item];
         const uint32_t ib = (uint32_t)ids.b[item];
         if (ia >= d.src.id_limit || ib >= d.dst.id_limit) {
             // Host validation makes this unreachable; never touch memory for a bad id.
             if (lane == 0 && d.err != nullptr) *(volatile uint32_t *)d.err = 1u;
-            continue;
-        }
+        } else {
         const char *sp = reinterpret_cast<const char *>(d.src.base + ia * d.src.s_id +
                                                         l * d.src.s_l + c * d.src.s_c);
         char *dp = reinterpret_cast<char *>(d.dst.base + ib * d.dst.s_id + l * d.dst.s_l +
@@ -177,6 +260,19 @@ __global__ void __launch_bounds__(kMoveThreads, 4)
                 }
             }
         }
+        }   // valid ids
+        if (d.layer_major) {
+            uint32_t t = 0;
+            if (lane == 0) t = atomicAdd(d.lay_work, 1u);
+            w = __shfl_sync(0xffffffffu, t, 0);
+        } else {
+            w += nwarps;
+        }
+    }
+    if (d.layer_major && cur_count != 0) {
+        __threadfence();   // this lane's stores are visible device-wide before they are counted
+        __syncwarp();
+        if (lane == 0) publish_layers(d, cur_layer, cur_count);
     }
     if (d.fence_word != nullptr) complete_grid(d);
 }
@@ -362,7 +458,7 @@ FastDiv make_fastdiv(uint32_t d) {
     return f;
 }
 
-template <int kCap>
+template <int kCap, int kThreads>
 static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
     IdsT<kCap> p;
     for (uint32_t i = 0; i < d.n; ++i) {
@@ -370,10 +466,18 @@ static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, c
         p.b[i] = ids.b[i];
     }
     if (d.transpose)
-        kv_move_kernel<true, kCap><<<ctas, kMoveThreads, 0, stream>>>(d, p);
+        kv_move_kernel<true, kCap, kThreads><<<ctas, kThreads, 0, stream>>>(d, p);
     else
-        kv_move_kernel<false, kCap><<<ctas, kMoveThreads, 0, stream>>>(d, p);
+        kv_move_kernel<false, kCap, kThreads><<<ctas, kThreads, 0, stream>>>(d, p);
     return cudaGetLastError();
+}
+
+template <int kThreads>
+static cudaError_t launch_threads(const MoveDesc &d, const MoveIds &ids, int ctas,
+                                  cudaStream_t stream) {
+    if (d.n <= 64) return launch_cap<64, kThreads>(d, ids, ctas, stream);
+    if (d.n <= 512) return launch_cap<512, kThreads>(d, ids, ctas, stream);
+    return launch_cap<kMaxItems, kThreads>(d, ids, ctas, stream);
 }
 
 template <int kCap>
@@ -404,12 +508,13 @@ cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStr
     return launch_bulk_cap<kMaxItems>(d, ids, ctas, stream);
 }
 
-cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
+cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int threads,
+                        cudaStream_t stream) {
     (void)cudaGetLastError();   // report this launch's error, not an earlier call's
     if (d.n > (uint32_t)kMaxItems) return cudaErrorInvalidValue;
-    if (d.n <= 64) return launch_cap<64>(d, ids, ctas, stream);
-    if (d.n <= 512) return launch_cap<512>(d, ids, ctas, stream);
-    return launch_cap<kMaxItems>(d, ids, ctas, stream);
+    if (threads == kWideThreads) return launch_threads<kWideThreads>(d, ids, ctas, stream);
+    if (threads == kMoveThreads) return launch_threads<kMoveThreads>(d, ids, ctas, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream) {

@@ -43,7 +43,7 @@ KVB_IPC_MAGIC = 0x4B564231
 # the symbols include/kvb.h declares
 EXPORTS = ("kv_pool_register", "kv_pool_export", "kv_pool_import", "kv_pool_close",
            "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
-           "kv_restore", "kv_backup_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
+           "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version")
@@ -72,7 +72,7 @@ class kv_ipc_desc(ctypes.Structure):
 class kv_config(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_uint32), ("max_ctas", ctypes.c_uint32),
                 ("staging_bytes", ctypes.c_uint64), ("flags", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32)]
+                ("cta_threads", ctypes.c_uint32)]
 
 
 def _load():
@@ -94,6 +94,7 @@ def _load():
         "kv_host_close": (st, [vp]),
         "kv_backup": (st, [vp, vp, vp, vp, u32, vp, P(u64)]),
         "kv_restore": (st, [vp, vp, vp, vp, u32, i32, vp, P(u64)]),
+        "kv_restore_layers": (st, [vp, vp, vp, vp, u32, u32, u32, vp, P(u64)]),
         "kv_backup_when_ready": (st, [vp, vp, vp, vp, u32, vp, u64, u64, vp, P(u64)]),
         "kv_device_gather": (st, [vp, vp, u64, u32, vp, u32, vp, P(u64)]),
         "kv_device_scatter": (st, [vp, vp, u64, u32, vp, u32, i32, vp, P(u64)]),
@@ -205,6 +206,19 @@ def kv_backup(pool: int, host: int, src_pages, host_slots, stream=None) -> int:
     return f.value
 
 
+def kv_restore_layers(pool: int, host: int, host_slots, dst_pages, first_layer: int,
+                      num_layers: int, stream=None) -> list:
+    """One call, progressive per-layer fences (list of num_layers fences)."""
+    a, pa = _ids(host_slots)
+    b, pb = _ids(dst_pages)
+    if a.size != b.size:
+        raise ValueError("host_slots and dst_pages differ in length")
+    fences = (ctypes.c_uint64 * max(1, num_layers))()
+    _check(_lib.kv_restore_layers(pool, host, pa, pb, a.size, first_layer, num_layers, stream,
+                                  fences))
+    return list(fences[:num_layers])
+
+
 def kv_backup_when_ready(pool: int, host: int, src_pages, host_slots, ready_word: int,
                          ready_value: int, ready_timeout_ns: int, stream=None) -> int:
     a, pa = _ids(src_pages)
@@ -285,8 +299,9 @@ def kv_config_get() -> kv_config:
 
 
 def kv_config_set(mode: int = KV_MODE_ZERO_COPY, max_ctas: int = 0, staging_bytes: int = 0,
-                  flags: int = 0):
-    _check(_lib.kv_config_set(ctypes.byref(kv_config(mode, max_ctas, staging_bytes, flags, 0))))
+                  flags: int = 0, cta_threads: int = 0):
+    _check(_lib.kv_config_set(ctypes.byref(kv_config(mode, max_ctas, staging_bytes, flags,
+                                                     cta_threads))))
 
 
 def kv_layout_page_bytes(layout: kv_layout) -> int:

@@ -132,12 +132,17 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1 } kv_mode;
 /* kv_config.flags */
 #define KV_CFG_NO_BULK 1u   /* HBM-only moves use the register kernel, not bulk copies */
 
+/* Defaults: host-link moves (zero-copy backup / restore) run 16 CTAs of 1024
+ * threads, one per SM, so the link saturates from 16 of the GPU's SMs and the
+ * rest stay free for compute; kv_restore_layers, made to run beside compute,
+ * runs 8; HBM-only moves run 4 CTAs of 256 threads per SM (bulk-copy kernel:
+ * 3 per SM). */
 typedef struct {
     uint32_t mode;           /* kv_mode                                         */
     uint32_t max_ctas;       /* CTA cap of the transfer kernel; 0 = default     */
     uint64_t staging_bytes;  /* STAGED: device staging bytes; 0 = default       */
     uint32_t flags;          /* KV_CFG_* bits                                   */
-    uint32_t reserved;       /* must be 0                                       */
+    uint32_t cta_threads;    /* host-link CTA size: 0 = default (1024), 256, 1024 */
 } kv_config;
 
 /* ------------------------------------------------------------------ pools */
@@ -240,6 +245,21 @@ KVB_API kv_status kv_restore(kv_pool pool, kv_host host, const int32_t *host_slo
                      const int32_t *dst_pages, uint32_t n, int32_t layer, void *stream,
                      kv_fence *fence);
 
+/* Layer-wise restore of many layers in one call, with progressive per-layer
+ * fences ([PR] §PP Prefetch Ticket Path: "Layer-wise H2D + forward" and the
+ * progressive publication of the globally safe prefix).  Same bytes as
+ * num_layers calls kv_restore(..., first_layer + j, ...), j = 0..num_layers-1,
+ * but one kernel streams every layer back to back through the host link.
+ * fences[j] (num_layers outputs) completes once layers first_layer ..
+ * first_layer + j are all in place, so layer j's fence implies every earlier
+ * one; a compute stream waits for one layer with kv_fence_stream_wait, which
+ * waits on the GPU for that fence word while later layers are still moving.
+ * Limits: n <= 2048, 1 <= num_layers <= 2048, first_layer + num_layers <= L.
+ * Errors: as kv_restore. */
+KVB_API kv_status kv_restore_layers(kv_pool pool, kv_host host, const int32_t *host_slots,
+                                    const int32_t *dst_pages, uint32_t n, uint32_t first_layer,
+                                    uint32_t num_layers, void *stream, kv_fence *fences);
+
 /* Device-side gather / scatter in host-tier layout (the first half of a
  * STAGED transfer, exposed on its own for callers that move the result with
  * their own engine: a NIC, storage, another process).  `buf` is DEVICE
@@ -299,7 +319,9 @@ KVB_API kv_status kv_op_validate(const kv_layout *layout, uint32_t num_slots, in
  * operation completed by giving up (kv_backup_when_ready whose ready fence
  * never arrived), INVALID_ARG for a fence never issued.  kv_fence_wait: polls
  * until complete or until timeout_ns has passed (TIMEOUT).  kv_fence_stream_wait: makes `stream` wait
- * for the fence on the GPU (the compute stream of a layer-wise restore). */
+ * for the fence on the GPU (the compute stream of a layer-wise restore): the
+ * stream waits for the fence's word itself (a 64-bit stream wait-value) where
+ * the driver supports it, else for the fence's event. */
 KVB_API kv_status kv_fence_query(kv_fence fence);
 KVB_API kv_status kv_fence_wait(kv_fence fence, uint64_t timeout_ns);
 KVB_API kv_status kv_fence_stream_wait(kv_fence fence, void *stream);

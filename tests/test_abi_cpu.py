@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 def test_struct_sizes_match_header():
     assert ctypes.sizeof(kvb.kv_layout) == 40
     assert ctypes.sizeof(kvb.kv_ipc_desc) == 168
-    assert ctypes.sizeof(kvb.kv_config) == 24
+    assert ctypes.sizeof(kvb.kv_config) == 24   # mode, max_ctas, staging, flags, cta_threads
     assert kvb.kv_abi_version() == 1
 
 

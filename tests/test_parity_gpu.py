@@ -445,3 +445,89 @@ def test_many_small_ops_reuse_fence_slots():
         rig.assert_equal((snap[0], host))
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("wname,first,count", [("mla_fp8", 0, 61), ("mla_fp8", 7, 5),
+                                               ("trtllm_ipc", 0, 40), ("llama8b", 30, 2),
+                                               ("tiny", 1, 1)])
+def test_restore_layers_progressive(wname, first, count):
+    """One call restoring many layers equals one kv_restore per layer (oracle), and its
+    per-layer fences complete as a prefix: layer j's fence implies every earlier one."""
+    import oracle
+    from gpu_rig import oracle_geom
+
+    w = {x.name: x for x in wl.WORKLOADS}[wname]
+    g = w.geom.with_(P=48)
+    n = 12
+    r = np.random.default_rng(w.seed + first)
+    rig = Rig(g, 16, pool_offset=w.pool_offset, seed=w.seed + 5)
+    try:
+        slots = r.permutation(16)[:n]
+        dst = r.permutation(g.P)[:n]
+        snap = rig.snapshot()
+        want = snap[0].copy()
+        for l in range(first, first + count):
+            oracle.restore(oracle_geom(g), want, snap[1], slots, dst, layer=l,
+                           pool_offset=rig.offset)
+        s = torch.cuda.Stream()
+        fences = kvb.kv_restore_layers(rig.pool, rig.hostt, slots, dst, first, count,
+                                       s.cuda_stream)
+        assert len(fences) == count and fences == sorted(fences)
+        violations, t0 = 0, time.perf_counter()
+        while True:
+            # read the last layer first: a complete later layer must see earlier ones complete
+            done = [False] * count
+            for j in reversed(range(count)):
+                done[j] = kvb.kv_fence_query(fences[j]) == kvb.KV_OK
+            for j in range(count):
+                if done[j] and not all(done[:j]):
+                    violations += 1
+            if all(done) or time.perf_counter() - t0 > 30:
+                break
+        assert all(done) and violations == 0
+        rig.assert_equal((want, snap[1]))
+        # a compute stream waiting on one layer's fence sees that layer (and earlier ones)
+        # restored from the new slots, whatever later layers are doing
+        slots2, dst2 = slots[3:6], dst[:3]
+        comp = torch.cuda.Stream()
+        fences = kvb.kv_restore_layers(rig.pool, rig.hostt, slots2, dst2, first, count,
+                                       s.cuda_stream)
+        mid = count // 2
+        kvb.kv_fence_stream_wait(fences[mid], comp.cuda_stream)
+        with torch.cuda.stream(comp):
+            seen = rig.alloc.clone()
+        comp.synchronize()
+        kvb.kv_fence_wait(fences[-1], 30_000_000_000)
+        want2 = want.copy()
+        mask_pool = np.zeros(rig.alloc.numel(), dtype=np.uint8)
+        ones = np.ones(16 * g.page_bytes, dtype=np.uint8)
+        for l in range(first, first + mid + 1):
+            oracle.restore(oracle_geom(g), want2, snap[1], slots2, dst2, layer=l,
+                           pool_offset=rig.offset)
+            oracle.restore(oracle_geom(g), mask_pool, ones, slots2, dst2, layer=l,
+                           pool_offset=rig.offset)
+        m = mask_pool == 1
+        assert m.sum() == 3 * (mid + 1) * g.layer_page_bytes
+        assert np.array_equal(seen.cpu().numpy()[m], want2[m])
+    finally:
+        rig.close()
+
+
+def test_restore_layers_limits_and_empty():
+    g = wl.MLA_FP8.geom.with_(P=8)
+    rig = Rig(g, 4, seed=31)
+    try:
+        snap = rig.snapshot()
+        fences = kvb.kv_restore_layers(rig.pool, rig.hostt, [], [], 3, 4)
+        for f in fences:
+            kvb.kv_fence_wait(f, 10_000_000_000)
+        rig.assert_equal(snap)
+        for first, count, status in [(60, 2, kvb.KV_ERR_OUT_OF_RANGE), (0, 0, kvb.KV_ERR_OUT_OF_RANGE)]:
+            with pytest.raises(kvb.KvError) as e:
+                kvb.kv_restore_layers(rig.pool, rig.hostt, [0], [1], first, count)
+            assert e.value.status == status
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_restore_layers(rig.pool, rig.hostt, [0, 1], [1, 1], 0, 2)
+        assert e.value.status == kvb.KV_ERR_DUPLICATE
+    finally:
+        rig.close()
