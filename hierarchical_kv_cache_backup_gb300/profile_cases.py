@@ -5,7 +5,8 @@
 
 Cases: ``backup`` (zero-copy D2H), ``restore`` (zero-copy H2D), ``gather``
 (device-side gather into a device buffer in host layout, HBM only),
-``scatter`` (its inverse), ``restore_layer`` (one-layer restores).  The
+``scatter`` (its inverse), ``restore_layer`` (one-layer restores),
+``restore_layers`` (every layer in one progressive call).  The
 geometry is the Llama-8B page (32 x {K,V} x 8 heads x 16 tokens x 256 B) unless
 ``--geometry trtllm`` (page-first HND, 40 x 2 x 8 x 32 x 256 B) or ``mla``
 (61 layers x 576 B latent x 256 tokens) is given.  Each op is one kv_move_kernel
@@ -30,8 +31,8 @@ def main(argv=None):
     from hierarchical_kv_cache_backup_gb300 import workloads as wl
 
     p = argparse.ArgumentParser()
-    p.add_argument("--case", choices=["backup", "restore", "gather", "scatter", "restore_layer"],
-                   required=True)
+    p.add_argument("--case", choices=["backup", "restore", "gather", "scatter", "restore_layer",
+                                      "restore_layers"], required=True)
     p.add_argument("--geometry", choices=["llama8b", "trtllm", "mla"], default="llama8b")
     p.add_argument("--pool-pages", type=int, default=512)
     p.add_argument("--pages", type=int, default=128)
@@ -64,6 +65,9 @@ def main(argv=None):
             f = kvb.kv_restore(pool, tier, i.restore_slots, i.restore_dst, -1, s.cuda_stream)
         elif a.case == "restore_layer":
             f = kvb.kv_restore(pool, tier, i.restore_slots, i.restore_dst, k % g.L, s.cuda_stream)
+        elif a.case == "restore_layers":
+            f = kvb.kv_restore_layers(pool, tier, i.restore_slots, i.restore_dst, 0, g.L,
+                                      s.cuda_stream)[-1]
         elif a.case == "gather":
             f = kvb.kv_device_gather(pool, buf.data_ptr(), buf.numel(), g.host_heads,
                                      i.backup_src, s.cuda_stream)
