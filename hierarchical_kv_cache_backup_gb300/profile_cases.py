@@ -9,9 +9,10 @@ Cases: ``backup`` (zero-copy D2H), ``restore`` (zero-copy H2D), ``gather``
 ``restore_layers`` (every layer in one progressive call).  The
 geometry is the Llama-8B page (32 x {K,V} x 8 heads x 16 tokens x 256 B) unless
 ``--geometry trtllm`` (page-first HND, 40 x 2 x 8 x 32 x 256 B) or ``mla``
-(61 layers x 576 B latent x 256 tokens) is given.  Each op is one kv_move_kernel
-launch followed by one kv_mark_kernel launch, so ``ncu -k regex:kv_move -s W
--c R`` captures exactly the R timed ops after W warm-up ops.
+(61 layers x 576 B latent x 256 tokens) is given.  Each op is one kernel launch
+(kv_move_kernel; kv_bulk_kernel for ``gather`` / ``scatter``) with its fence
+fused in, so ``ncu -k regex:kv_move -s W -c R`` captures exactly the R timed ops
+after W warm-up ops.
 """
 from __future__ import annotations
 
