@@ -1,0 +1,381 @@
+// kvb_ring.cpp -- shared-memory descriptor ring between a submitting process
+// (the scheduler) and a serving process (the data plane).
+//
+// "[Feature] [RFC] [HiCache] Out-of-process HiCache data plane with
+// device-memory IPC", §Device IPC data path: after the pool is registered once,
+// operations only carry descriptors (page IDs, keys, fences), over a control
+// path such as shared-memory submission / completion rings, NVMe-style; and
+// device-memory sharing and cross-process synchronization are separate
+// capabilities.  Here the bulk bytes never leave the GPU / host tier, the
+// ring carries descriptors, and completion is written by the GPU straight into
+// the shared page the submitter polls.
+//
+// Layout of the shared segment (page-aligned regions):
+//   [0, 4096)            RingHeader
+//   [comp_off, +C)       CompRec[slots]   (registered with CUDA by the server)
+//   [entry_off, +E)      kv_ring_op[slots]
+// Ticket t (1, 2, ...) uses slot (t - 1) % slots.  tail = last ticket published
+// by the submitter, head = last ticket taken by the server.  A slot is reused
+// for ticket t only when t - slots has been taken and completed.
+#include "kvb.h"
+#include "kvb_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <cerrno>
+#include <cstdio>
+#include <cstring>
+#include <ctime>
+#include <fcntl.h>
+#include <mutex>
+#include <sched.h>
+#include <string>
+#include <sys/mman.h>
+#include <sys/stat.h>
+#include <unistd.h>
+#include <unordered_map>
+
+namespace {
+
+constexpr uint32_t kRingMagic = 0x4B565252u;   // "KVRR"
+constexpr uint32_t kRingVersion = 1u;
+constexpr uint32_t kMaxSlots = 4096;
+constexpr size_t kPage = 4096;
+
+struct RingHeader {
+    uint32_t magic, version, slots, entry_bytes;
+    uint64_t comp_off, entry_off, total_bytes;
+    int64_t creator_pid;
+    alignas(64) uint64_t tail;        // last published ticket
+    alignas(64) uint64_t head;        // last taken ticket
+    alignas(64) int64_t server_pid;   // last server that took a descriptor
+};
+static_assert(sizeof(RingHeader) <= kPage, "ring header fits one page");
+
+// done: written by the GPU (or the CPU) when ticket `done` is complete.
+// err_ticket / err: written by the CPU, before done, when a ticket failed.
+struct CompRec {
+    uint64_t done;
+    uint64_t err_ticket;
+    int32_t err;
+    int32_t pad;
+    uint64_t pad2;
+};
+static_assert(sizeof(CompRec) == 32, "completion record size");
+
+struct RingObj {
+    std::string name;
+    bool creator;
+    int fd;
+    void *base;
+    size_t bytes;
+    RingHeader *h;
+    CompRec *comp;
+    kv_ring_op *ops;
+    std::mutex mu;                  // one submitter / one server thread at a time
+    CompRec *comp_dev = nullptr;    // device view once registered by a server
+    bool registered = false;
+};
+
+std::mutex g_rings_mu;
+std::unordered_map<uint64_t, RingObj *> g_rings;
+uint64_t g_next_ring = 1;
+
+kv_status err(kv_status st, const char *msg) {
+    return (kv_status)kvb::set_last_error(st, msg);
+}
+
+double now_ns() {
+    timespec ts;
+    clock_gettime(CLOCK_MONOTONIC, &ts);
+    return ts.tv_sec * 1e9 + ts.tv_nsec;
+}
+
+void backoff(int &spins) {
+    if (++spins < 64) {
+        sched_yield();
+    } else {
+        timespec ts{0, 10000};
+        nanosleep(&ts, nullptr);
+    }
+}
+
+uint64_t ld(const uint64_t *p) { return __atomic_load_n(p, __ATOMIC_ACQUIRE); }
+void st(uint64_t *p, uint64_t v) { __atomic_store_n(p, v, __ATOMIC_RELEASE); }
+
+size_t round_page(size_t x) { return (x + kPage - 1) / kPage * kPage; }
+
+bool valid_name(const char *name) {
+    if (name == nullptr || name[0] != '/' || name[1] == '\0') return false;
+    const size_t n = strnlen(name, 256);
+    if (n >= 255) return false;
+    return std::strchr(name + 1, '/') == nullptr;
+}
+
+RingObj *find(kv_ring r) {
+    std::lock_guard<std::mutex> lk(g_rings_mu);
+    auto it = g_rings.find((uint64_t)(uintptr_t)r);
+    return it == g_rings.end() ? nullptr : it->second;
+}
+
+kv_ring publish(RingObj *o) {
+    std::lock_guard<std::mutex> lk(g_rings_mu);
+    const uint64_t id = g_next_ring++;
+    g_rings[id] = o;
+    return (kv_ring)(uintptr_t)id;
+}
+
+void bind(RingObj *o) {
+    char *b = (char *)o->base;
+    o->h = (RingHeader *)b;
+    o->comp = (CompRec *)(b + o->h->comp_off);
+    o->ops = (kv_ring_op *)(b + o->h->entry_off);
+}
+
+uint32_t slot_of(const RingObj *o, uint64_t t) { return (uint32_t)((t - 1) % o->h->slots); }
+
+// CPU completion of ticket t with status s (error record first, then done).
+void complete_cpu(RingObj *o, uint64_t t, kv_status s) {
+    CompRec &c = o->comp[slot_of(o, t)];
+    if (s != KV_OK) {
+        c.err = (int32_t)s;
+        st(&c.err_ticket, t);
+    }
+    st(&c.done, t);
+}
+
+}  // namespace
+
+extern "C" {
+
+kv_status kv_ring_create(const char *name, uint32_t slots, kv_ring *out) {
+    if (out == nullptr) return err(KV_ERR_INVALID_ARG, "output handle pointer is NULL");
+    if (!valid_name(name)) return err(KV_ERR_INVALID_ARG, "ring name must be \"/name\"");
+    if (slots < 2 || slots > kMaxSlots) return err(KV_ERR_INVALID_ARG, "slots must be 2..4096");
+    const size_t comp_off = kPage;
+    const size_t comp_bytes = round_page(slots * sizeof(CompRec));
+    const size_t entry_off = comp_off + comp_bytes;
+    const size_t total = entry_off + round_page((size_t)slots * sizeof(kv_ring_op));
+    const int fd = shm_open(name, O_CREAT | O_EXCL | O_RDWR, 0600);
+    if (fd < 0)
+        return err(KV_ERR_INVALID_ARG, errno == EEXIST ? "a ring of that name already exists"
+                                                       : "shm_open failed");
+    if (ftruncate(fd, (off_t)total) != 0) {
+        close(fd);
+        shm_unlink(name);
+        return err(KV_ERR_NO_MEMORY, "ftruncate of the ring failed");
+    }
+    void *base = mmap(nullptr, total, PROT_READ | PROT_WRITE, MAP_SHARED, fd, 0);
+    if (base == MAP_FAILED) {
+        close(fd);
+        shm_unlink(name);
+        return err(KV_ERR_NO_MEMORY, "mmap of the ring failed");
+    }
+    std::memset(base, 0, total);
+    RingHeader *h = (RingHeader *)base;
+    h->slots = slots;
+    h->entry_bytes = (uint32_t)sizeof(kv_ring_op);
+    h->comp_off = comp_off;
+    h->entry_off = entry_off;
+    h->total_bytes = total;
+    h->creator_pid = (int64_t)getpid();
+    h->version = kRingVersion;
+    __atomic_store_n(&h->magic, kRingMagic, __ATOMIC_RELEASE);   // last: marks it initialised
+    RingObj *o = new RingObj{name, true, fd, base, total, nullptr, nullptr, nullptr, {}};
+    bind(o);
+    *out = publish(o);
+    return KV_OK;
+}
+
+kv_status kv_ring_attach(const char *name, kv_ring *out) {
+    if (out == nullptr) return err(KV_ERR_INVALID_ARG, "output handle pointer is NULL");
+    if (!valid_name(name)) return err(KV_ERR_INVALID_ARG, "ring name must be \"/name\"");
+    const int fd = shm_open(name, O_RDWR, 0600);
+    if (fd < 0) return err(KV_ERR_INVALID_ARG, "no ring of that name");
+    struct stat sb;
+    if (fstat(fd, &sb) != 0 || (size_t)sb.st_size < kPage) {
+        close(fd);
+        return err(KV_ERR_INVALID_ARG, "ring segment too small");
+    }
+    void *base = mmap(nullptr, (size_t)sb.st_size, PROT_READ | PROT_WRITE, MAP_SHARED, fd, 0);
+    if (base == MAP_FAILED) {
+        close(fd);
+        return err(KV_ERR_NO_MEMORY, "mmap of the ring failed");
+    }
+    RingHeader *h = (RingHeader *)base;
+    if (__atomic_load_n(&h->magic, __ATOMIC_ACQUIRE) != kRingMagic || h->version != kRingVersion ||
+        h->entry_bytes != sizeof(kv_ring_op) || h->total_bytes != (uint64_t)sb.st_size ||
+        h->slots < 2 || h->slots > kMaxSlots) {
+        munmap(base, (size_t)sb.st_size);
+        close(fd);
+        return err(KV_ERR_INVALID_ARG, "segment is not a ring of this version");
+    }
+    RingObj *o = new RingObj{name, false, fd, base, (size_t)sb.st_size, nullptr, nullptr, nullptr,
+                             {}};
+    bind(o);
+    *out = publish(o);
+    return KV_OK;
+}
+
+kv_status kv_ring_close(kv_ring r) {
+    RingObj *o;
+    {
+        std::lock_guard<std::mutex> lk(g_rings_mu);
+        auto it = g_rings.find((uint64_t)(uintptr_t)r);
+        if (it == g_rings.end()) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+        o = it->second;
+        g_rings.erase(it);
+    }
+    kv_status s = KV_OK;
+    if (o->registered && cudaHostUnregister(o->comp) != cudaSuccess) {
+        (void)cudaGetLastError();
+        s = err(KV_ERR_CUDA, "cudaHostUnregister of the completion page failed");
+    }
+    munmap(o->base, o->bytes);
+    close(o->fd);
+    if (o->creator) shm_unlink(o->name.c_str());
+    delete o;
+    return s;
+}
+
+kv_status kv_ring_submit(kv_ring r, const kv_ring_op *op, uint64_t timeout_ns, uint64_t *ticket) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (op == nullptr || ticket == nullptr) return err(KV_ERR_INVALID_ARG, "NULL argument");
+    if (op->kind > KV_RING_OP_RESTORE) return err(KV_ERR_INVALID_ARG, "unknown operation kind");
+    if (op->n > KV_RING_MAX_IDS) return err(KV_ERR_INVALID_ARG, "n exceeds KV_RING_MAX_IDS");
+    std::lock_guard<std::mutex> lk(o->mu);
+    RingHeader *h = o->h;
+    const uint64_t t = ld(&h->tail) + 1;
+    const uint64_t slots = h->slots;
+    const double deadline = now_ns() + (double)timeout_ns;
+    int spins = 0;
+    // the slot's previous ticket (t - slots) must be taken and completed
+    while (t > slots && (ld(&h->head) < t - slots ||
+                         ld(&o->comp[slot_of(o, t)].done) < t - slots)) {
+        if (now_ns() >= deadline) return err(KV_ERR_TIMEOUT, "ring full: the server is behind");
+        backoff(spins);
+    }
+    kv_ring_op &e = o->ops[slot_of(o, t)];
+    std::memcpy(&e, op, offsetof(kv_ring_op, a));
+    std::memcpy(e.a, op->a, op->n * sizeof(int32_t));
+    std::memcpy(e.b, op->b, op->n * sizeof(int32_t));
+    st(&h->tail, t);
+    *ticket = t;
+    return KV_OK;
+}
+
+kv_status kv_ring_wait(kv_ring r, uint64_t ticket, uint64_t timeout_ns, kv_status *op_status) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (ticket == 0 || ticket > ld(&o->h->tail))
+        return err(KV_ERR_INVALID_ARG, "ticket was never submitted");
+    CompRec &c = o->comp[slot_of(o, ticket)];
+    const double deadline = now_ns() + (double)timeout_ns;
+    int spins = 0;
+    while (ld(&c.done) < ticket) {
+        if (now_ns() >= deadline) return err(KV_ERR_TIMEOUT, "ticket not complete in time");
+        backoff(spins);
+    }
+    if (op_status != nullptr)
+        *op_status = ld(&c.err_ticket) == ticket ? (kv_status)__atomic_load_n(&c.err,
+                                                                             __ATOMIC_ACQUIRE)
+                                                 : KV_OK;
+    return KV_OK;
+}
+
+kv_status kv_ring_pop(kv_ring r, uint64_t timeout_ns, kv_ring_op *op, uint64_t *ticket) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (op == nullptr || ticket == nullptr) return err(KV_ERR_INVALID_ARG, "NULL argument");
+    std::lock_guard<std::mutex> lk(o->mu);
+    RingHeader *h = o->h;
+    const uint64_t t = ld(&h->head) + 1;
+    const double deadline = now_ns() + (double)timeout_ns;
+    int spins = 0;
+    while (ld(&h->tail) < t) {
+        if (now_ns() >= deadline) return err(KV_ERR_TIMEOUT, "no descriptor in time");
+        backoff(spins);
+    }
+    const kv_ring_op &e = o->ops[slot_of(o, t)];
+    std::memcpy(op, &e, offsetof(kv_ring_op, a));
+    const uint32_t n = op->n <= KV_RING_MAX_IDS ? op->n : 0;
+    std::memcpy(op->a, e.a, n * sizeof(int32_t));
+    std::memcpy(op->b, e.b, n * sizeof(int32_t));
+    __atomic_store_n(&h->server_pid, (int64_t)getpid(), __ATOMIC_RELAXED);
+    st(&h->head, t);   // the slot may now be refilled (after t completes)
+    *ticket = t;
+    return KV_OK;
+}
+
+kv_status kv_ring_complete(kv_ring r, uint64_t ticket, kv_status op_status) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (ticket == 0 || ticket > ld(&o->h->head))
+        return err(KV_ERR_INVALID_ARG, "ticket was never taken");
+    complete_cpu(o, ticket, op_status);
+    return KV_OK;
+}
+
+kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_host host,
+                        void *stream, uint32_t max_ops, uint64_t idle_timeout_ns,
+                        uint32_t *served) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (served == nullptr || (npools > 0 && pools == nullptr))
+        return err(KV_ERR_INVALID_ARG, "NULL argument");
+    *served = 0;
+    if (!o->registered) {
+        // The completion records become device-visible: the GPU stores each
+        // ticket there itself once its operation is complete.
+        const size_t bytes = round_page(o->h->slots * sizeof(CompRec));
+        cudaError_t e = cudaHostRegister(o->comp, bytes,
+                                         cudaHostRegisterMapped | cudaHostRegisterPortable);
+        void *dv = nullptr;
+        if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dv, o->comp, 0);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return err(KV_ERR_CUDA, "registering the ring's completion page with CUDA failed");
+        }
+        o->comp_dev = (CompRec *)dv;
+        o->registered = true;
+    }
+    static thread_local kv_ring_op op;
+    for (uint32_t k = 0; k < max_ops; ++k) {
+        uint64_t t = 0;
+        kv_status s = kv_ring_pop(r, k == 0 ? idle_timeout_ns : 0, &op, &t);
+        if (s == KV_ERR_TIMEOUT) break;
+        if (s != KV_OK) return s;
+        ++*served;
+        if (op.pool_index >= npools) {
+            complete_cpu(o, t, KV_ERR_INVALID_ARG);
+            continue;
+        }
+        kv_fence f = 0;
+        if (op.kind == KV_RING_OP_BACKUP)
+            s = op.layer == -1 ? kv_backup(pools[op.pool_index], host, op.a, op.b, op.n, stream, &f)
+                               : KV_ERR_INVALID_ARG;
+        else
+            s = kv_restore(pools[op.pool_index], host, op.a, op.b, op.n, op.layer, stream, &f);
+        if (s != KV_OK) {
+            complete_cpu(o, t, s);
+            continue;
+        }
+        int device = 0;
+        kvb::pool_device_of(pools[op.pool_index], &device);
+        int prev = -1;
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != device) cudaSetDevice(device);
+        cudaError_t e = kvb::launch_mark((unsigned long long *)&o->comp_dev[slot_of(o, t)].done,
+                                         t, (cudaStream_t)stream);
+        if (prev >= 0 && prev != device) cudaSetDevice(prev);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            kv_fence_wait(f, 60ull * 1000 * 1000 * 1000);   // the bytes land; report the failure
+            complete_cpu(o, t, KV_ERR_CUDA);
+        }
+    }
+    return KV_OK;
+}
+
+}  // extern "C"

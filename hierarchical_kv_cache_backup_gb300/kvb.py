@@ -46,7 +46,9 @@ EXPORTS = ("kv_pool_register", "kv_pool_export", "kv_pool_import", "kv_pool_clos
            "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
-           "kv_launch_count", "kv_last_error", "kv_abi_version")
+           "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
+           "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
+           "kv_ring_pop", "kv_ring_complete")
 
 
 class KvError(RuntimeError):
@@ -67,6 +69,17 @@ class kv_ipc_desc(ctypes.Structure):
                 ("nbytes", ctypes.c_uint64), ("instance_id", ctypes.c_uint64),
                 ("generation", ctypes.c_uint64), ("exporter_pid", ctypes.c_int64),
                 ("device_uuid", ctypes.c_uint8 * 16), ("layout", kv_layout)]
+
+
+KV_RING_MAX_IDS = 1024
+KV_RING_OP_BACKUP, KV_RING_OP_RESTORE = 0, 1
+
+
+class kv_ring_op(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_uint32), ("pool_index", ctypes.c_uint32),
+                ("n", ctypes.c_uint32), ("layer", ctypes.c_int32),
+                ("operation_id", ctypes.c_uint64),
+                ("a", ctypes.c_int32 * KV_RING_MAX_IDS), ("b", ctypes.c_int32 * KV_RING_MAX_IDS)]
 
 
 class kv_config(ctypes.Structure):
@@ -109,6 +122,14 @@ def _load():
         "kv_launch_count": (u64, []),
         "kv_last_error": (ctypes.c_char_p, []),
         "kv_abi_version": (u32, []),
+        "kv_ring_create": (st, [ctypes.c_char_p, u32, P(vp)]),
+        "kv_ring_attach": (st, [ctypes.c_char_p, P(vp)]),
+        "kv_ring_close": (st, [vp]),
+        "kv_ring_submit": (st, [vp, P(kv_ring_op), u64, P(u64)]),
+        "kv_ring_wait": (st, [vp, u64, u64, P(ctypes.c_int)]),
+        "kv_ring_serve": (st, [vp, P(vp), u32, vp, vp, u32, u64, P(u32)]),
+        "kv_ring_pop": (st, [vp, u64, P(kv_ring_op), P(u64)]),
+        "kv_ring_complete": (st, [vp, u64, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -320,6 +341,70 @@ def kv_last_error() -> str:
 
 def kv_abi_version() -> int:
     return _lib.kv_abi_version()
+
+
+# ----------------------------------------------------------- descriptor ring
+
+def make_ring_op(kind: int, a, b, pool_index: int = 0, layer: int = -1,
+                 operation_id: int = 0) -> kv_ring_op:
+    a_, _ = _ids(a)
+    b_, _ = _ids(b)
+    if a_.size != b_.size or a_.size > KV_RING_MAX_IDS:
+        raise ValueError("id lists differ in length or exceed KV_RING_MAX_IDS")
+    op = kv_ring_op()
+    op.kind, op.pool_index, op.n, op.layer, op.operation_id = kind, pool_index, a_.size, layer, \
+        operation_id
+    ctypes.memmove(op.a, a_.ctypes.data, a_.nbytes) if a_.size else None
+    ctypes.memmove(op.b, b_.ctypes.data, b_.nbytes) if b_.size else None
+    return op
+
+
+def kv_ring_create(name: str, slots: int) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.kv_ring_create(name.encode(), slots, ctypes.byref(out)))
+    return out.value
+
+
+def kv_ring_attach(name: str) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.kv_ring_attach(name.encode(), ctypes.byref(out)))
+    return out.value
+
+
+def kv_ring_close(ring: int) -> None:
+    _check(_lib.kv_ring_close(ring))
+
+
+def kv_ring_submit(ring: int, op: kv_ring_op, timeout_ns: int = 10_000_000_000) -> int:
+    t = ctypes.c_uint64()
+    _check(_lib.kv_ring_submit(ring, ctypes.byref(op), timeout_ns, ctypes.byref(t)))
+    return t.value
+
+
+def kv_ring_wait(ring: int, ticket: int, timeout_ns: int = 10_000_000_000) -> int:
+    """Waits for a ticket; returns the operation's own status (raises on TIMEOUT etc.)."""
+    s = ctypes.c_int()
+    _check(_lib.kv_ring_wait(ring, ticket, timeout_ns, ctypes.byref(s)))
+    return s.value
+
+
+def kv_ring_serve(ring: int, pools, host: int, stream=None, max_ops: int = 1,
+                  idle_timeout_ns: int = 1_000_000_000) -> int:
+    arr = (ctypes.c_void_p * max(1, len(pools)))(*pools)
+    served = ctypes.c_uint32()
+    _check(_lib.kv_ring_serve(ring, arr, len(pools), host, stream, max_ops, idle_timeout_ns,
+                              ctypes.byref(served)))
+    return served.value
+
+
+def kv_ring_pop(ring: int, timeout_ns: int = 1_000_000_000):
+    op, t = kv_ring_op(), ctypes.c_uint64()
+    _check(_lib.kv_ring_pop(ring, timeout_ns, ctypes.byref(op), ctypes.byref(t)))
+    return t.value, op
+
+
+def kv_ring_complete(ring: int, ticket: int, status: int = KV_OK) -> None:
+    _check(_lib.kv_ring_complete(ring, ticket, status))
 
 
 def library():

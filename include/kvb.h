@@ -309,6 +309,75 @@ KVB_API kv_status kv_backup_staged_noalloc(kv_pool pool, kv_host host, const int
 KVB_API kv_status kv_op_validate(const kv_layout *layout, uint32_t num_slots, int kind,
                          const int32_t *a, const int32_t *b, uint32_t n, int32_t layer);
 
+/* ------------------------------------------------- descriptor ring (IPC) */
+
+/* A shared-memory submission / completion ring between a submitting process
+ * (the scheduler) and a serving process (the data plane) on one node ([RFC]
+ * §Device IPC data path: operations carry page IDs and fences, not tensors;
+ * control and completion through shared-memory submission/completion rings,
+ * NVMe-style).  One submitter and one server per ring.  Tickets are 1, 2, 3...
+ * in submission order.  The server registers the ring's completion records
+ * with CUDA, so the GPU itself stores a ticket into shared memory when that
+ * operation's bytes are in place; the submitter polls it with no help from
+ * the server's CPU (cross-process completion, [RFC] DeviceSyncIPC).  A server
+ * that dies leaves the submitter's waits to time out (fail closed). */
+typedef struct kv_ring_s *kv_ring;
+
+#define KV_RING_MAX_IDS 1024
+#define KV_RING_OP_BACKUP 0u
+#define KV_RING_OP_RESTORE 1u
+
+/* One BACKUP / RESTORE descriptor ([RFC] §Device IPC data path).  POD. */
+typedef struct {
+    uint32_t kind;           /* KV_RING_OP_BACKUP or KV_RING_OP_RESTORE              */
+    uint32_t pool_index;     /* index into the server's pool table                 */
+    uint32_t n;              /* ids in a[] and b[] (<= KV_RING_MAX_IDS)            */
+    int32_t layer;           /* restore: -1 = all layers, else one; backup: -1     */
+    uint64_t operation_id;   /* the submitter's operation_id, returned by pop      */
+    int32_t a[KV_RING_MAX_IDS];   /* backup: source pages; restore: host slots     */
+    int32_t b[KV_RING_MAX_IDS];   /* backup: host slots; restore: destination pages */
+} kv_ring_op;
+
+/* Creates POSIX shared memory `name` ("/name", no other '/') holding a ring of
+ * `slots` (2..4096) descriptors and completion records, and attaches to it.
+ * The creator unlinks the name when it closes.  Errors: INVALID_ARG (name,
+ * slots, name exists), NO_MEMORY. */
+KVB_API kv_status kv_ring_create(const char *name, uint32_t slots, kv_ring *out);
+/* Attaches to an existing ring.  Errors: INVALID_ARG (no such ring, wrong
+ * magic or version). */
+KVB_API kv_status kv_ring_attach(const char *name, kv_ring *out);
+/* Detaches (and unlinks, for the creator; unregisters the completion page
+ * from CUDA, for a server).  Errors: CLOSED. */
+KVB_API kv_status kv_ring_close(kv_ring ring);
+
+/* Submitter: copies `op` into the next slot and publishes it; waits up to
+ * timeout_ns for a free slot (TIMEOUT: ring full -- the server is behind or
+ * gone).  Returns the ticket.  Errors: INVALID_ARG (kind, n), TIMEOUT. */
+KVB_API kv_status kv_ring_submit(kv_ring ring, const kv_ring_op *op, uint64_t timeout_ns,
+                                 uint64_t *ticket);
+/* Submitter: waits up to timeout_ns for `ticket` to complete and returns the
+ * operation's own status in *op_status (OK, or the error the server met, e.g.
+ * OUT_OF_RANGE).  TIMEOUT if not complete in time, INVALID_ARG for a ticket
+ * never submitted. */
+KVB_API kv_status kv_ring_wait(kv_ring ring, uint64_t ticket, uint64_t timeout_ns,
+                               kv_status *op_status);
+
+/* Server: takes up to max_ops descriptors, waiting up to idle_timeout_ns for
+ * the first, and enqueues each on `stream` as kv_backup / kv_restore on
+ * pools[op.pool_index] and `host`; the GPU completes each ticket in shared
+ * memory after its bytes.  A descriptor the engine rejects is completed at
+ * once with that error.  *served = descriptors taken.  Errors: INVALID_ARG,
+ * CUDA (registering the completion page). */
+KVB_API kv_status kv_ring_serve(kv_ring ring, const kv_pool *pools, uint32_t npools, kv_host host,
+                                void *stream, uint32_t max_ops, uint64_t idle_timeout_ns,
+                                uint32_t *served);
+/* Server without a GPU (tests, or a server that moves bytes some other way):
+ * takes the next descriptor (waiting up to timeout_ns; TIMEOUT if none) ... */
+KVB_API kv_status kv_ring_pop(kv_ring ring, uint64_t timeout_ns, kv_ring_op *op,
+                              uint64_t *ticket);
+/* ... and completes a ticket from the CPU with the given status. */
+KVB_API kv_status kv_ring_complete(kv_ring ring, uint64_t ticket, kv_status op_status);
+
 /* --------------------------------------------------------------- fences */
 
 /* DeviceSyncIPC wait/query ([RFC] §Device IPC data path).  A fence completes
