@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--max-ctas", type=int, default=0)
     p.add_argument("--no-bulk", action="store_true",
                    help="HBM-only moves use the register kernel instead of bulk copies")
+    p.add_argument("--no-pdl", action="store_true",
+                   help="host-link moves launch without programmatic dependent launch")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -262,7 +264,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     mode = kvb.KV_MODE_STAGED if args.mode == "staged" else kvb.KV_MODE_ZERO_COPY
-    kvb.kv_config_set(mode, args.max_ctas, 0, kvb.KV_CFG_NO_BULK if args.no_bulk else 0)
+    kvb.kv_config_set(mode, args.max_ctas, 0, (kvb.KV_CFG_NO_BULK if args.no_bulk else 0) |
+                      (kvb.KV_CFG_NO_PDL if args.no_pdl else 0))
 
     w = {"llama8b": wl.LLAMA8B, "mla_fp8": wl.MLA_FP8, "trtllm_ipc": wl.TRTLLM}[args.workload]
     g = w.geom

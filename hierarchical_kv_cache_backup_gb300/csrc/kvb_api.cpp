@@ -755,6 +755,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             p.d.skip_tag = fs.seq;
         }
         p.threads = link_threads();
+        p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
         st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false, &ds, &fs);
         if (st != KV_OK) return st;
         fused = true;
@@ -997,7 +998,7 @@ kv_status kv_config_set(const kv_config *cfg) {
     if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
     if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
         return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
-    if ((cfg->flags & ~(uint32_t)KV_CFG_NO_BULK) != 0)
+    if ((cfg->flags & ~(uint32_t)(KV_CFG_NO_BULK | KV_CFG_NO_PDL)) != 0)
         return fail(KV_ERR_INVALID_ARG, "unknown config flags %#x", cfg->flags);
     if (cfg->cta_threads != 0 && cfg->cta_threads != (uint32_t)kMoveThreads &&
         cfg->cta_threads != (uint32_t)kWideThreads)

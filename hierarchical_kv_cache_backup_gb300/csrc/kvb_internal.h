@@ -81,6 +81,10 @@ struct MoveDesc {
     uint32_t *lay_published;        // layers published so far (zeroed before launch)
     uint32_t *lay_work;             // next segment ticket (zeroed before launch)
     uint32_t *lay_lock;             // publisher lock (zeroed before launch)
+    // Programmatic dependent launch: launched so that it may start while the
+    // previous kernel on its stream finishes; it waits (griddepcontrol.wait)
+    // for that kernel's completion before touching memory.
+    uint32_t pdl;
 };
 
 // Ids of one launch, inside the kernel's parameter block.  Launches use the

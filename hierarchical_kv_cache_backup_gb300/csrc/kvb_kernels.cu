@@ -152,6 +152,11 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const uint32_t lc_per_item = d.nl * d.C;
 
+    if (d.pdl) {
+        // Wait for the previous kernel on this stream (and its memory) before
+        // any access here; a no-op when it was not launched as a dependent.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     uint32_t cur_layer = 0xffffffffu, cur_count = 0;   // progressive: this warp's tally
     bool skip = false;
     if (d.skip_word != nullptr) {   // gated op: the gate decided once, before this launch
@@ -268,6 +273,13 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
         } else {
             w += nwarps;
         }
+    }
+    if (d.pdl) {
+        // This CTA has issued all its copies: the next kernel on the stream may
+        // start launching (it still waits for this grid to complete), which
+        // hides its launch behind this grid's drain without parking its CTAs
+        // on SMs for the whole of this one.
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (d.layer_major && cur_count != 0) {
         __threadfence();   // this lane's stores are visible device-wide before they are counted
@@ -464,6 +476,21 @@ static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, c
     for (uint32_t i = 0; i < d.n; ++i) {
         p.a[i] = ids.a[i];
         p.b[i] = ids.b[i];
+    }
+    if (d.pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas);
+        cfg.blockDim = dim3((unsigned)kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (d.transpose)
+            return cudaLaunchKernelEx(&cfg, kv_move_kernel<true, kCap, kThreads>, d, p);
+        return cudaLaunchKernelEx(&cfg, kv_move_kernel<false, kCap, kThreads>, d, p);
     }
     if (d.transpose)
         kv_move_kernel<true, kCap, kThreads><<<ctas, kThreads, 0, stream>>>(d, p);

@@ -38,6 +38,7 @@ KV_LAYER_FIRST, KV_PAGE_FIRST = 0, 1
 KV_NHD, KV_HND = 0, 1
 KV_MODE_ZERO_COPY, KV_MODE_STAGED = 0, 1
 KV_CFG_NO_BULK = 1
+KV_CFG_NO_PDL = 2
 KVB_IPC_MAGIC = 0x4B564231
 
 # the symbols include/kvb.h declares
