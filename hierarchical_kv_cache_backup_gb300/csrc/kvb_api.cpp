@@ -114,6 +114,9 @@ struct PoolObj {
     uint64_t instance_id, generation;
     bool imported;
     std::string ipc_key; // handle bytes of the mapping (imported pools)
+    // split pools: one device buffer per (layer, component); the table of their
+    // addresses (entry l * C + c) lives in device memory for the kernels
+    unsigned long long *table_dev = nullptr;
 };
 
 struct HostObj {
@@ -484,6 +487,13 @@ Side pool_side(const PoolObj &p) {
     }
     s.hnd = g.heads;
     s.id_limit = (uint32_t)std::min<uint64_t>(g.P, 0xffffffffull);
+    if (p.table_dev != nullptr) {     // split pool: [P][chunk] inside each buffer
+        s.lc_base = p.table_dev;
+        s.base = 0;
+        s.s_id = g.cb;
+        s.s_l = 0;
+        s.s_c = 0;
+    }
     return s;
 }
 
@@ -1056,11 +1066,83 @@ kv_status kv_pool_register(const kv_layout *layout, void *base, uint64_t offset,
     return KV_OK;
 }
 
+kv_status kv_pool_register_split(const kv_layout *layout, void *const *bases,
+                                 uint64_t instance_id, uint64_t generation, kv_pool *out) {
+    if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output handle pointer is NULL");
+    Geo g{};
+    kv_status st = check_layout(layout, &g);
+    if (st != KV_OK) return st;
+    if (g.order != KV_LAYER_FIRST)
+        return fail(KV_ERR_LAYOUT, "a split pool is layer-first: one buffer per layer and "
+                    "component");
+    if (bases == nullptr) return fail(KV_ERR_INVALID_ARG, "buffer table is NULL");
+    const uint64_t nb = g.L * g.C;
+    if (nb > (1u << 20)) return fail(KV_ERR_LAYOUT, "too many layer buffers");
+    const uint64_t buf_bytes = g.P * g.cb;   // [P][T][H][B] or [P][H][T][B]
+    for (uint64_t i = 0; i < nb; ++i) {
+        if (bases[i] == nullptr)
+            return fail(KV_ERR_INVALID_ARG, "buffer of layer %llu component %llu is NULL",
+                        (unsigned long long)(i / g.C), (unsigned long long)(i % g.C));
+        if (((uintptr_t)bases[i]) % 16 != 0)
+            return fail(KV_ERR_ALIGNMENT, "buffer %p is not 16-byte aligned", bases[i]);
+    }
+    int device = -1;
+    for (uint64_t i = 0; i < nb; ++i) {
+        cudaPointerAttributes attr;
+        cudaError_t e = cudaPointerGetAttributes(&attr, bases[i]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(layer buffer)");
+        if (attr.type != cudaMemoryTypeDevice)
+            return fail(KV_ERR_INVALID_ARG, "layer buffer %p is not device memory", bases[i]);
+        if (device >= 0 && attr.device != device)
+            return fail(KV_ERR_INVALID_ARG, "layer buffers live on different devices");
+        device = attr.device;
+        uintptr_t ab;
+        size_t as;
+        {
+            DeviceGuard guard(device);
+            st = address_range(bases[i], &ab, &as);
+        }
+        if (st != KV_OK) return st;
+        if ((uintptr_t)bases[i] + buf_bytes > ab + as)
+            return fail(KV_ERR_OUT_OF_RANGE, "layer buffer %p of %llu bytes overruns its "
+                        "allocation", bases[i], (unsigned long long)buf_bytes);
+    }
+    std::vector<unsigned long long> table(nb);
+    for (uint64_t i = 0; i < nb; ++i) table[i] = (unsigned long long)(uintptr_t)bases[i];
+    void *tdev = nullptr;
+    {
+        DeviceGuard guard(device);
+        cudaError_t e = cudaMalloc(&tdev, nb * sizeof(unsigned long long));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(tdev, table.data(), nb * sizeof(unsigned long long),
+                           cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            if (tdev) cudaFree(tdev);
+            return cuda_fail(e, "copying the split pool's buffer table to the device");
+        }
+    }
+    PoolObj *p = new (std::nothrow) PoolObj{g, *layout, (char *)bases[0], buf_bytes * nb, device,
+                                            instance_id, generation, false, std::string()};
+    if (p == nullptr) {
+        cudaFree(tdev);
+        return fail(KV_ERR_NO_MEMORY, "out of host memory");
+    }
+    p->table_dev = (unsigned long long *)tdev;
+    std::lock_guard<std::mutex> lk(g_mu);
+    const uint64_t id = g_next_handle++;
+    g_pools[id] = p;
+    *out = (kv_pool)(uintptr_t)id;
+    return KV_OK;
+}
+
 kv_status kv_pool_export(kv_pool pool_h, kv_ipc_desc *out) {
     if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output descriptor pointer is NULL");
     std::lock_guard<std::mutex> lk(g_mu);
     PoolObj *p = find_pool(pool_h);
     if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    if (p->table_dev != nullptr)
+        return fail(KV_ERR_LAYOUT, "a split pool spans several allocations: one IPC "
+                    "descriptor cannot describe it");
     DeviceGuard guard(p->device);
     uintptr_t ab;
     size_t as;
@@ -1159,6 +1241,11 @@ kv_status kv_pool_close(kv_pool pool_h) {
     PoolObj *p = it->second;
     g_pools.erase(it);
     kv_status st = KV_OK;
+    if (p->table_dev != nullptr) {
+        DeviceGuard guard(p->device);
+        if (cudaFree(p->table_dev) != cudaSuccess)
+            st = cuda_fail(cudaErrorUnknown, "cudaFree(split pool table)");
+    }
     if (p->imported) {
         auto m = g_maps.find(p->ipc_key);
         if (m != g_maps.end() && --m->second.refs == 0) {

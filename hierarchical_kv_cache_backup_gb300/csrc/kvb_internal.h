@@ -28,6 +28,9 @@ struct Side {
     uint64_t s_c;       // bytes between components
     uint32_t hnd;       // head order inside a chunk: 0 = NHD, 1 = HND
     uint32_t id_limit;  // ids must be below this (checked again on the GPU)
+    // Split pools: when set, chunk address = lc_base[layer * C + comp] + id * s_id
+    // (one device buffer per layer and component; base, s_l, s_c unused).
+    const unsigned long long *lc_base;
 };
 
 // Kernel-parameter budget: the ids of one launch travel inside the launch

@@ -69,6 +69,14 @@ __device__ __forceinline__ uint32_t permute_piece(uint32_t q, uint32_t from_hnd,
 
 constexpr int kUnroll = kSegPieces / 32;  // 16-byte pieces per lane per segment
 
+// Address of chunk (id, layer l, component c) on one side: strided, or from
+// the split pool's per-(layer, component) buffer table.
+__device__ __forceinline__ uint64_t chunk_base(const Side &s, uint32_t id, uint64_t l, uint32_t c,
+                                               uint32_t C) {
+    if (s.lc_base != nullptr) return __ldg(s.lc_base + l * C + c) + id * s.s_id;
+    return s.base + id * s.s_id + l * s.s_l + c * s.s_c;
+}
+
 // Completion of a grid, fused into its last CTA: every thread makes its own
 // stores visible system-wide, the CTA counts itself done, and the CTA that
 // finishes last publishes the sequence number for the host (and resets the
@@ -215,10 +223,8 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
             // Host validation makes this unreachable; never touch memory for a bad id.
             if (lane == 0 && d.err != nullptr) *(volatile uint32_t *)d.err = 1u;
         } else {
-        const char *sp = reinterpret_cast<const char *>(d.src.base + ia * d.src.s_id +
-                                                        l * d.src.s_l + c * d.src.s_c);
-        char *dp = reinterpret_cast<char *>(d.dst.base + ib * d.dst.s_id + l * d.dst.s_l +
-                                            c * d.dst.s_c);
+        const char *sp = reinterpret_cast<const char *>(chunk_base(d.src, ia, l, c, d.C));
+        char *dp = reinterpret_cast<char *>(chunk_base(d.dst, ib, l, c, d.C));
         const uint32_t q0 = seg * (uint32_t)kSegPieces;
         const uint32_t qn = min((uint32_t)kSegPieces, d.cb16 - q0);
 
@@ -343,10 +349,8 @@ __device__ __forceinline__ BulkSeg bulk_segment(const MoveDesc &d, const int32_t
     const uint64_t off = (uint64_t)seg * kBulkBytes;
     const uint64_t cb = (uint64_t)d.cb16 * 16u;
     r.bytes = (uint32_t)min((uint64_t)kBulkBytes, cb - off);
-    r.src = reinterpret_cast<const char *>(d.src.base + ia * d.src.s_id + l * d.src.s_l +
-                                           c * d.src.s_c + off);
-    r.dst = reinterpret_cast<char *>(d.dst.base + ib * d.dst.s_id + l * d.dst.s_l +
-                                     c * d.dst.s_c + off);
+    r.src = reinterpret_cast<const char *>(chunk_base(d.src, ia, l, c, d.C) + off);
+    r.dst = reinterpret_cast<char *>(chunk_base(d.dst, ib, l, c, d.C) + off);
     return r;
 }
 

@@ -42,7 +42,7 @@ KV_CFG_NO_PDL = 2
 KVB_IPC_MAGIC = 0x4B564231
 
 # the symbols include/kvb.h declares
-EXPORTS = ("kv_pool_register", "kv_pool_export", "kv_pool_import", "kv_pool_close",
+EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_pool_import", "kv_pool_close",
            "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
            "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
@@ -99,6 +99,7 @@ def _load():
     P = ctypes.POINTER
     sig = {
         "kv_pool_register": (st, [P(kv_layout), vp, u64, u64, u64, P(vp)]),
+        "kv_pool_register_split": (st, [P(kv_layout), P(vp), u64, u64, P(vp)]),
         "kv_pool_export": (st, [vp, P(kv_ipc_desc)]),
         "kv_pool_import": (st, [P(kv_ipc_desc), P(vp)]),
         "kv_pool_close": (st, [vp]),
@@ -163,6 +164,16 @@ def kv_pool_register(layout: kv_layout, base: int, offset: int = 0, instance_id:
     out = ctypes.c_void_p()
     _check(_lib.kv_pool_register(ctypes.byref(layout), base, offset, instance_id, generation,
                                  ctypes.byref(out)))
+    return out.value
+
+
+def kv_pool_register_split(layout: kv_layout, bases, instance_id: int = 0,
+                           generation: int = 0) -> int:
+    """bases: L x C device pointers, entry l * C + c."""
+    arr = (ctypes.c_void_p * max(1, len(bases)))(*bases)
+    out = ctypes.c_void_p()
+    _check(_lib.kv_pool_register_split(ctypes.byref(layout), arr, instance_id, generation,
+                                       ctypes.byref(out)))
     return out.value
 
 

@@ -160,6 +160,20 @@ typedef struct {
 KVB_API kv_status kv_pool_register(const kv_layout *layout, void *base, uint64_t offset,
                            uint64_t instance_id, uint64_t generation, kv_pool *out);
 
+/* A layer-first pool held in separate device buffers, one per layer and
+ * component -- the per-layer K and V buffers of a serving engine's pool.
+ * `bases` holds L x C device pointers (entry l * C + c); each buffer holds the
+ * P pages of that layer and component, page p at byte p x T x H x B, heads
+ * in the layout's order ([P][T][H][B] for NHD, [P][H][T][B] for HND).  Same
+ * bytes as one layer-first pool [L][C][P][T][H][B] cut at every (l, c).
+ * layout->order must be KV_LAYER_FIRST.  Each buffer: 16-B aligned, device
+ * memory of one device, P x T x H x B bytes inside its allocation.  The
+ * library keeps a device copy of the table (freed by kv_pool_close).  Split
+ * pools cannot be exported over IPC (one descriptor names one allocation).
+ * Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, CUDA, NO_MEMORY. */
+KVB_API kv_status kv_pool_register_split(const kv_layout *layout, void *const *bases,
+                                         uint64_t instance_id, uint64_t generation, kv_pool *out);
+
 /* Export ([RFC] DeviceMemoryIPC "export allocation"; [LMC] §共享与重建的完整链路
  * sender steps 3-5): finds the allocation base of the pool start, takes the
  * IPC handle of that base and records the pool's byte offset from it.  Fails
@@ -191,7 +205,8 @@ KVB_API kv_status kv_pool_close(kv_pool pool);
 KVB_API kv_status kv_pool_retire(uint64_t instance_id, uint64_t min_generation);
 
 /* Device address of the pool's first byte (base + offset, or mapped base +
- * alloc_offset) and its byte size.  Either output may be NULL. */
+ * alloc_offset; a split pool's first buffer) and its byte size (all buffers
+ * of a split pool).  Either output may be NULL. */
 KVB_API kv_status kv_pool_info(kv_pool pool, kv_layout *layout, void **dev_ptr, uint64_t *nbytes);
 
 /* ------------------------------------------------------------- host tier */

@@ -171,3 +171,20 @@ def test_descriptor_bytes_roundtrip():
     with pytest.raises(kvb.KvError) as err:
         kvb.kv_pool_import(kvb.desc_from_bytes(bytes(bad)))
     assert err.value.status == kvb.KV_ERR_INVALID_ARG
+
+
+def test_split_pool_checks_before_cuda():
+    lay_pf = lay(order=1)
+    with pytest.raises(kvb.KvError) as e:                      # split pools are layer-first
+        kvb.kv_pool_register_split(lay_pf, [0x1000] * 4)
+    assert e.value.status == kvb.KV_ERR_LAYOUT
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_pool_register_split(lay(), [0x1000, 0, 0x2000, 0x3000])
+    assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_pool_register_split(lay(), [0x1000, 0x1008, 0x2000, 0x3000])
+    assert e.value.status == kvb.KV_ERR_ALIGNMENT
+    lib = kvb.library()
+    out = ctypes.c_void_p()
+    assert lib.kv_pool_register_split(ctypes.byref(lay()), None, 0, 0, ctypes.byref(out)) == \
+        kvb.KV_ERR_INVALID_ARG
