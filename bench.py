@@ -170,6 +170,28 @@ class ClockSampler:
                 "power_w_max": max(pw), "reasons": sorted(reasons)}
 
 
+def _exporter(q, done, device, seed, pool_offset):
+    """Second process of the TRT-LLM workload: owns the pool allocation (a raw
+    allocation with the pool at a byte offset), exports it over CUDA IPC and
+    keeps it alive until the benchmark is done with it."""
+    import torch
+
+    sys.path.insert(0, ROOT)
+    from hierarchical_kv_cache_backup_gb300 import kvb as k
+
+    torch.cuda.set_device(device)
+    g = wl.TRTLLM.geom
+    alloc = torch.empty(pool_offset + g.pool_bytes, dtype=torch.uint8, device=f"cuda:{device}")
+    wl.fill_random_(alloc, seed)
+    torch.cuda.synchronize()
+    lay = k.make_layout(g.L, g.C, g.P, g.T, g.H, g.B, g.order, g.dev_heads, g.elem_bytes)
+    pool = k.kv_pool_register(lay, alloc.data_ptr(), pool_offset, instance_id=os.getpid(),
+                              generation=1)
+    q.put(k.desc_to_bytes(k.kv_pool_export(pool)))
+    done.wait(3600)
+    k.kv_pool_close(pool)
+
+
 # ------------------------------------------------------------- CPU oracle leg
 
 def oracle_sample(cpu_seconds: float, steps: int | None = None, n_sample: int = 512,
@@ -270,11 +292,28 @@ def run_ours(args):
     w = {"llama8b": wl.LLAMA8B, "mla_fp8": wl.MLA_FP8, "trtllm_ipc": wl.TRTLLM}[args.workload]
     g = w.geom
     lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B, g.order, g.dev_heads, g.elem_bytes)
-    alloc = torch.empty(w.pool_offset + g.pool_bytes, dtype=torch.uint8, device=dev)
-    wl.fill_random_(alloc, w.seed + 100 * rank)
+    exporter = None
     host = torch.empty(w.host_slots * g.page_bytes, dtype=torch.uint8, pin_memory=True)
-    host.copy_(alloc[:host.numel()])
-    pool = kvb.kv_pool_register(lay, alloc.data_ptr(), w.pool_offset)
+    if w is wl.TRTLLM:
+        # the pool lives in a second process and is imported over CUDA IPC
+        import multiprocessing as mp
+
+        ctx = mp.get_context("spawn")
+        q, done_ev = ctx.Queue(), ctx.Event()
+        exporter = ctx.Process(target=_exporter,
+                               args=(q, done_ev, local, w.seed + 100 * rank, w.pool_offset))
+        exporter.start()
+        pool = kvb.kv_pool_import(kvb.desc_from_bytes(q.get(timeout=900)))
+        alloc = torch.empty(2 << 30, dtype=torch.uint8, device=dev)   # probe buffer only
+        wl.fill_random_(alloc, w.seed + 7)
+        for lo in range(0, host.numel(), alloc.numel()):
+            hi = min(host.numel(), lo + alloc.numel())
+            host[lo:hi].copy_(alloc[:hi - lo])
+    else:
+        alloc = torch.empty(w.pool_offset + g.pool_bytes, dtype=torch.uint8, device=dev)
+        wl.fill_random_(alloc, w.seed + 100 * rank)
+        host.copy_(alloc[:host.numel()])
+        pool = kvb.kv_pool_register(lay, alloc.data_ptr(), w.pool_offset)
     tier = kvb.kv_host_register(host.data_ptr(), host.numel(), w.host_slots, g.host_heads, lay)
     s_a = torch.cuda.Stream(device=dev)
     s_b = torch.cuda.Stream(device=dev)
@@ -592,7 +631,8 @@ def run_ours(args):
                              if w is wl.LLAMA8B else
                              "61 one-layer restores of 64 pages on a copy stream"
                              if w is wl.MLA_FP8 else
-                             "backup n pages (stream A) while restoring n others (stream B)")),
+                             "backup n pages (stream A) while restoring n others (stream B) on "
+                             "a pool imported over CUDA IPC from a second process")),
         "backup_gbs": round(backup_gbs, 2) if backup_gbs else None,
         "restore_gbs": round(restore_gbs, 2) if restore_gbs else None,
         "pages_per_s": round(ws * (w.n * (2 if bytes_b else 1)) * args.steps / elapsed, 1),
@@ -626,6 +666,9 @@ def run_ours(args):
         line["cpu_baseline"] = None
     kvb.kv_pool_close(pool)
     kvb.kv_host_close(tier)
+    if exporter is not None:
+        done_ev.set()
+        exporter.join(120)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -1471,21 +1471,30 @@ kv_status kv_fence_query(kv_fence f) {
 }
 
 kv_status kv_fence_wait(kv_fence f, uint64_t timeout_ns) {
-    const double deadline = now_ns() + (double)timeout_ns;
-    int spins = 0;
-    for (;;) {
-        kv_status st = kv_fence_query(f);
-        if (st != KV_ERR_TIMEOUT) return st;
-        if (now_ns() >= deadline)
+    bool done = false, aborted = false;
+    int d = 0, k = 0;
+    kv_status st = fence_state(f, &done, &d, &k, &aborted);   // validates the fence once
+    if (st != KV_OK) return st;
+    // Poll the fence's mapped word directly (no lock): busy for the first 50 us
+    // (small operations finish in a few microseconds), then yield, then sleep.
+    const unsigned long long *word = &g_dev[d].words[k];
+    const uint64_t seq = f & kSeqMask;
+    const double t0 = now_ns(), deadline = t0 + (double)timeout_ns;
+    while (!done) {
+        if (load_acquire(word) >= seq) break;
+        const double t = now_ns();
+        if (t >= deadline)
             return fail(KV_ERR_TIMEOUT, "fence %llu not complete after %llu ns",
                         (unsigned long long)f, (unsigned long long)timeout_ns);
-        if (++spins < 64) {
+        if (t - t0 < 50e3) continue;
+        if (t - t0 < 2e6) {
             sched_yield();
         } else {
-            timespec ts{0, 20000};   // 20 us
+            timespec ts{0, 20000};
             nanosleep(&ts, nullptr);
         }
     }
+    return kv_fence_query(f);   // complete: report aborted ops and kernel id errors
 }
 
 kv_status kv_fence_stream_wait(kv_fence f, void *stream) {

@@ -17,17 +17,24 @@ from gpu_rig import Rig  # noqa: E402
 from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
 from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
 
-MODES = [kvb.KV_MODE_ZERO_COPY, kvb.KV_MODE_STAGED]
+# (mode, flags, host-link CTA size): the defaults, the other CTA shape without
+# programmatic dependent launch, and staged mode with and without bulk copies
+MODES = [(kvb.KV_MODE_ZERO_COPY, 0, 0),
+         (kvb.KV_MODE_ZERO_COPY, kvb.KV_CFG_NO_PDL, 256),
+         (kvb.KV_MODE_STAGED, 0, 0),
+         (kvb.KV_MODE_STAGED, kvb.KV_CFG_NO_BULK, 0)]
 LAYOUTS = [(o, d, h) for o in (wl.LAYER_FIRST, wl.PAGE_FIRST) for d in (wl.NHD, wl.HND)
            for h in (wl.NHD, wl.HND)]
 
 
-@pytest.fixture(params=MODES, ids=["zero_copy", "staged"])
+@pytest.fixture(params=MODES, ids=["zero_copy", "zero_copy_256_nopdl", "staged",
+                                   "staged_nobulk"])
 def mode(request):
     old = kvb.kv_config_get()
-    kvb.kv_config_set(request.param, 0, 4 << 20)   # small staging: forces several chunks
-    yield request.param
-    kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes)
+    m, flags, threads = request.param
+    kvb.kv_config_set(m, 0, 4 << 20, flags, threads)   # small staging: forces several chunks
+    yield m
+    kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
 
 
 def run_backup(rig, src, slots, stream=None):
