@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <ctime>
@@ -53,6 +54,47 @@ kv_status cuda_fail(cudaError_t e, const char *what) {
                         cudaGetErrorString(e));
     (void)cudaGetLastError();   // a non-sticky error must not resurface at a later launch
     return st;
+}
+
+// ----------------------------------------------------------- fault injection
+// Host-side failure drills ("[PP + HiCache] Add PP Prefetch Tickets",
+// §Targeted fault-injection validation: injected allocation failures must fall
+// back and leave the service running).  The next `count` passes through a
+// point fail as if the CUDA call there had failed; nothing touches the GPU.
+enum FaultPoint { FP_STAGING_ALLOC, FP_FENCE_RESERVE, FP_LAUNCH, FP_IPC_OPEN, FP_HOST_REGISTER,
+                  FP_COUNT };
+const char *const kFaultNames[FP_COUNT] = {"staging_alloc", "fence_reserve", "launch", "ipc_open",
+                                           "host_register"};
+std::atomic<uint32_t> g_fault[FP_COUNT];
+std::once_flag g_fault_env_once;
+
+void load_fault_env() {
+    // KVB_FAULT="point:count[,point:count...]"
+    const char *v = getenv("KVB_FAULT");
+    if (v == nullptr) return;
+    std::string spec(v);
+    size_t pos = 0;
+    while (pos < spec.size()) {
+        size_t end = spec.find(',', pos);
+        if (end == std::string::npos) end = spec.size();
+        const std::string item = spec.substr(pos, end - pos);
+        const size_t colon = item.find(':');
+        const std::string name = item.substr(0, colon);
+        const uint32_t count = colon == std::string::npos ? 1u
+                                                          : (uint32_t)strtoul(item.c_str() + colon + 1,
+                                                                              nullptr, 10);
+        for (int i = 0; i < FP_COUNT; ++i)
+            if (name == kFaultNames[i]) g_fault[i].store(count);
+        pos = end + 1;
+    }
+}
+
+bool fault_hit(FaultPoint p) {
+    std::call_once(g_fault_env_once, load_fault_env);
+    uint32_t c = g_fault[p].load();
+    while (c > 0)
+        if (g_fault[p].compare_exchange_weak(c, c - 1)) return true;
+    return false;
 }
 
 // ---------------------------------------------------------------- geometry
@@ -316,6 +358,8 @@ struct FenceSlot {
 };
 
 kv_status reserve_fence(int d, FenceSlot *out) {
+    if (fault_hit(FP_FENCE_RESERVE))
+        return fail(KV_ERR_NO_MEMORY, "fence ring exhausted: injected failure");
     DevState &s = g_dev[d];
     const uint64_t seq = g_next_seq;
     if (seq > kSeqMask) return fail(KV_ERR_NO_MEMORY, "fence sequence space exhausted");
@@ -344,6 +388,8 @@ kv_status reserve_fence(int d, FenceSlot *out) {
 // Reserves `count` consecutive sequence numbers (count <= kRing / 2), each
 // slot free; returns the first.  Nothing is committed.
 kv_status reserve_fence_range(int d, uint32_t count, uint64_t *seq0) {
+    if (fault_hit(FP_FENCE_RESERVE))
+        return fail(KV_ERR_NO_MEMORY, "fence ring exhausted: injected failure");
     DevState &s = g_dev[d];
     const uint64_t first = g_next_seq;
     if (first + count > kSeqMask) return fail(KV_ERR_NO_MEMORY, "fence sequence space exhausted");
@@ -650,6 +696,8 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
         const uint32_t per_cta = p.bulk ? 1u : (uint32_t)(p.threads / 32);   // segments in flight
         const uint64_t need = ((uint64_t)p.d.total_segs + per_cta - 1) / per_cta;
         const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
+        if (i0 == 0 && fault_hit(FP_LAUNCH))
+            return fail(KV_ERR_CUDA, "launch of the move kernel: injected failure");
         cudaError_t e = p.bulk ? launch_bulk(p.d, ids, ctas, stream)
                                : launch_move(p.d, ids, ctas, p.threads, stream);
         if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
@@ -669,6 +717,9 @@ kv_status ensure_staging(DevState &s) {
         s.staging_used[0] = s.staging_used[1] = false;
     }
     void *p = nullptr;
+    if (fault_hit(FP_STAGING_ALLOC))
+        return fail(KV_ERR_NO_MEMORY, "staging buffer of %llu bytes: injected failure",
+                    (unsigned long long)want);
     cudaError_t e = cudaMalloc(&p, want);
     if (e != cudaSuccess) return fail(KV_ERR_NO_MEMORY, "staging buffer of %llu bytes: %s",
                                       (unsigned long long)want, cudaGetErrorString(e));
@@ -982,6 +1033,17 @@ extern "C" {
 
 uint32_t kv_abi_version(void) { return KVB_ABI_VERSION; }
 
+kv_status kv_fault_inject(const char *point, uint32_t count) {
+    std::call_once(g_fault_env_once, load_fault_env);
+    if (point == nullptr) return fail(KV_ERR_INVALID_ARG, "fault point is NULL");
+    for (int i = 0; i < FP_COUNT; ++i)
+        if (std::strcmp(point, kFaultNames[i]) == 0) {
+            g_fault[i].store(count);
+            return KV_OK;
+        }
+    return fail(KV_ERR_INVALID_ARG, "unknown fault point \"%s\"", point);
+}
+
 const char *kv_last_error(void) { return t_err.c_str(); }
 
 uint64_t kv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
@@ -1210,6 +1272,7 @@ kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out) {
         DeviceGuard guard(device);
         cudaIpcMemHandle_t h;
         std::memcpy(h.reserved, desc->handle, sizeof desc->handle);
+        if (fault_hit(FP_IPC_OPEN)) return fail(KV_ERR_CUDA, "cudaIpcOpenMemHandle: injected failure");
         e = cudaIpcOpenMemHandle(&base, h, cudaIpcMemLazyEnablePeerAccess);
         if (e != cudaSuccess) return cuda_fail(e, "cudaIpcOpenMemHandle");
     }
@@ -1292,6 +1355,8 @@ kv_status kv_host_register(void *host, uint64_t bytes, uint32_t num_slots, uint3
         return fail(KV_ERR_OUT_OF_RANGE, "host tier of %llu bytes cannot hold %u slots of %llu bytes",
                     (unsigned long long)bytes, num_slots, (unsigned long long)g.pb);
     cudaPointerAttributes attr;
+    if (fault_hit(FP_HOST_REGISTER))
+        return fail(KV_ERR_CUDA, "host tier registration: injected failure");
     cudaError_t e = cudaPointerGetAttributes(&attr, host);
     if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(host tier)");
     if (attr.type != cudaMemoryTypeHost)

@@ -49,7 +49,7 @@ EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_p
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
            "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
-           "kv_ring_pop", "kv_ring_complete")
+           "kv_ring_pop", "kv_ring_complete", "kv_fault_inject")
 
 
 class KvError(RuntimeError):
@@ -132,6 +132,7 @@ def _load():
         "kv_ring_serve": (st, [vp, P(vp), u32, vp, vp, u32, u64, P(u32)]),
         "kv_ring_pop": (st, [vp, u64, P(kv_ring_op), P(u64)]),
         "kv_ring_complete": (st, [vp, u64, ctypes.c_int]),
+        "kv_fault_inject": (st, [ctypes.c_char_p, u32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -417,6 +418,10 @@ def kv_ring_pop(ring: int, timeout_ns: int = 1_000_000_000):
 
 def kv_ring_complete(ring: int, ticket: int, status: int = KV_OK) -> None:
     _check(_lib.kv_ring_complete(ring, ticket, status))
+
+
+def kv_fault_inject(point: str, count: int = 1) -> None:
+    _check(_lib.kv_fault_inject(point.encode(), count))
 
 
 def library():

@@ -425,6 +425,16 @@ KVB_API uint64_t kv_launch_count(void);
 KVB_API const char *kv_last_error(void);
 KVB_API uint32_t kv_abi_version(void);
 
+/* Host-side failure drills ([PR] §Targeted fault-injection validation: an
+ * injected allocation failure must fall back and leave the service running).
+ * The next `count` passes through `point` fail as if the CUDA call there had
+ * failed -- "staging_alloc" (NO_MEMORY), "fence_reserve" (NO_MEMORY),
+ * "launch" (CUDA, before anything of the op is enqueued), "ipc_open" (CUDA),
+ * "host_register" (CUDA); count 0 disarms.  The environment variable
+ * KVB_FAULT="point:count[,point:count]" arms points at first use.  Nothing
+ * here touches the GPU.  Errors: INVALID_ARG for an unknown point. */
+KVB_API kv_status kv_fault_inject(const char *point, uint32_t count);
+
 #ifdef __cplusplus
 }
 #endif

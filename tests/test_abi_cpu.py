@@ -188,3 +188,16 @@ def test_split_pool_checks_before_cuda():
     out = ctypes.c_void_p()
     assert lib.kv_pool_register_split(ctypes.byref(lay()), None, 0, 0, ctypes.byref(out)) == \
         kvb.KV_ERR_INVALID_ARG
+
+
+def test_fault_injection_points_without_gpu():
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_fault_inject("no_such_point", 1)
+    assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    kvb.kv_fault_inject("host_register", 1)
+    with pytest.raises(kvb.KvError) as e:        # checks pass, then the injected failure
+        kvb.kv_host_register(0x10000, 1 << 20, 4, 0, lay())
+    assert e.value.status == kvb.KV_ERR_CUDA and "injected" in kvb.kv_last_error()
+    kvb.kv_fault_inject("host_register", 0)
+    for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open"):
+        kvb.kv_fault_inject(p, 0)

@@ -1,0 +1,138 @@
+"""Host-side failure drills on the GPU path: an injected failure at each point
+returns its code, enqueues nothing, leaves every byte of the pool and the host
+tier unchanged, and the next operation succeeds (the engine keeps serving).
+No GPU fault, trap or hang is involved: the failures are made on the host."""
+import multiprocessing as mp
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from gpu_rig import Rig  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture
+def rig():
+    r = Rig(wl.LLAMA8B.geom.with_(P=48, L=4), 16, seed=61)
+    yield r
+    for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open", "host_register"):
+        kvb.kv_fault_inject(p, 0)
+    r.close()
+
+
+def _ops(rig):
+    return {
+        "backup": lambda: kvb.kv_backup(rig.pool, rig.hostt, [3, 9, 11], [0, 5, 7]),
+        "restore": lambda: kvb.kv_restore(rig.pool, rig.hostt, [0, 5], [20, 21]),
+        "restore_layer": lambda: kvb.kv_restore(rig.pool, rig.hostt, [0, 5], [20, 21], 2),
+        "restore_layers": lambda: kvb.kv_restore_layers(rig.pool, rig.hostt, [0, 5], [20, 21],
+                                                         0, 4)[-1],
+    }
+
+
+@pytest.mark.parametrize("point,status,mode", [
+    ("fence_reserve", kvb.KV_ERR_NO_MEMORY, kvb.KV_MODE_ZERO_COPY),
+    ("launch", kvb.KV_ERR_CUDA, kvb.KV_MODE_ZERO_COPY),
+    ("launch", kvb.KV_ERR_CUDA, kvb.KV_MODE_STAGED),
+    ("staging_alloc", kvb.KV_ERR_NO_MEMORY, kvb.KV_MODE_STAGED),
+])
+def test_injected_failure_has_no_side_effect_and_engine_recovers(rig, point, status, mode):
+    old = kvb.kv_config_get()
+    try:
+        ops = _ops(rig)
+        names = ["backup", "restore", "restore_layer"] + (["restore_layers"]
+                                                          if mode == kvb.KV_MODE_ZERO_COPY else [])
+        for i, name in enumerate(names):
+            # a new staging size forces the staged path to allocate again
+            kvb.kv_config_set(mode, 0, (6 + i) << 20)
+            snap = rig.snapshot()
+            launches = kvb.kv_launch_count()
+            kvb.kv_fault_inject(point, 1)
+            with pytest.raises(kvb.KvError) as e:
+                ops[name]()
+            assert e.value.status == status, (name, kvb.kv_last_error())
+            assert "injected" in kvb.kv_last_error()
+            assert kvb.kv_launch_count() == launches
+            rig.assert_equal(snap)
+            # and the next one lands, bit-exact
+            if name == "backup":
+                want = rig.expect_backup(snap, [3, 9, 11], [0, 5, 7])
+            elif name == "restore":
+                want = rig.expect_restore(snap, [0, 5], [20, 21])
+            elif name == "restore_layer":
+                want = rig.expect_restore(snap, [0, 5], [20, 21], 2)
+            else:
+                want = rig.expect_restore(snap, [0, 5], [20, 21])
+            kvb.kv_fence_wait(ops[name](), 30_000_000_000)
+            rig.assert_equal(want)
+    finally:
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+
+
+def test_fault_points_armed_from_the_environment():
+    code = f"""
+import sys
+sys.path[:0] = [{ROOT!r}, {os.path.join(ROOT, 'tests')!r}]
+import torch
+from gpu_rig import Rig
+from hierarchical_kv_cache_backup_gb300 import kvb, workloads as wl
+rig = Rig(wl.TINY.geom, 16, seed=3)
+codes = []
+for _ in range(3):
+    try:
+        kvb.kv_fence_wait(kvb.kv_backup(rig.pool, rig.hostt, [1], [2]), 10_000_000_000)
+        codes.append(0)
+    except kvb.KvError as e:
+        codes.append(e.status)
+print("CODES", codes)
+"""
+    env = dict(os.environ, KVB_FAULT="fence_reserve:1,launch:1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert f"CODES [{kvb.KV_ERR_NO_MEMORY}, {kvb.KV_ERR_CUDA}, 0]" in r.stdout
+
+
+def _export(q, done):
+    sys.path.insert(0, ROOT)
+    import torch as t
+    from hierarchical_kv_cache_backup_gb300 import kvb as k
+    from hierarchical_kv_cache_backup_gb300 import workloads as w
+
+    g = w.TINY.geom
+    a = t.zeros(g.pool_bytes, dtype=t.uint8, device="cuda")
+    lay = k.make_layout(g.L, g.C, g.P, g.T, g.H, g.B)
+    p = k.kv_pool_register(lay, a.data_ptr(), 0)
+    q.put(k.desc_to_bytes(k.kv_pool_export(p)))
+    done.wait(300)
+    k.kv_pool_close(p)
+
+
+def test_injected_ipc_open_failure_then_import():
+    ctx = mp.get_context("spawn")
+    q, done = ctx.Queue(), ctx.Event()
+    p = ctx.Process(target=_export, args=(q, done))
+    p.start()
+    try:
+        desc = kvb.desc_from_bytes(q.get(timeout=300))
+        kvb.kv_fault_inject("ipc_open", 1)
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_pool_import(desc)
+        assert e.value.status == kvb.KV_ERR_CUDA and "injected" in kvb.kv_last_error()
+        pool = kvb.kv_pool_import(desc)          # the retry maps it
+        kvb.kv_pool_close(pool)
+    finally:
+        done.set()
+        p.join(120)
