@@ -929,6 +929,7 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
         FenceSlot fs;
         st = reserve_fence(d, &fs);
         if (st != KV_OK) return st;
+        p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
         const int ctas = default_ctas(ds, false, bulk);
         if (kind == 0) {
             st = run_moves(p, pages, nullptr, n, ctas, stream, true, &ds, &fs);

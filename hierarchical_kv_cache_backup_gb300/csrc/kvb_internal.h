@@ -43,8 +43,10 @@ constexpr int kWideThreads = 1024;  // wide CTAs: host-link moves packed onto fe
 // Bulk-copy (TMA) variant for HBM-only moves whose two sides share a head
 // order: one warp per CTA, lane 0 streams each chunk through a ring of
 // kBulkStages shared-memory buffers of kBulkBytes with cp.async.bulk.
-constexpr int kBulkStages = 4;
-constexpr uint32_t kBulkBytes = 16384;
+// 8 x 8 KiB (64 KiB per CTA, 3 CTAs per SM) measured best on GB300 for a
+// gather of random 32 KiB chunks: 6.8 TB/s, against 6.4 TB/s for 4 x 16 KiB.
+constexpr int kBulkStages = 8;
+constexpr uint32_t kBulkBytes = 8192;
 constexpr int kBulkThreads = 32;
 
 struct MoveDesc {

@@ -359,6 +359,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     kv_bulk_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ IdsT<kCap> ids) {
     extern __shared__ __align__(128) unsigned char ring[];   // kBulkStages x kBulkBytes
     __shared__ __align__(8) unsigned long long bar[kBulkStages];
+    if (d.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");   // previous kernel done
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBulkStages; ++s)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])) : "memory");
@@ -419,6 +420,8 @@ __global__ void __launch_bounds__(kBulkThreads)
                         : "memory");
             }
         }
+        // every segment of this CTA is issued: the next kernel may start launching
+        if (d.pdl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (failed) {
             // Never leave while a load may still be writing this CTA's shared
             // memory: wait (bounded) for every stage, then report.
@@ -526,6 +529,19 @@ static cudaError_t launch_bulk_cap(const MoveDesc &d, const MoveIds &ids, int ct
     for (uint32_t i = 0; i < d.n; ++i) {
         p.a[i] = ids.a[i];
         p.b[i] = ids.b[i];
+    }
+    if (d.pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas);
+        cfg.blockDim = dim3((unsigned)kBulkThreads);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kv_bulk_kernel<kCap>, d, p);
     }
     kv_bulk_kernel<kCap><<<ctas, kBulkThreads, smem, stream>>>(d, p);
     return cudaGetLastError();

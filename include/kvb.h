@@ -131,8 +131,9 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1 } kv_mode;
 
 /* kv_config.flags */
 #define KV_CFG_NO_BULK 1u   /* HBM-only moves use the register kernel, not bulk copies */
-#define KV_CFG_NO_PDL 2u    /* host-link moves launch plainly: no programmatic dependent
-                               launch overlapping a kernel's start with the previous end */
+#define KV_CFG_NO_PDL 2u    /* zero-copy moves and device gathers / scatters launch plainly:
+                               no programmatic dependent launch overlapping a kernel's
+                               launch with the previous kernel's end */
 
 /* Defaults: host-link moves (zero-copy backup / restore) run 16 CTAs of 1024
  * threads, one per SM, so the link saturates from 16 of the GPU's SMs and the
