@@ -572,13 +572,18 @@ struct Plan {
     MoveDesc d;
     uint32_t max_items;   // items per launch
     bool bulk = false;    // launch the bulk-copy kernel
+    bool tsp = false;     // launch the transposing bulk kernel
     int threads = kMoveThreads;   // CTA size of the register kernel
 };
 
-// bulk: plan for the bulk-copy kernel (identity chunks, kBulkBytes segments)
-// instead of the register kernel (kSegPieces x 16-byte warp segments).
+// Which kernel a plan is for: the register kernel (kSegPieces x 16-byte warp
+// segments), the bulk-copy kernel (identity chunks, kBulkBytes segments) or
+// the transposing bulk kernel (one work item per chunk).
+enum PlanKernel { PK_REG = 0, PK_BULK = 1, PK_TSP = 2 };
+
 kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint32_t l0,
-               uint32_t *err_dev, bool iter_dst, Plan *out, bool bulk = false) {
+               uint32_t *err_dev, bool iter_dst, Plan *out, int kernel = PK_REG) {
+    const bool bulk = kernel == PK_BULK;
     MoveDesc d{};
     d.src = src;
     d.dst = dst;
@@ -586,8 +591,9 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
     d.l0 = l0;
     d.C = (uint32_t)g.C;
     d.cb16 = (uint32_t)(g.cb / 16);
-    d.segs = bulk ? (uint32_t)((g.cb + kBulkBytes - 1) / kBulkBytes)
-                  : (d.cb16 + kSegPieces - 1) / kSegPieces;
+    d.segs = kernel == PK_TSP ? 1u
+             : bulk           ? (uint32_t)((g.cb + kBulkBytes - 1) / kBulkBytes)
+                              : (d.cb16 + kSegPieces - 1) / kSegPieces;
     d.H = (uint32_t)g.H;
     d.T = (uint32_t)g.T;
     d.B16 = (uint32_t)(g.B / 16);
@@ -604,6 +610,7 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
                     (unsigned long long)per_item);
     out->max_items = (uint32_t)std::min<uint64_t>(m, (uint64_t)kMaxItems);
     out->bulk = bulk;
+    out->tsp = kernel == PK_TSP;
     d.div_segs = make_fastdiv(d.segs);
     d.div_lc = make_fastdiv(nl * d.C);
     d.div_c = make_fastdiv(d.C);
@@ -653,19 +660,24 @@ kv_status plan_layer_major(Plan &p, uint32_t n, const DevState &ds, uint64_t seq
     return KV_OK;
 }
 
-int default_ctas(const DevState &s, bool touches_host, bool bulk = false) {
+int default_ctas(const DevState &s, bool touches_host, int kernel = PK_REG) {
     if (g_cfg.max_ctas != 0) return (int)g_cfg.max_ctas;
-    if (bulk) return 3 * s.sms;   // 3 x 64 KiB rings fit one SM's shared memory
+    if (kernel == PK_BULK) return 3 * s.sms;   // 3 x 64 KiB rings fit one SM's shared memory
+    if (kernel == PK_TSP) return s.sms;        // one 192 KiB ring per SM
     if (!touches_host) return 4 * s.sms;
     return link_threads() == kWideThreads ? std::min(kLinkWideCtas, s.sms)
                                           : std::min(kLinkCtas, 4 * s.sms);
 }
 
-// HBM-only moves of identity chunks go through the bulk-copy kernel unless
-// the caller turned it off (KV_CFG_NO_BULK).
-bool use_bulk(const Geo &g, const Side &a, const Side &b) {
+// HBM-only moves go through the bulk-copy kernels unless the caller turned
+// them off (KV_CFG_NO_BULK): identity chunks through kv_bulk_kernel, chunks
+// whose head order changes (and fit the shared-memory ring) through
+// kv_tsp_kernel, the rest through the register kernel.
+int hbm_kernel(const Geo &g, const Side &a, const Side &b) {
+    if ((g_cfg.flags & KV_CFG_NO_BULK) != 0) return PK_REG;
     const bool transpose = a.hnd != b.hnd && g.H > 1 && g.T > 1;
-    return !transpose && (g_cfg.flags & KV_CFG_NO_BULK) == 0;
+    if (!transpose) return PK_BULK;
+    return g.cb <= kTspMaxChunk ? PK_TSP : PK_REG;
 }
 
 // Launches the move for items [0, n) of (a, b) in slices of at most max_items.
@@ -693,13 +705,14 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
             std::memcpy(ids.b, b + i0, m * sizeof(int32_t));
         p.d.n = m;
         p.d.total_segs = m * p.d.nl * p.d.C * p.d.segs;
-        const uint32_t per_cta = p.bulk ? 1u : (uint32_t)(p.threads / 32);   // segments in flight
+        const uint32_t per_cta = (p.bulk || p.tsp) ? 1u : (uint32_t)(p.threads / 32);
         const uint64_t need = ((uint64_t)p.d.total_segs + per_cta - 1) / per_cta;
         const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
         if (i0 == 0 && fault_hit(FP_LAUNCH))
             return fail(KV_ERR_CUDA, "launch of the move kernel: injected failure");
-        cudaError_t e = p.bulk ? launch_bulk(p.d, ids, ctas, stream)
-                               : launch_move(p.d, ids, ctas, p.threads, stream);
+        cudaError_t e = p.tsp    ? launch_tsp(p.d, ids, ctas, stream)
+                        : p.bulk ? launch_bulk(p.d, ids, ctas, stream)
+                                 : launch_move(p.d, ids, ctas, p.threads, stream);
         if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -847,12 +860,12 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             for (uint32_t i0 = 0; i0 < n; i0 += (uint32_t)std::min<uint64_t>(fit, n)) {
                 const uint32_t m = (uint32_t)std::min<uint64_t>(fit, n - i0);
                 const Side ss = staging_side(stg, pool->g, host->heads, g_n, la, m);
-                const bool bulk = use_bulk(pool->g, ps, ss);
+                const int kernel = hbm_kernel(pool->g, ps, ss);
                 Plan p;
                 st = plan(pool->g, backup ? ps : ss, backup ? ss : ps, g_n, la, ds.err_dev, backup,
-                          &p, bulk);
+                          &p, kernel);
                 if (st != KV_OK) return st;
-                const int ctas = default_ctas(ds, false, bulk);
+                const int ctas = default_ctas(ds, false, kernel);
                 if (backup) {
                     st = run_moves(p, a + i0, nullptr, m, ctas, stream, true);
                     if (st == KV_OK)
@@ -921,16 +934,16 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
             return fail(KV_ERR_INVALID_ARG, "buffer %p is not device memory of device %d", buf, d);
         const Side ps = pool_side(*pool);
         const Side bs = staging_side((char *)buf, g, buf_heads, nl, l0, n);
-        const bool bulk = use_bulk(g, ps, bs);
+        const int kernel = hbm_kernel(g, ps, bs);
         Plan p;
         st = plan(g, kind == 0 ? ps : bs, kind == 0 ? bs : ps, nl, l0, ds.err_dev, kind == 0, &p,
-                  bulk);
+                  kernel);
         if (st != KV_OK) return st;
         FenceSlot fs;
         st = reserve_fence(d, &fs);
         if (st != KV_OK) return st;
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
-        const int ctas = default_ctas(ds, false, bulk);
+        const int ctas = default_ctas(ds, false, kernel);
         if (kind == 0) {
             st = run_moves(p, pages, nullptr, n, ctas, stream, true, &ds, &fs);
         } else {

@@ -48,6 +48,12 @@ constexpr int kWideThreads = 1024;  // wide CTAs: host-link moves packed onto fe
 constexpr int kBulkStages = 8;
 constexpr uint32_t kBulkBytes = 8192;
 constexpr int kBulkThreads = 32;
+// Transposing variant for HBM-only moves whose sides differ in head order:
+// whole chunks are bulk-loaded into a ring of shared-memory stages and 256
+// threads write them out in destination order.  Chunks up to kTspMaxChunk.
+constexpr int kTspThreads = 256;
+constexpr uint32_t kTspSmem = 196608;        // ring bytes per CTA (1 CTA per SM)
+constexpr uint32_t kTspMaxChunk = kTspSmem / 2;
 
 struct MoveDesc {
     Side src, dst;
@@ -109,6 +115,9 @@ cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int thr
 // Launch the bulk-copy variant (identity chunks only; d.segs / d.div_segs /
 // d.total_segs count kBulkBytes segments).  `ctas` CTAs of kBulkThreads.
 cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
+// Launch the transposing variant (d.segs = 1: one work item per chunk; chunk
+// bytes <= kTspMaxChunk).  `ctas` CTAs of kTspThreads.
+cudaError_t launch_tsp(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream);
 // Launch the completion marker: stores `seq` to `word` (system scope, release)
 // once everything before it on `stream` has finished.
 cudaError_t launch_mark(unsigned long long *word, unsigned long long seq, cudaStream_t stream);

@@ -435,6 +435,89 @@ __global__ void __launch_bounds__(kBulkThreads)
     if (d.fence_word != nullptr) complete_grid(d);
 }
 
+// ------------------------------------------------- transposing bulk path
+
+// One chunk per work item: lane 0 of warp 0 bulk-loads whole chunks (T*H*B
+// bytes, contiguous on the source side) into a ring of `stages` shared-memory
+// buffers; every thread waits on the chunk's mbarrier, then the CTA writes the
+// chunk in destination order -- consecutive threads store consecutive 16-byte
+// pieces (fully coalesced) and read the matching pieces of the source order
+// from shared memory (B-byte runs, conflict-free).  Waits are bounded; a CTA
+// that gives up waits (bounded) for its loads in flight and sets the error word.
+template <int kCap>
+__global__ void __launch_bounds__(kTspThreads, 1)
+    kv_tsp_kernel(const __grid_constant__ MoveDesc d, const __grid_constant__ IdsT<kCap> ids,
+                  uint32_t stage_bytes, uint32_t stages) {
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) unsigned long long bar[kTspSmem / 4096];
+    if (d.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t cb = d.cb16 * 16u;
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < stages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    auto issue = [&](uint32_t w, uint32_t s) {   // thread 0 only
+        const BulkSeg g = bulk_segment(d, ids.a, ids.b, w);
+        const uint32_t b = smem_addr(&bar[s]);
+        const uint32_t bytes = g.ok ? cb : 0u;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes)
+                     : "memory");
+        if (bytes)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                "[%0], [%1], %2, [%3];" ::"r"(smem_addr(ring + s * stage_bytes)), "l"(g.src),
+                "r"(bytes), "r"(b)
+                : "memory");
+    };
+    const uint32_t first = blockIdx.x, step = gridDim.x;
+    if (threadIdx.x == 0)
+        for (uint32_t s = 0; s < stages; ++s) {
+            const uint64_t w = first + (uint64_t)s * step;
+            if (w >= d.total_segs) break;
+            issue((uint32_t)w, s);
+        }
+    uint32_t parity = 0;
+    bool failed = false;
+    for (uint32_t i = 0;; ++i) {
+        const uint64_t w = first + (uint64_t)i * step;
+        if (w >= d.total_segs) break;
+        const uint32_t s = i % stages;
+        const bool ok = mbar_wait(smem_addr(&bar[s]), (parity >> s) & 1u);
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        parity ^= 1u << s;
+        const BulkSeg g = bulk_segment(d, ids.a, ids.b, (uint32_t)w);
+        if (g.ok) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(ring + s * stage_bytes);
+            char *dst = g.dst;
+            for (uint32_t q = threadIdx.x; q < d.cb16; q += kTspThreads) {
+                const uint32_t qs = permute_piece(q, d.dst.hnd, d);
+                store16(dst + (uint64_t)q * 16u, src[qs]);
+            }
+        } else if (threadIdx.x == 0 && d.err != nullptr) {
+            *(volatile uint32_t *)d.err = 1u;   // unreachable after host validation
+        }
+        __syncthreads();   // every read of this stage is done
+        const uint64_t wn = w + (uint64_t)stages * step;
+        if (threadIdx.x == 0 && wn < d.total_segs) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue((uint32_t)wn, s);
+        }
+    }
+    if (d.pdl) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0 && failed) {
+        // loads may still be landing in this CTA's shared memory: wait for all
+        for (uint32_t s = 0; s < stages; ++s) mbar_wait(smem_addr(&bar[s]), (parity >> s) & 1u);
+        if (d.err != nullptr) *(volatile uint32_t *)d.err = 2u;
+    }
+    if (d.fence_word != nullptr) complete_grid(d);
+}
+
 __global__ void kv_mark_kernel(unsigned long long *word, unsigned long long seq) {
     if (threadIdx.x == 0) {
         __threadfence_system();
@@ -553,6 +636,54 @@ cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStr
     if (d.n <= 64) return launch_bulk_cap<64>(d, ids, ctas, stream);
     if (d.n <= 512) return launch_bulk_cap<512>(d, ids, ctas, stream);
     return launch_bulk_cap<kMaxItems>(d, ids, ctas, stream);
+}
+
+template <int kCap>
+static cudaError_t launch_tsp_cap(const MoveDesc &d, const MoveIds &ids, int ctas,
+                                  cudaStream_t stream) {
+    static bool attr_set = false;   // per instantiation; host calls are serialised
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kv_tsp_kernel<kCap>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kTspSmem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const uint32_t cb = d.cb16 * 16u;
+    const uint32_t stage = (cb + 127u) / 128u * 128u;
+    uint32_t stages = kTspSmem / stage;
+    if (stages > 4) stages = 4;
+    if (stages < 2) return cudaErrorInvalidValue;
+    IdsT<kCap> p;
+    for (uint32_t i = 0; i < d.n; ++i) {
+        p.a[i] = ids.a[i];
+        p.b[i] = ids.b[i];
+    }
+    const size_t smem = (size_t)stages * stage;
+    if (d.pdl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas);
+        cfg.blockDim = dim3((unsigned)kTspThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kv_tsp_kernel<kCap>, d, p, stage, stages);
+    }
+    kv_tsp_kernel<kCap><<<ctas, kTspThreads, smem, stream>>>(d, p, stage, stages);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tsp(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
+    (void)cudaGetLastError();
+    if (d.n > (uint32_t)kMaxItems || !d.transpose || d.segs != 1 || d.cb16 * 16u > kTspMaxChunk)
+        return cudaErrorInvalidValue;
+    if (d.n <= 64) return launch_tsp_cap<64>(d, ids, ctas, stream);
+    if (d.n <= 512) return launch_tsp_cap<512>(d, ids, ctas, stream);
+    return launch_tsp_cap<kMaxItems>(d, ids, ctas, stream);
 }
 
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int threads,
