@@ -466,12 +466,15 @@ def run_ours(args):
             if i >= 1:
                 ts.append(e0.elapsed_time(e1) / 1000 / gathers)
         gb_s = 2 * n * g.page_bytes / statistics.median(ts) / GB
-        hbm = {"bound": "hbm", "kernel": ("kv_move_kernel" if args.no_bulk or g.dev_heads != g.host_heads
-                                          else "kv_bulk_kernel") +
+        hbm = {"bound": "hbm", "kernel": ("kv_move_kernel" if args.no_bulk else
+                                          "kv_tsp_kernel" if g.dev_heads != g.host_heads else
+                                          "kv_bulk_kernel") +
                          " (device gather, pool -> device buffer in host layout)",
                "achieved": round(gb_s, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                "frac": round(gb_s / peaks["hbm_gbs"], 4),
-               "traffic": recorded_traffic("device_gather_dram_bytes_per_launch"),
+               "traffic": recorded_traffic("device_gather_transposed_dram_bytes_per_launch"
+                                           if g.dev_heads != g.host_heads else
+                                           "device_gather_dram_bytes_per_launch"),
                "algorithmic_bytes_per_launch": 2 * n * g.page_bytes,
                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
         del buf
