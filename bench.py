@@ -89,11 +89,18 @@ def measured_peaks():
 
 
 def kernel_sha():
+    """Hash of the kernels' code (comments and blank space removed), so that
+    recorded profiler figures stay attached to the code they were taken on."""
+    import re
+
     h = hashlib.sha256()
     for rel in ("hierarchical_kv_cache_backup_gb300/csrc/kvb_kernels.cu",
                 "hierarchical_kv_cache_backup_gb300/csrc/kvb_internal.h"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

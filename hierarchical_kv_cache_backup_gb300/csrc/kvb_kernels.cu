@@ -1,27 +1,35 @@
 // kvb_kernels.cu -- sm_103a kernels of the KV backup / restore engine.
 //
-// kv_move: the one data-movement kernel.  It copies whole KV "chunks" (the
-// T*H*B bytes of one page-or-slot, layer and component) from a source side to
-// a destination side, optionally permuting the head order inside each chunk
-// (HND <-> NHD).  Both sides are described by strides (kvb_internal.h), so
-// the same kernel serves
-//   - backup, zero-copy : pool (HBM)          -> host tier (mapped pinned memory)
-//   - restore, zero-copy: host tier (mapped)  -> pool (HBM)
-//   - staged gather     : pool                -> device staging buffer (HBM only)
-//   - staged scatter    : device staging      -> pool
-// This is the BACKUP / RESTORE data movement of "[RFC][HiCache] Out-of-process
-// HiCache data plane with device-memory IPC" (§Device IPC data path), with
-// the layer restriction of "[PP + HiCache] Add PP Prefetch Tickets" (§PP
-// Prefetch Ticket Path, layer-wise H2D) and the HND pool of "LMCache
+// The data movement of BACKUP / RESTORE in "[RFC][HiCache] Out-of-process
+// HiCache data plane with device-memory IPC" (§Device IPC data path), with the
+// layer restriction of "[PP + HiCache] Add PP Prefetch Tickets" (§PP Prefetch
+// Ticket Path, layer-wise H2D) and the HND pool of "LMCache
 // RawCudaIPCWrapper深度解析" (§在项目中的实际接入方式).  Payload moves as raw
-// 16-byte integer vectors: no float type touches it (§uint8字节往返).
+// 16-byte integer vectors or bulk copies: no float type touches it
+// (§uint8字节往返).  Every kernel copies whole KV "chunks" (the T*H*B bytes of
+// one page-or-slot, layer and component) from a source side to a destination
+// side described by strides or a per-(layer, component) table
+// (kvb_internal.h), optionally permuting the head order inside each chunk.
 //
-// Work split: the op is a flat list of 4 KiB warp segments (chunk, segment);
-// warps stride over it.  A segment's id lookup and address math happen once;
-// then each lane issues eight independent 16-byte loads (4 KiB in flight per
-// warp) followed by eight stores, so consecutive lanes touch consecutive
-// 16-byte pieces: every warp-wide access covers 512 contiguous bytes, or B-byte
-// runs (B >= 16, usually 128-576) when a head permutation is fused in.
+//   kv_move_kernel  registers as staging; host-link moves (zero-copy backup /
+//                   restore over mapped pinned memory) and the fallback for
+//                   HBM-only moves.  The op is a flat list of 4 KiB warp
+//                   segments; warps take them by grid stride (or, for a
+//                   progressive layer restore, from a ticket counter in layer
+//                   order).  Per segment one id lookup and address decode,
+//                   then eight independent 16-byte loads per lane (4 KiB in
+//                   flight per warp) and eight stores: each warp-wide access
+//                   covers 512 contiguous bytes, or B-byte runs when a head
+//                   permutation is fused in.
+//   kv_bulk_kernel  HBM-only identity moves through cp.async.bulk and an
+//                   8-stage shared-memory ring (one warp per CTA).
+//   kv_tsp_kernel   HBM-only moves that change head order: whole chunks
+//                   bulk-loaded into shared memory, written in destination
+//                   order by 256 threads.
+//   kv_gate_kernel  bounded wait for a ready fence before a gated backup.
+//   kv_mark_kernel  stores a fence word after copy-engine work.
+// The move kernels complete their op's fence from their last CTA; all waits
+// inside kernels are bounded and nothing traps.
 #include "kvb_internal.h"
 
 namespace kvb {
