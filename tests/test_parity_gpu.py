@@ -538,3 +538,51 @@ def test_restore_layers_limits_and_empty():
         assert e.value.status == kvb.KV_ERR_DUPLICATE
     finally:
         rig.close()
+
+
+def test_many_threads_many_streams():
+    """Four host threads issue backups and restores at once, each on its own stream and
+    slot range; every byte ends as the oracle says (ops of one thread in order)."""
+    import threading
+
+    import oracle
+    from gpu_rig import oracle_geom
+
+    g = wl.LLAMA8B.geom.with_(P=64, L=4)
+    rig = Rig(g, 64, seed=71)
+    try:
+        snap = rig.snapshot()
+        plans = []
+        r = np.random.default_rng(9)
+        for t in range(4):
+            ops = []
+            for k in range(25):
+                src = r.permutation(g.P)[:4]
+                slots = t * 16 + r.permutation(16)[:4]
+                ops.append((src, slots))
+            plans.append(ops)
+        errors = []
+
+        def worker(t):
+            try:
+                s = torch.cuda.Stream()
+                last = None
+                for src, slots in plans[t]:
+                    last = kvb.kv_backup(rig.pool, rig.hostt, src, slots, s.cuda_stream)
+                kvb.kv_fence_wait(last, 60_000_000_000)
+            except Exception as e:   # reported below
+                errors.append(repr(e))
+
+        threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+        for th in threads:
+            th.start()
+        for th in threads:
+            th.join()
+        assert not errors, errors
+        host = snap[1].copy()
+        for t in range(4):               # slot ranges are disjoint across threads
+            for src, slots in plans[t]:
+                oracle.backup(oracle_geom(g), snap[0], host, src, slots)
+        rig.assert_equal((snap[0], host))
+    finally:
+        rig.close()
