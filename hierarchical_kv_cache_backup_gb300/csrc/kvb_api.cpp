@@ -1406,6 +1406,43 @@ kv_status kv_backup(kv_pool pool, kv_host host, const int32_t *src_pages,
     return issue(pool, host, 0, src_pages, host_slots, n, -1, stream, fence);
 }
 
+namespace {
+// Checks a ready word and returns its device-visible address (or an error).
+kv_status ready_word_dev(const uint64_t *ready_word, uint64_t ready_timeout_ns,
+                         const void **dev_word) {
+    if (ready_word == nullptr) return fail(KV_ERR_INVALID_ARG, "ready_word is NULL");
+    if (((uintptr_t)ready_word) % 8 != 0)
+        return fail(KV_ERR_ALIGNMENT, "ready_word %p is not 8-byte aligned", (const void *)ready_word);
+    if (ready_timeout_ns > kMaxReadyTimeoutNs)
+        return fail(KV_ERR_INVALID_ARG, "ready_timeout_ns %llu exceeds the %llu ns limit",
+                    (unsigned long long)ready_timeout_ns, (unsigned long long)kMaxReadyTimeoutNs);
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, ready_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(ready_word)");
+    *dev_word = nullptr;
+    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
+        *dev_word = ready_word;
+    else if (attr.type == cudaMemoryTypeHost)
+        *dev_word = attr.devicePointer;
+    if (*dev_word == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "ready_word %p is not visible to the GPU (use device or "
+                    "pinned mapped host memory)", (const void *)ready_word);
+    return KV_OK;
+}
+}  // namespace
+
+kv_status kv_restore_when_ready(kv_pool pool, kv_host host, const int32_t *host_slots,
+                                const int32_t *dst_pages, uint32_t n, int32_t layer,
+                                const uint64_t *ready_word, uint64_t ready_value,
+                                uint64_t ready_timeout_ns, void *stream, kv_fence *fence) {
+    const void *dev_word = nullptr;
+    kv_status st = ready_word_dev(ready_word, ready_timeout_ns, &dev_word);
+    if (st != KV_OK) return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue(pool, host, 1, host_slots, dst_pages, n, layer, stream, fence,
+                 (const unsigned long long *)dev_word, ready_value, ready_timeout_ns);
+}
+
 kv_status kv_backup_when_ready(kv_pool pool, kv_host host, const int32_t *src_pages,
                                const int32_t *host_slots, uint32_t n, const uint64_t *ready_word,
                                uint64_t ready_value, uint64_t ready_timeout_ns, void *stream,

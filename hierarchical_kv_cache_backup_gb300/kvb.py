@@ -44,7 +44,7 @@ KVB_IPC_MAGIC = 0x4B564231
 # the symbols include/kvb.h declares
 EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_pool_import", "kv_pool_close",
            "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
-           "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
+           "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_restore_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
@@ -110,6 +110,7 @@ def _load():
         "kv_backup": (st, [vp, vp, vp, vp, u32, vp, P(u64)]),
         "kv_restore": (st, [vp, vp, vp, vp, u32, i32, vp, P(u64)]),
         "kv_restore_layers": (st, [vp, vp, vp, vp, u32, u32, u32, vp, P(u64)]),
+        "kv_restore_when_ready": (st, [vp, vp, vp, vp, u32, i32, vp, u64, u64, vp, P(u64)]),
         "kv_backup_when_ready": (st, [vp, vp, vp, vp, u32, vp, u64, u64, vp, P(u64)]),
         "kv_device_gather": (st, [vp, vp, u64, u32, vp, u32, vp, P(u64)]),
         "kv_device_scatter": (st, [vp, vp, u64, u32, vp, u32, i32, vp, P(u64)]),
@@ -262,6 +263,19 @@ def kv_backup_when_ready(pool: int, host: int, src_pages, host_slots, ready_word
     f = ctypes.c_uint64()
     _check(_lib.kv_backup_when_ready(pool, host, pa, pb, a.size, ready_word, ready_value,
                                      ready_timeout_ns, stream, ctypes.byref(f)))
+    return f.value
+
+
+def kv_restore_when_ready(pool: int, host: int, host_slots, dst_pages, ready_word: int,
+                          ready_value: int, ready_timeout_ns: int, layer: int = -1,
+                          stream=None) -> int:
+    a, pa = _ids(host_slots)
+    b, pb = _ids(dst_pages)
+    if a.size != b.size:
+        raise ValueError("host_slots and dst_pages differ in length")
+    f = ctypes.c_uint64()
+    _check(_lib.kv_restore_when_ready(pool, host, pa, pb, a.size, layer, ready_word, ready_value,
+                                      ready_timeout_ns, stream, ctypes.byref(f)))
     return f.value
 
 

@@ -253,6 +253,18 @@ KVB_API kv_status kv_backup_when_ready(kv_pool pool, kv_host host, const int32_t
                                        const uint64_t *ready_word, uint64_t ready_value,
                                        uint64_t ready_timeout_ns, void *stream, kv_fence *fence);
 
+/* RESTORE gated on its data being in the host tier ([PR] §PP Prefetch Ticket
+ * Path: the storage GET lands in host memory before the layer-wise H2D).  As
+ * kv_restore, but on the GPU the copy waits until the 64-bit `ready_word`
+ * holds a value >= ready_value (set by whoever fills the host slots: a
+ * storage client, another process, the host); same rules for the word and the
+ * bounded wait as kv_backup_when_ready.  On time-out no pool byte is written
+ * and the fence completes with KV_ERR_ABORTED.  Always the zero-copy path. */
+KVB_API kv_status kv_restore_when_ready(kv_pool pool, kv_host host, const int32_t *host_slots,
+                                        const int32_t *dst_pages, uint32_t n, int32_t layer,
+                                        const uint64_t *ready_word, uint64_t ready_value,
+                                        uint64_t ready_timeout_ns, void *stream, kv_fence *fence);
+
 /* RESTORE ([RFC] §Device IPC data path; layer-wise per [PR] §PP Prefetch
  * Ticket Path): for every i < n, page dst_pages[i] receives the units of
  * host slot host_slots[i] for every layer (layer = -1) or for that one layer

@@ -586,3 +586,32 @@ def test_many_threads_many_streams():
         rig.assert_equal((snap[0], host))
     finally:
         rig.close()
+
+
+def test_restore_when_ready_waits_and_gives_up():
+    """RESTORE gated on its host data: nothing is written until the word arrives; a word
+    that never arrives leaves the pool untouched and the fence reports ABORTED."""
+    g = wl.MLA_FP8.geom.with_(P=16, L=6)
+    rig = Rig(g, 4, seed=41)
+    word = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    try:
+        snap = rig.snapshot()
+        want = rig.expect_restore(snap, [0, 3], [9, 2], 4)
+        f = kvb.kv_restore_when_ready(rig.pool, rig.hostt, [0, 3], [9, 2], word.data_ptr(), 2,
+                                      20_000_000_000, layer=4)
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_fence_wait(f, 50_000_000)
+        assert e.value.status == kvb.KV_ERR_TIMEOUT
+        rig.assert_equal(snap)
+        word[0] = 2
+        kvb.kv_fence_wait(f, 20_000_000_000)
+        rig.assert_equal(want)
+        snap2 = rig.snapshot()
+        f = kvb.kv_restore_when_ready(rig.pool, rig.hostt, [1], [5], word.data_ptr(), 3,
+                                      200_000_000)
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_fence_wait(f, 20_000_000_000)
+        assert e.value.status == kvb.KV_ERR_ABORTED
+        rig.assert_equal(snap2)
+    finally:
+        rig.close()
