@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["llama8b", "mla_fp8", "trtllm_ipc"], default="llama8b")
-    p.add_argument("--mode", choices=["zero_copy", "staged"], default="zero_copy")
+    p.add_argument("--mode", choices=["zero_copy", "staged", "copy_engine"], default="zero_copy")
     p.add_argument("--max-ctas", type=int, default=0)
     p.add_argument("--no-bulk", action="store_true",
                    help="HBM-only moves use the register kernel instead of bulk copies")
@@ -202,17 +202,18 @@ def _exporter(q, done, device, seed, pool_offset):
 # ------------------------------------------------------------- CPU oracle leg
 
 def oracle_sample(cpu_seconds: float, steps: int | None = None, n_sample: int = 512,
-                  pool_pages: int = 1024):
+                  pool_pages: int = 1024, threads: int | None = None):
     """Times the CPU oracle (as it stands) on the host cores: backup of n_sample
     random pages of the Llama-8B geometry, then restore into n_sample others, on a
-    pool of ``pool_pages`` pages.  Returns (GB/s, threads, sample text, per-step s)."""
+    pool of ``pool_pages`` pages, with ``threads`` threads (all cores by default).
+    Returns (GB/s, threads, sample text, per-step s)."""
     import oracle
 
     g = wl.LLAMA8B.geom.with_(P=pool_pages)
     og = oracle.geom(g.L, g.C, g.P, g.T, g.H, g.B)
     pool = np.full(g.pool_bytes, 7, dtype=np.uint8)
     host = np.full(n_sample * g.page_bytes, 3, dtype=np.uint8)
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     r = wl.rng(wl.LLAMA8B.seed)
     per_step = 2 * n_sample * g.page_bytes
     times = []
@@ -292,7 +293,8 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    mode = kvb.KV_MODE_STAGED if args.mode == "staged" else kvb.KV_MODE_ZERO_COPY
+    mode = {"zero_copy": kvb.KV_MODE_ZERO_COPY, "staged": kvb.KV_MODE_STAGED,
+            "copy_engine": kvb.KV_MODE_COPY_ENGINE}[args.mode]
     kvb.kv_config_set(mode, args.max_ctas, 0, (kvb.KV_CFG_NO_BULK if args.no_bulk else 0) |
                       (kvb.KV_CFG_NO_PDL if args.no_pdl else 0))
 
@@ -409,7 +411,11 @@ def run_ours(args):
         fb = kvb.kv_backup(pool, tier, ids.backup_src, ids.backup_slots, s_a.cuda_stream)
         if evs:
             evs[1].record(s_a)
+        if evs:
+            evs[3].record(s_b)
         fr = kvb.kv_restore(pool, tier, ids.restore_slots, ids.restore_dst, -1, s_b.cuda_stream)
+        if evs:
+            evs[4].record(s_b)
         ev2 = torch.cuda.Event()
         ev2.record(s_b)
         s_a.wait_event(ev2)
@@ -427,7 +433,7 @@ def run_ours(args):
     barrier()
 
     # ---- timed region: device clock (CUDA events on the launching stream)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     l0 = kvb.kv_launch_count()
     with ClockSampler(local) as clk:
         barrier()
@@ -442,6 +448,8 @@ def run_ours(args):
     elapsed = dist_max(t_start.elapsed_time(t_end) / 1000, dist, dev)
     b_ms = [e[0].elapsed_time(e[1]) for e in evs]
     r_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if w is wl.TRTLLM:   # the restore ran on stream B, bracketed by its own events
+        r_ms = [e[3].elapsed_time(e[4]) for e in evs]
     step_bytes = bytes_b + bytes_r
     value = job_gbs(step_bytes, args.steps, ws, elapsed)
 
@@ -571,6 +579,79 @@ def run_ours(args):
                    "exposed_transfer_ms_progressive": round(t_p2 - t_c, 3)}
         del A, Bm, Cm
 
+    # ---- Llama-8B: write-through backup beside the prefill that fills the pages.
+    # The step's 512 pages are written by 8 chunks of a stand-in forward (bf16
+    # GEMMs on a compute stream, sized near one chunk's backup time); each chunk's
+    # 64 pages are backed up on the copy stream once that chunk's forward is done
+    # (a GPU-side event wait), so the backup of chunk k runs beside the forward of
+    # chunk k + 1.  Exposed backup = pipelined - compute-only; the last chunk's
+    # backup can never overlap and is reported beside it.
+    write_through = None
+    if w is wl.LLAMA8B:
+        comp = torch.cuda.Stream(device=dev)
+        M, per_chunk, chunks = 3456, 16, 8
+        A = torch.randn(M, M, dtype=torch.bfloat16, device=dev)
+        Bm = torch.randn(M, M, dtype=torch.bfloat16, device=dev)
+        Cm = torch.empty(M, M, dtype=torch.bfloat16, device=dev)
+        cp = w.n // chunks
+
+        def wt_timed(fn, reps=5):
+            out = []
+            for i in range(reps + 2):
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s_a)
+                ev = torch.cuda.Event()
+                ev.record(s_a)
+                comp.wait_event(ev)
+                fn(i)
+                ev2 = torch.cuda.Event()
+                ev2.record(comp)
+                s_a.wait_event(ev2)
+                e1.record(s_a)
+                e1.synchronize()
+                if i >= 2:
+                    out.append(e0.elapsed_time(e1))
+            return statistics.median(out)
+
+        def wt_compute(i):
+            with torch.cuda.stream(comp):
+                for _ in range(chunks * per_chunk):
+                    torch.matmul(A, Bm, out=Cm)
+
+        def wt_backup(i, last_only=False):
+            ids = idsets[i % R]
+            for c in range(chunks - 1 if last_only else 0, chunks):
+                sl = slice(c * cp, (c + 1) * cp)
+                kvb.kv_backup(pool, tier, ids.backup_src[sl], ids.backup_slots[sl],
+                              s_a.cuda_stream)
+
+        def wt_pipelined(i):
+            ids = idsets[i % R]
+            for c in range(chunks):
+                with torch.cuda.stream(comp):
+                    for _ in range(per_chunk):
+                        torch.matmul(A, Bm, out=Cm)
+                done = torch.cuda.Event()
+                done.record(comp)
+                s_a.wait_event(done)
+                sl = slice(c * cp, (c + 1) * cp)
+                kvb.kv_backup(pool, tier, ids.backup_src[sl], ids.backup_slots[sl],
+                              s_a.cuda_stream)
+
+        t_c = wt_timed(wt_compute)
+        t_b = wt_timed(wt_backup)
+        t_last = wt_timed(lambda i: wt_backup(i, True))
+        t_p = wt_timed(wt_pipelined)
+        write_through = {
+            "forward_stand_in": f"bf16 GEMM {M}^3 x {per_chunk} per chunk on a compute stream",
+            "chunks": chunks, "pages_per_chunk": cp,
+            "compute_only_ms": round(t_c, 3), "backup_only_ms": round(t_b, 3),
+            "pipelined_ms": round(t_p, 3), "exposed_backup_ms": round(t_p - t_c, 3),
+            "last_chunk_backup_ms": round(t_last, 3),
+            "exposed_beyond_last_chunk_ms": round(t_p - t_c - t_last, 3)}
+        del A, Bm, Cm
+
     # ---- small-op latency: the tiny workload (8 pages of 16 KiB) through the C ABI
     latency = None
     if w is wl.LLAMA8B:
@@ -615,8 +696,9 @@ def run_ours(args):
         dom_ms = statistics.mean(b_ms)
         dom_bytes = bytes_b
         dom_peak, dom_dir = link["d2h"], "d2h"
-        kern = "kv_move_kernel (backup, zero-copy D2H)" if mode == 0 else \
-            "kv_move_kernel + cudaMemcpyAsync (backup, staged D2H)"
+        kern = {0: "kv_move_kernel (backup, zero-copy D2H)",
+                1: "kv_move_kernel + cudaMemcpyAsync (backup, staged D2H)",
+                2: "cudaMemcpy2DAsync per page (backup, copy engine D2H)"}[mode]
     achieved = dom_bytes / (dom_ms / 1000) / GB
     roofline = {"bound": "host_link", "kernel": kern, "achieved": round(achieved, 2),
                 "peak": round(dom_peak, 2), "unit": "GB/s", "frac": round(achieved / dom_peak, 4),
@@ -624,12 +706,21 @@ def run_ours(args):
                 "algorithmic_bytes_per_launch": dom_bytes,
                 "peak_source": f"pinned cudaMemcpyAsync {dom_dir} of 2 GiB measured in this run, "
                                "best of 10 (host link peak; not in MEASURED_PEAKS.json)"}
-    backup_gbs = bytes_b / (statistics.mean(b_ms) / 1000) / GB if bytes_b and w is not wl.MLA_FP8 \
-        else None
-    restore_gbs = bytes_r / (statistics.mean(r_ms if w is wl.LLAMA8B else b_ms) / 1000) / GB \
-        if w is not wl.TRTLLM else None
+    # per-direction device times: the backup on stream A; the restore on stream A
+    # after it (llama8b), on stream B beside it (trtllm), or the 61 one-layer calls
+    op_b, op_r = (None, b_ms) if w is wl.MLA_FP8 else (b_ms, r_ms)
+    backup_gbs = bytes_b / (statistics.mean(op_b) / 1000) / GB if op_b else None
+    restore_gbs = bytes_r / (statistics.mean(op_r) / 1000) / GB
+
+    def op_stats(ms, pages):
+        return {"median_ms": round(statistics.median(ms), 4), "best_ms": round(min(ms), 4),
+                "pages_per_s": round(pages / (statistics.mean(ms) / 1000), 1)}
+
+    per_op = {"restore": op_stats(op_r, w.n)}
+    if op_b:
+        per_op["backup"] = op_stats(op_b, w.n)
     if w is wl.MLA_FP8:
-        restore_gbs = bytes_r / (statistics.mean(b_ms) / 1000) / GB
+        per_op["restore"]["per_layer_call_us"] = round(1000 * statistics.mean(op_r) / g.L, 2)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
@@ -647,14 +738,17 @@ def run_ours(args):
         "backup_gbs": round(backup_gbs, 2) if backup_gbs else None,
         "restore_gbs": round(restore_gbs, 2) if restore_gbs else None,
         "pages_per_s": round(ws * (w.n * (2 if bytes_b else 1)) * args.steps / elapsed, 1),
+        "per_op": per_op,
         "host_link_peak_gbs": {k: round(v, 2) for k, v in link.items()},
         "pct_of_host_link_peak": {
             "d2h": round(100 * backup_gbs / link["d2h"], 2) if backup_gbs else None,
             "h2d": round(100 * restore_gbs / link["h2d"], 2) if restore_gbs else None,
-            "step_vs_sequential_peak": round(
-                100 * value / ws / (step_bytes / ((bytes_b / link["d2h"] if bytes_b else 0) +
-                                                  bytes_r / link["h2d"])), 2)
-            if w is not wl.TRTLLM else round(100 * value / ws / link["bidir"], 2)},
+            **({"step_vs_bidir_peak": round(100 * value / ws / link["bidir"], 2),
+                "note": "d2h / h2d: each direction while the other runs, against its solo peak"}
+               if w is wl.TRTLLM else
+               {"step_vs_sequential_peak": round(
+                   100 * value / ws / (step_bytes / ((bytes_b / link["d2h"] if bytes_b else 0) +
+                                                     bytes_r / link["h2d"])), 2)})},
         "roofline": roofline,
         "roofline_hbm": hbm,
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": bytes_r +
@@ -665,6 +759,7 @@ def run_ours(args):
         "latency_small_ops": latency,
         "layerwise_progressive": progressive,
         "overlap_with_compute": overlap,
+        "write_through": write_through,
         "clocks": clk.summary(),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -673,6 +768,10 @@ def run_ours(args):
         gbs, used, sample, _ = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": used,
                                 "kind": "oracle", "sample": sample}
+        gbs1, _, sample1, _ = oracle_sample(max(1.0, args.cpu_seconds / 4), n_sample=64,
+                                            threads=1)
+        line["cpu_baseline_single_thread"] = {"value": round(gbs1, 3), "unit": "GB/s",
+                                              "cores": 1, "kind": "oracle", "sample": sample1}
     else:
         line["cpu_baseline"] = None
     kvb.kv_pool_close(pool)

@@ -159,6 +159,7 @@ struct PoolObj {
     // split pools: one device buffer per (layer, component); the table of their
     // addresses (entry l * C + c) lives in device memory for the kernels
     unsigned long long *table_dev = nullptr;
+    std::vector<unsigned long long> table_host;   // the same table, for copy-engine moves
 };
 
 struct HostObj {
@@ -773,6 +774,100 @@ kv_status staged_copies(const HostObj &h, char *staging, const int32_t *slots, u
     return KV_OK;
 }
 
+// One (page, layer, component) chunk between the pool and a host slot through
+// the copy engine.  Same head order (or H = 1 or T = 1): one copy of cb bytes.
+// Otherwise the chunk is transposed with min(H, T) pitched copies of B-byte
+// rows: per head, T rows; or per token, H rows.
+kv_status ce_chunk(const Geo &g, char *dst, uint32_t dst_hnd, const char *src, uint32_t src_hnd,
+                   cudaMemcpyKind kind, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    const uint64_t B = g.B, H = g.H, T = g.T;
+    if (src_hnd == dst_hnd || H == 1 || T == 1) {
+        e = cudaMemcpyAsync(dst, src, g.cb, kind, stream);
+    } else if (H <= T) {
+        // per head h: the T vectors are contiguous in HND ([H][T][B]) and H*B apart in NHD
+        for (uint64_t h = 0; h < H && e == cudaSuccess; ++h) {
+            const bool to_nhd = dst_hnd == KV_NHD;
+            char *dp = dst + (to_nhd ? h * B : h * T * B);
+            const char *sp = src + (to_nhd ? h * T * B : h * B);
+            e = cudaMemcpy2DAsync(dp, to_nhd ? H * B : B, sp, to_nhd ? B : H * B, B, T, kind,
+                                  stream);
+        }
+    } else {
+        // per token t: the H vectors are contiguous in NHD ([T][H][B]) and T*B apart in HND
+        for (uint64_t t = 0; t < T && e == cudaSuccess; ++t) {
+            const bool to_nhd = dst_hnd == KV_NHD;
+            char *dp = dst + (to_nhd ? t * H * B : t * B);
+            const char *sp = src + (to_nhd ? t * B : t * H * B);
+            e = cudaMemcpy2DAsync(dp, to_nhd ? B : T * B, sp, to_nhd ? T * B : B, B, H, kind,
+                                  stream);
+        }
+    }
+    return e == cudaSuccess ? KV_OK : cuda_fail(e, "copy-engine cudaMemcpy*Async");
+}
+
+// KV_MODE_COPY_ENGINE: the backup (pool -> host) or restore (host -> pool) of
+// items [0, n), layers [l0, l0 + nl), issued as copy-engine copies of the
+// pinned host tier.  `pages` / `slots` are the validated ids.  One contiguous
+// pool with the host's head order: one pitched copy per item (its nl x C
+// chunks are evenly spaced on both sides), or one copy for a run of items whose
+// pages and slots both step by one and whose spans are contiguous.  Split pools
+// and head-order changes: per chunk (ce_chunk).
+kv_status ce_copies(const PoolObj &pool, const HostObj &host, bool backup, const int32_t *pages,
+                    const int32_t *slots, uint32_t n, uint32_t nl, uint32_t l0,
+                    cudaStream_t stream) {
+    const Geo &g = pool.g;
+    const cudaMemcpyKind kind = backup ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice;
+    const Side ps = pool_side(pool);
+    const uint64_t nchunks = (uint64_t)nl * g.C;
+    const bool same_heads = pool.g.heads == host.heads || g.H == 1 || g.T == 1;
+    auto dev_chunk = [&](uint64_t p, uint64_t l, uint64_t c) -> char * {
+        if (!pool.table_host.empty())
+            return (char *)(uintptr_t)pool.table_host[l * g.C + c] + p * g.cb;
+        return pool.dev + p * ps.s_id + l * ps.s_l + c * ps.s_c;
+    };
+    auto host_chunk = [&](uint64_t s, uint64_t l, uint64_t c) -> char * {
+        return host.host + s * g.pb + (l * g.C + c) * g.cb;
+    };
+    if (!same_heads || !pool.table_host.empty()) {
+        for (uint32_t i = 0; i < n; ++i)
+            for (uint64_t l = l0; l < l0 + nl; ++l)
+                for (uint64_t c = 0; c < g.C; ++c) {
+                    char *dp = dev_chunk((uint64_t)pages[i], l, c);
+                    char *hp = host_chunk((uint64_t)slots[i], l, c);
+                    kv_status st = backup ? ce_chunk(g, hp, host.heads, dp, pool.g.heads, kind, stream)
+                                          : ce_chunk(g, dp, pool.g.heads, hp, host.heads, kind, stream);
+                    if (st != KV_OK) return st;
+                }
+        return KV_OK;
+    }
+    // chunk j = (l - l0) * C + c sits at j * s_c in the pool (s_l = C * s_c in both
+    // orders) and at j * cb in the slot
+    const uint64_t dev_pitch = ps.s_c;
+    const bool contiguous = nchunks == 1 || dev_pitch == g.cb;   // one run on both sides
+    const uint64_t span = nchunks * g.cb;
+    const bool mergeable = contiguous && ps.s_id == span && g.pb == span;
+    for (uint32_t i = 0; i < n;) {
+        uint32_t j = i + 1;
+        if (mergeable)
+            while (j < n && pages[j] == pages[j - 1] + 1 && slots[j] == slots[j - 1] + 1) ++j;
+        char *dp = dev_chunk((uint64_t)pages[i], l0, 0);
+        char *hp = host_chunk((uint64_t)slots[i], l0, 0);
+        cudaError_t e;
+        if (contiguous) {
+            const uint64_t bytes = (uint64_t)(j - i) * span;
+            e = backup ? cudaMemcpyAsync(hp, dp, bytes, kind, stream)
+                       : cudaMemcpyAsync(dp, hp, bytes, kind, stream);
+        } else {
+            e = backup ? cudaMemcpy2DAsync(hp, g.cb, dp, dev_pitch, g.cb, nchunks, kind, stream)
+                       : cudaMemcpy2DAsync(dp, dev_pitch, hp, g.cb, g.cb, nchunks, kind, stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "copy-engine cudaMemcpy*Async");
+        i = j;
+    }
+    return KV_OK;
+}
+
 // Issues one backup (kind 0) or restore (kind 1).  g_mu held.
 // `ready` (device-visible, or NULL): BACKUP's ready_fence -- the move starts
 // only once *ready >= ready_value, waited for on the GPU for at most
@@ -833,6 +928,10 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false, &ds, &fs);
         if (st != KV_OK) return st;
         fused = true;
+    } else if (n > 0 && g_cfg.mode == KV_MODE_COPY_ENGINE) {
+        st = backup ? ce_copies(*pool, *host, true, a, b, n, nl, l0, stream)
+                    : ce_copies(*pool, *host, false, b, a, n, nl, l0, stream);
+        if (st != KV_OK) return st;
     } else if (n > 0) {
         st = ensure_staging(ds);
         if (st != KV_OK) return st;
@@ -1080,7 +1179,7 @@ kv_status kv_config_get(kv_config *out) {
 
 kv_status kv_config_set(const kv_config *cfg) {
     if (cfg == nullptr) return fail(KV_ERR_INVALID_ARG, "config is NULL");
-    if (cfg->mode > KV_MODE_STAGED) return fail(KV_ERR_INVALID_ARG, "unknown mode %u", cfg->mode);
+    if (cfg->mode > KV_MODE_COPY_ENGINE) return fail(KV_ERR_INVALID_ARG, "unknown mode %u", cfg->mode);
     if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
     if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
         return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
@@ -1204,6 +1303,7 @@ kv_status kv_pool_register_split(const kv_layout *layout, void *const *bases,
         return fail(KV_ERR_NO_MEMORY, "out of host memory");
     }
     p->table_dev = (unsigned long long *)tdev;
+    p->table_host.swap(table);
     std::lock_guard<std::mutex> lk(g_mu);
     const uint64_t id = g_next_handle++;
     g_pools[id] = p;

@@ -36,7 +36,7 @@ STATUS_NAMES = {v: k for k, v in dict(globals()).items() if k.startswith("KV_OK"
 
 KV_LAYER_FIRST, KV_PAGE_FIRST = 0, 1
 KV_NHD, KV_HND = 0, 1
-KV_MODE_ZERO_COPY, KV_MODE_STAGED = 0, 1
+KV_MODE_ZERO_COPY, KV_MODE_STAGED, KV_MODE_COPY_ENGINE = 0, 1, 2
 KV_CFG_NO_BULK = 1
 KV_CFG_NO_PDL = 2
 KVB_IPC_MAGIC = 0x4B564231
@@ -150,9 +150,21 @@ def _check(status: int):
         raise KvError(status, _lib.kv_last_error().decode(errors="replace"))
 
 
+_I32 = np.dtype(np.int32)
+
+
 def _ids(x):
-    a = np.ascontiguousarray(np.asarray(x, dtype=np.int32))
-    return a, (a.ctypes.data if a.size else None)
+    """An int32 C-contiguous view or copy of `x` and its address (None if empty).
+    Arrays that already qualify pass through; the address comes from the buffer
+    protocol (cheaper than ndarray.ctypes on every call)."""
+    if type(x) is not np.ndarray or x.dtype != _I32 or not x.flags.c_contiguous:
+        x = np.ascontiguousarray(x, dtype=np.int32)
+    if x.size == 0:
+        return x, None
+    try:
+        return x, ctypes.addressof(ctypes.c_char.from_buffer(x))
+    except TypeError:                       # read-only buffer
+        return x, x.ctypes.data
 
 
 def make_layout(L, C, P, T, H, B, order=KV_LAYER_FIRST, heads=KV_NHD, elem_bytes=2) -> kv_layout:

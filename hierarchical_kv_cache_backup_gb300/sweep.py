@@ -6,10 +6,10 @@ Pool: 8192 pages of one opaque run each (L = C = T = H = 1, B = page bytes),
 random payload.  For every page size in 4 KiB .. 1 MiB and batch in 1 .. 4096,
 with sequential (0..n-1) or seeded-random page ids, it times a backup (D2H),
 a restore (H2D) and both at once on two streams (disjoint pages and slots), in
-ZERO_COPY and STAGED mode, with CUDA events on the launching stream (median of
+ZERO_COPY, STAGED and COPY_ENGINE mode, with CUDA events on the launching stream (median of
 ``--reps`` after warm-up; every rep uses another page set so small batches do
 not run from L2).  Writes one JSON record per point and prints a table of the
-zero-copy GB/s and which mode wins.
+zero-copy GB/s and which mode wins at each point.
 """
 from __future__ import annotations
 
@@ -22,6 +22,9 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+
+
+MODES = (("zero_copy", 0), ("staged", 1), ("copy_engine", 2))   # kv_mode values
 
 
 def main(argv=None):
@@ -37,10 +40,16 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=2)
     p.add_argument("--quick", action="store_true", help="every other page size and batch")
     p.add_argument("--pages", type=int, default=8192)
+    p.add_argument("--page-bytes", type=int, nargs="*", help="only these page sizes")
+    p.add_argument("--batches", type=int, nargs="*", help="only these batch sizes")
     a = p.parse_args(argv)
 
     sizes = wl.SWEEP_PAGE_BYTES[::2] if a.quick else wl.SWEEP_PAGE_BYTES
     batches = wl.SWEEP_BATCHES[::2] if a.quick else wl.SWEEP_BATCHES
+    if a.page_bytes:
+        sizes = [x for x in sizes if x in a.page_bytes]
+    if a.batches:
+        batches = [x for x in batches if x in a.batches]
     P = a.pages
     max_pb, max_n = max(sizes), max(batches)
     dev_bytes = P * max_pb
@@ -72,8 +81,7 @@ def main(argv=None):
                     sets.append((src, dst))
                 slots_b = np.arange(n, dtype=np.int32)
                 slots_r = np.arange(n, 2 * n, dtype=np.int32)
-                for mode_name, mode in (("zero_copy", kvb.KV_MODE_ZERO_COPY),
-                                        ("staged", kvb.KV_MODE_STAGED)):
+                for mode_name, mode in MODES:
                     kvb.kv_config_set(mode, 0, 0)
                     for direction in ("d2h", "h2d", "both"):
                         ts = []
@@ -111,18 +119,21 @@ def main(argv=None):
     with open(a.out, "w") as f:
         json.dump({"points": records}, f)
 
-    # summary: zero-copy GB/s for random ids, and the winning mode per point
-    for direction in ("d2h", "h2d", "both"):
-        print(f"\n{direction}: zero-copy GB/s, random ids (winner: z = zero-copy, s = staged)")
-        print("page \\ batch " + " ".join(f"{n:>7d}" for n in batches))
-        for pb in sizes:
-            cells = []
-            for n in batches:
-                pt = {rr["mode"]: rr for rr in records if rr["page_bytes"] == pb and
-                      rr["batch"] == n and rr["ids"] == "random" and rr["direction"] == direction}
-                z, s = pt["zero_copy"]["gbs"], pt["staged"]["gbs"]
-                cells.append(f"{z:6.1f}{'z' if z >= s else 's'}")
-            print(f"{pb // 1024:>8d} KiB " + " ".join(cells))
+    # summary: zero-copy GB/s and the winning mode per point
+    # (winner: z = zero-copy, s = staged, c = copy engine)
+    for ids in ("random", "seq"):
+        for direction in ("d2h", "h2d", "both"):
+            print(f"\n{direction}, {ids} ids: zero-copy GB/s and the winner "
+                  "(z zero-copy, s staged, c copy engine)")
+            print("page \\ batch " + " ".join(f"{n:>7d}" for n in batches))
+            for pb in sizes:
+                cells = []
+                for n in batches:
+                    pt = {rr["mode"]: rr["gbs"] for rr in records if rr["page_bytes"] == pb and
+                          rr["batch"] == n and rr["ids"] == ids and rr["direction"] == direction}
+                    win = max(pt, key=pt.get)[0]
+                    cells.append(f"{pt['zero_copy']:6.1f}{win}")
+                print(f"{pb // 1024:>8d} KiB " + " ".join(cells))
 
 
 if __name__ == "__main__":

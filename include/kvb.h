@@ -126,8 +126,16 @@ typedef struct {
 /* Transfer modes.  ZERO_COPY: one kernel moves every byte between HBM and the
  * mapped pinned host tier over the host link.  STAGED: a kernel gathers /
  * scatters between the pool and a device staging buffer in host layout, and
- * the copy engine moves the staging buffer to / from the host tier. */
-typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1 } kv_mode;
+ * the copy engine moves the staging buffer to / from the host tier.
+ * COPY_ENGINE: no kernel moves data; every contiguous run goes straight
+ * between the pool and the pinned host tier as cudaMemcpyAsync /
+ * cudaMemcpy2DAsync copies (one pitched copy per page when the head orders
+ * agree, merged across pages whose ids and slots both step by one; a head-order
+ * change costs min(H, T) pitched copies per page, layer and component, so it
+ * is slow to issue).  The fence completes through a marker kernel after the
+ * copies.  kv_restore_layers and ready-gated backups / restores run zero-copy
+ * in every mode. */
+typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 2 } kv_mode;
 
 /* kv_config.flags */
 #define KV_CFG_NO_BULK 1u   /* HBM-only moves use the register kernel, not bulk copies */

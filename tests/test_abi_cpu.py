@@ -120,7 +120,9 @@ def test_config_roundtrip_and_checks():
         kvb.kv_config_set(kvb.KV_MODE_STAGED, 64, 64 << 20)
         c = kvb.kv_config_get()
         assert (c.mode, c.max_ctas, c.staging_bytes) == (1, 64, 64 << 20)
-        for bad in [dict(mode=5), dict(max_ctas=1 << 20), dict(staging_bytes=1000)]:
+        kvb.kv_config_set(kvb.KV_MODE_COPY_ENGINE)
+        assert kvb.kv_config_get().mode == 2
+        for bad in [dict(mode=3), dict(mode=5), dict(max_ctas=1 << 20), dict(staging_bytes=1000)]:
             with pytest.raises(kvb.KvError) as e:
                 kvb.kv_config_set(**bad)
             assert e.value.status == kvb.KV_ERR_INVALID_ARG

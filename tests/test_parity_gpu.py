@@ -22,13 +22,14 @@ from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
 MODES = [(kvb.KV_MODE_ZERO_COPY, 0, 0),
          (kvb.KV_MODE_ZERO_COPY, kvb.KV_CFG_NO_PDL, 256),
          (kvb.KV_MODE_STAGED, 0, 0),
-         (kvb.KV_MODE_STAGED, kvb.KV_CFG_NO_BULK, 0)]
+         (kvb.KV_MODE_STAGED, kvb.KV_CFG_NO_BULK, 0),
+         (kvb.KV_MODE_COPY_ENGINE, 0, 0)]
 LAYOUTS = [(o, d, h) for o in (wl.LAYER_FIRST, wl.PAGE_FIRST) for d in (wl.NHD, wl.HND)
            for h in (wl.NHD, wl.HND)]
 
 
 @pytest.fixture(params=MODES, ids=["zero_copy", "zero_copy_256_nopdl", "staged",
-                                   "staged_nobulk"])
+                                   "staged_nobulk", "copy_engine"])
 def mode(request):
     old = kvb.kv_config_get()
     m, flags, threads = request.param

@@ -48,7 +48,8 @@ class SplitRig:
 
 
 @pytest.mark.parametrize("heads", [(wl.NHD, wl.NHD), (wl.HND, wl.NHD)], ids=["NHD", "HND-to-NHD"])
-@pytest.mark.parametrize("mode", [kvb.KV_MODE_ZERO_COPY, kvb.KV_MODE_STAGED], ids=["zc", "staged"])
+@pytest.mark.parametrize("mode", [kvb.KV_MODE_ZERO_COPY, kvb.KV_MODE_STAGED,
+                                  kvb.KV_MODE_COPY_ENGINE], ids=["zc", "staged", "copy_engine"])
 def test_split_pool_backup_restore(heads, mode):
     g = wl.LLAMA8B.geom.with_(P=40, L=6, dev_heads=heads[0], host_heads=heads[1])
     og = oracle_geom(g)
