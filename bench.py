@@ -652,6 +652,32 @@ def run_ours(args):
             "exposed_beyond_last_chunk_ms": round(t_p - t_c - t_last, 3)}
         del A, Bm, Cm
 
+    # ---- Llama-8B: the hop below the host tier.  The step's 512 backed-up host
+    # slots (1 GiB) are put into 512 records of a memfd and got back, on the
+    # host cores (host memory bandwidth bound; no GPU work).
+    l3 = None
+    if w is wl.LLAMA8B and hasattr(os, "memfd_create"):
+        fd = os.memfd_create("kvb_bench_l3")
+        threads = min(16, len(os.sched_getaffinity(0)))
+        store = kvb.kv_l3_open(fd, 0, g.page_bytes, w.n, threads)
+        ids = idsets[0]
+        recs = np.arange(w.n, dtype=np.int32)
+        kvb.kv_l3_put(store, host.data_ptr(), w.host_slots, ids.backup_slots, recs)  # grows it
+        tp, tg = [], []
+        for _ in range(5):
+            t0 = time.perf_counter()
+            kvb.kv_l3_put(store, host.data_ptr(), w.host_slots, ids.backup_slots, recs)
+            t1 = time.perf_counter()
+            kvb.kv_l3_get(store, host.data_ptr(), w.host_slots, recs, ids.backup_slots)
+            tp.append(t1 - t0)
+            tg.append(time.perf_counter() - t1)
+        l3 = {"store": f"memfd, {w.n} records of {g.page_bytes} bytes, host clock",
+              "threads": threads,
+              "put_gbs": round(w.n * g.page_bytes / statistics.median(tp) / GB, 2),
+              "get_gbs": round(w.n * g.page_bytes / statistics.median(tg) / GB, 2)}
+        kvb.kv_l3_close(store)
+        os.close(fd)
+
     # ---- small-op latency: the tiny workload (8 pages of 16 KiB) through the C ABI
     latency = None
     if w is wl.LLAMA8B:
@@ -760,6 +786,7 @@ def run_ours(args):
         "layerwise_progressive": progressive,
         "overlap_with_compute": overlap,
         "write_through": write_through,
+        "l3_hop": l3,
         "clocks": clk.summary(),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

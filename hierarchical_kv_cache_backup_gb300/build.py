@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkvb.so")
 
-SOURCES = ["kvb_api.cpp", "kvb_kernels.cu", "kvb_noalloc.cu", "kvb_ring.cpp"]
+SOURCES = ["kvb_api.cpp", "kvb_kernels.cu", "kvb_noalloc.cu", "kvb_ring.cpp", "kvb_l3.cpp"]
 HEADERS = [os.path.join(CSRC, "kvb_internal.h"), os.path.join(INCLUDE, "kvb.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

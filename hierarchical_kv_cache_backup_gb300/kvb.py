@@ -32,6 +32,7 @@ KV_ERR_CUDA = 8
 KV_ERR_NO_MEMORY = 9
 KV_ERR_CLOSED = 10
 KV_ERR_ABORTED = 11
+KV_ERR_IO = 12
 STATUS_NAMES = {v: k for k, v in dict(globals()).items() if k.startswith("KV_OK") or k.startswith("KV_ERR_")}
 
 KV_LAYER_FIRST, KV_PAGE_FIRST = 0, 1
@@ -49,7 +50,8 @@ EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_p
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
            "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
-           "kv_ring_pop", "kv_ring_complete", "kv_fault_inject")
+           "kv_ring_pop", "kv_ring_complete", "kv_fault_inject", "kv_l3_open", "kv_l3_close",
+           "kv_l3_put", "kv_l3_get")
 
 
 class KvError(RuntimeError):
@@ -134,6 +136,10 @@ def _load():
         "kv_ring_pop": (st, [vp, u64, P(kv_ring_op), P(u64)]),
         "kv_ring_complete": (st, [vp, u64, ctypes.c_int]),
         "kv_fault_inject": (st, [ctypes.c_char_p, u32]),
+        "kv_l3_open": (st, [ctypes.c_int, u64, u64, u64, u32, P(vp)]),
+        "kv_l3_close": (st, [vp]),
+        "kv_l3_put": (st, [vp, vp, u64, vp, vp, u32]),
+        "kv_l3_get": (st, [vp, vp, u64, vp, vp, u32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -444,6 +450,38 @@ def kv_ring_pop(ring: int, timeout_ns: int = 1_000_000_000):
 
 def kv_ring_complete(ring: int, ticket: int, status: int = KV_OK) -> None:
     _check(_lib.kv_ring_complete(ring, ticket, status))
+
+
+# ------------------------------------------------------- L3 record store
+
+def kv_l3_open(fd: int, base_offset: int, record_bytes: int, num_records: int,
+               threads: int = 0) -> int:
+    out = ctypes.c_void_p()
+    _check(_lib.kv_l3_open(fd, base_offset, record_bytes, num_records, threads,
+                           ctypes.byref(out)))
+    return out.value
+
+
+def kv_l3_close(store: int) -> None:
+    _check(_lib.kv_l3_close(store))
+
+
+def kv_l3_put(store: int, host: int, host_slots: int, slots, records) -> None:
+    """Host slots -> records; ``host`` is the address of the slot array."""
+    a, pa = _ids(slots)
+    b, pb = _ids(records)
+    if a.size != b.size:
+        raise ValueError("slots and records differ in length")
+    _check(_lib.kv_l3_put(store, host, host_slots, pa, pb, a.size))
+
+
+def kv_l3_get(store: int, host: int, host_slots: int, records, slots) -> None:
+    """Records -> host slots."""
+    a, pa = _ids(records)
+    b, pb = _ids(slots)
+    if a.size != b.size:
+        raise ValueError("records and slots differ in length")
+    _check(_lib.kv_l3_get(store, host, host_slots, pa, pb, a.size))
 
 
 def kv_fault_inject(point: str, count: int = 1) -> None:

@@ -80,7 +80,8 @@ typedef enum {
     KV_ERR_CUDA = 8,          /* a CUDA call failed; see kv_last_error()     */
     KV_ERR_NO_MEMORY = 9,     /* library could not allocate its resources    */
     KV_ERR_CLOSED = 10,       /* handle already closed                       */
-    KV_ERR_ABORTED = 11       /* op gave up: its ready fence never arrived   */
+    KV_ERR_ABORTED = 11,      /* op gave up: its ready fence never arrived   */
+    KV_ERR_IO = 12            /* a file read / write failed (L3 record store) */
 } kv_status;
 
 typedef enum { KV_LAYER_FIRST = 0, KV_PAGE_FIRST = 1 } kv_order;
@@ -415,6 +416,53 @@ KVB_API kv_status kv_ring_pop(kv_ring ring, uint64_t timeout_ns, kv_ring_op *op,
                               uint64_t *ticket);
 /* ... and completes a ticket from the CPU with the given status. */
 KVB_API kv_status kv_ring_complete(kv_ring ring, uint64_t ticket, kv_status op_status);
+
+/* ------------------------------------------------ L3 record store (files) */
+
+/* The tier below the host tier ([RFC] §Summary: the daemon's host tier with
+ * external L3 storage below it; §Relationship to existing SGLang work: the
+ * standalone L3 StorageServer keeps its bulk bytes in shared memfd host
+ * memory).  A store is `num_records` fixed-size records of a file descriptor:
+ * record r is bytes [base_offset + r * record_bytes, + record_bytes).  Puts and
+ * gets move whole host-tier pages: slot s of a host tier is bytes
+ * [s * record_bytes, + record_bytes) of `host` (the page-contiguous host tier
+ * registered with kv_host_register, whose page bytes equal record_bytes, or
+ * any host buffer of that shape).  The bytes are never interpreted. */
+typedef struct kv_l3_s *kv_l3;
+
+/* Opens a store over `fd` (a regular file, a memfd or a block device; the
+ * caller keeps ownership and closes it after kv_l3_close).  `threads` worker
+ * threads move the bytes (0 = 8, at most 64).  The file is not resized: a put
+ * past its end grows it, a get past its end fails with KV_ERR_IO.  If the
+ * caller opened fd with O_DIRECT, buffers, offsets and record_bytes must meet
+ * its alignment or calls fail with KV_ERR_IO.
+ * Errors: INVALID_ARG (fd not open / not a file or block device, zero sizes,
+ * threads > 64), OUT_OF_RANGE (num_records > 2^31 or offsets overflow),
+ * NO_MEMORY. */
+KVB_API kv_status kv_l3_open(int fd, uint64_t base_offset, uint64_t record_bytes,
+                             uint64_t num_records, uint32_t threads, kv_l3 *out);
+/* Stops the workers (a call in flight on another thread finishes first). */
+KVB_API kv_status kv_l3_close(kv_l3 store);
+
+/* PUT: record records[i] <- host slot slots[i], for i < n.  Synchronous:
+ * returns once every byte is written to the descriptor (no fsync).  Runs of
+ * consecutive records go out as one pwritev each, spread over the workers.
+ * Checks before any write: ids in range (slots < host_slots, records <
+ * num_records), no record named twice.  The host slots must not be written
+ * meanwhile (wait for the backup's fence first).
+ * Errors: CLOSED, INVALID_ARG, OUT_OF_RANGE, DUPLICATE (nothing written);
+ * IO (a write failed: the named records are then undefined). */
+KVB_API kv_status kv_l3_put(kv_l3 store, const void *host, uint64_t host_slots,
+                            const int32_t *slots, const int32_t *records, uint32_t n);
+/* GET: host slot slots[i] <- record records[i], for i < n.  Synchronous; runs
+ * of consecutive records come in as one preadv each.  Checks as for PUT, with
+ * no slot named twice.  Restore from the slots only after this returns (or
+ * gate the restore with kv_restore_when_ready on a word set afterwards).
+ * Errors: CLOSED, INVALID_ARG, OUT_OF_RANGE, DUPLICATE (nothing read);
+ * IO (a read failed or a record lies past the end of the file: the named
+ * slots are then undefined). */
+KVB_API kv_status kv_l3_get(kv_l3 store, void *host, uint64_t host_slots,
+                            const int32_t *records, const int32_t *slots, uint32_t n);
 
 /* --------------------------------------------------------------- fences */
 

@@ -67,6 +67,10 @@ def _bind(lib):
     lib.kvo_backup_mt.restype = ctypes.c_int
     lib.kvo_restore_mt.argtypes = [gp, vp, i64, vp, vp, vp, i64, i32, ctypes.c_int]
     lib.kvo_restore_mt.restype = ctypes.c_int
+    lib.kvo_l3_put.argtypes = [vp, i64, vp, vp, i64, vp, i64]
+    lib.kvo_l3_put.restype = None
+    lib.kvo_l3_get.argtypes = [vp, i64, i64, vp, vp, i64, vp]
+    lib.kvo_l3_get.restype = None
 
 
 def load(path: str | None = None):
@@ -133,3 +137,25 @@ def restore(g: Geom, pool: np.ndarray, host: np.ndarray, slots, dst, layer: int 
         return 1
     return lib.kvo_restore_mt(ctypes.byref(g), _ptr(pool), pool_offset, _ptr(host),
                               _ptr(slots), _ptr(dst), slots.size, layer, threads)
+
+
+def l3_put(host: np.ndarray, record_bytes: int, slots, records, file_image: np.ndarray,
+           base: int = 0, lib=None) -> None:
+    """file_image[base + records[i]*rb : +rb] <- host[slots[i]*rb : +rb] in place."""
+    lib = lib or load()
+    slots, records = _ids(slots), _ids(records)
+    assert slots.shape == records.shape and host.dtype == np.uint8
+    assert file_image.dtype == np.uint8
+    lib.kvo_l3_put(_ptr(host), record_bytes, _ptr(slots), _ptr(records), slots.size,
+                   _ptr(file_image), base)
+
+
+def l3_get(file_image: np.ndarray, record_bytes: int, records, slots, host: np.ndarray,
+           base: int = 0, lib=None) -> None:
+    """host[slots[i]*rb : +rb] <- file_image[base + records[i]*rb : +rb] in place."""
+    lib = lib or load()
+    records, slots = _ids(records), _ids(slots)
+    assert slots.shape == records.shape and host.dtype == np.uint8
+    assert file_image.dtype == np.uint8
+    lib.kvo_l3_get(_ptr(file_image), base, record_bytes, _ptr(records), _ptr(slots),
+                   slots.size, _ptr(host))

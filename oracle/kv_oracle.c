@@ -226,3 +226,30 @@ int kvo_restore_mt(const kvo_geom *g, uint8_t *pool_base, int64_t pool_offset,
     return run_threads(g, pool_base + pool_offset, (uint8_t *)host, slot, dst,
                        n, layer, 0, threads);
 }
+
+/* ------------------------------------------------------ L3 record store
+ * The tier below the host tier ("[Feature] [RFC] [HiCache] Out-of-process
+ * HiCache data plane with device-memory IPC", §Summary: host tier and L3
+ * storage under the daemon; §Relationship to existing SGLang work: the L3
+ * StorageServer's bulk bytes live in shared memfd memory).  Reading taken: a
+ * store is fixed-size records of a file, record r at byte base + r * rb, one
+ * host-tier page per record; host slot s is bytes [s * rb, (s + 1) * rb) of the
+ * host tier.  The file is modelled by its byte image.
+ *   put: for all i, b < rb:  file[base + records[i] * rb + b] = host[slots[i] * rb + b]
+ *   get: for all i, b < rb:  host[slots[i] * rb + b] = file[base + records[i] * rb + b]
+ * Every other byte is left unchanged. */
+void kvo_l3_put(const uint8_t *host, int64_t rb, const int32_t *slots,
+                const int32_t *records, int64_t n, uint8_t *file, int64_t base)
+{
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t b = 0; b < rb; ++b)
+            file[base + (int64_t)records[i] * rb + b] = host[(int64_t)slots[i] * rb + b];
+}
+
+void kvo_l3_get(const uint8_t *file, int64_t base, int64_t rb, const int32_t *records,
+                const int32_t *slots, int64_t n, uint8_t *host)
+{
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t b = 0; b < rb; ++b)
+            host[(int64_t)slots[i] * rb + b] = file[base + (int64_t)records[i] * rb + b];
+}

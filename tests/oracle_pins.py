@@ -23,6 +23,11 @@ What pins what:
     addressing, layer-by-layer restore equals whole-prefix restore, every device
     layout of the same logical KV gives the same host tier, threaded = serial.
   * ``pin_page_bytes`` -- bytes per page of the five workloads, written out by hand.
+  * ``pin_l3_records`` -- the L3 record store: numpy fancy indexing over a
+    [records, record_bytes] view of the file image restates put and get; a tiny
+    store is checked byte by byte against tags naming (slot, byte); put then get
+    into other slots returns the original pages; untouched records, slots and
+    the bytes around the store are unchanged.
 """
 from __future__ import annotations
 
@@ -337,5 +342,67 @@ def pin_page_bytes(lib):
         assert oracle.page_bytes(g, lib=lib) == d["page_bytes"], name
 
 
+def pin_l3_records(lib, seed=23):
+    r = np.random.default_rng(seed)
+    # (1) restated with numpy: the store is file[base : base + R*rb] viewed [R, rb]
+    for rb, S, R, base, n in [(16, 5, 7, 0, 3), (48, 9, 12, 32, 9), (256, 4, 40, 4096 + 16, 4),
+                              (64, 30, 30, 8, 30)]:
+        host = r.integers(0, 256, S * rb, dtype=np.uint8)
+        image = r.integers(0, 256, base + R * rb + 64, dtype=np.uint8)
+        slots = r.integers(0, S, n).astype(np.int32)          # a put may read a slot twice
+        records = r.permutation(R)[:n].astype(np.int32)
+        want = image.copy()
+        want[base:base + R * rb].reshape(R, rb)[records] = host.reshape(S, rb)[slots]
+        got = image.copy()
+        oracle.l3_put(host, rb, slots, records, got, base, lib=lib)
+        assert np.array_equal(got, want), ("numpy put", rb, S, R, base, n)
+        m = min(n, S)
+        gslots = r.permutation(S)[:m].astype(np.int32)
+        grecs = r.integers(0, R, m).astype(np.int32)          # a get may read a record twice
+        wanth = host.copy()
+        wanth.reshape(S, rb)[gslots] = image[base:base + R * rb].reshape(R, rb)[grecs]
+        goth = host.copy()
+        oracle.l3_get(image, rb, grecs, gslots, goth, base, lib=lib)
+        assert np.array_equal(goth, wanth), ("numpy get", rb, S, R, base, m)
+    # (2) brute force on a tiny store: every byte checked against its tag
+    rb, S, R, base = 16, 3, 4, 5
+    host = np.array([(s * 16 + b) & 0xFF for s in range(S) for b in range(rb)], dtype=np.uint8)
+    for slots in itertools.permutations(range(S), 2):
+        for records in itertools.permutations(range(R), 2):
+            image = np.full(base + R * rb + 3, 0xEE, dtype=np.uint8)
+            oracle.l3_put(host, rb, list(slots), list(records), image, base, lib=lib)
+            for pos in range(image.size):
+                rec, b = divmod(pos - base, rb)
+                if pos >= base and rec < R and rec in records:
+                    s = slots[records.index(rec)]
+                    assert image[pos] == s * 16 + b, ("tag put", slots, records, pos)
+                else:
+                    assert image[pos] == 0xEE, ("untouched put", slots, records, pos)
+            back = np.full(S * rb, 0xDD, dtype=np.uint8)
+            oracle.l3_get(image, rb, list(records), list(slots[::-1]), back, base, lib=lib)
+            for pos in range(back.size):
+                s, b = divmod(pos, rb)
+                if s in slots[::-1]:
+                    rec = records[list(slots[::-1]).index(s)]
+                    src = slots[records.index(rec)]
+                    assert back[pos] == src * 16 + b, ("tag get", slots, records, pos)
+                else:
+                    assert back[pos] == 0xDD, ("untouched get", slots, records, pos)
+    # (3) put then get into other slots returns the pages
+    rb, S, R, n = 128, 10, 25, 5
+    host = r.integers(0, 256, S * rb, dtype=np.uint8)
+    image = np.zeros(R * rb, dtype=np.uint8)
+    src = r.permutation(S)[:n].astype(np.int32)
+    recs = r.permutation(R)[:n].astype(np.int32)
+    oracle.l3_put(host, rb, src, recs, image, lib=lib)
+    back = host.copy()
+    dst = np.array([s for s in range(S) if s not in src][:n], dtype=np.int32)
+    oracle.l3_get(image, rb, recs, dst, back, lib=lib)
+    hv, bv = host.reshape(S, rb), back.reshape(S, rb)
+    assert np.array_equal(bv[dst], hv[src]), "round trip through records"
+    keep = np.setdiff1d(np.arange(S), dst)
+    assert np.array_equal(bv[keep], hv[keep]), "slots not named stay unchanged"
+
+
 ALL_PINS = [pin_offsets_row_major, pin_backup_tags, pin_restore_tags, pin_trtllm_view,
-            pin_numpy_restatement, pin_invariants, pin_page_bytes]
+            pin_numpy_restatement, pin_invariants, pin_page_bytes, pin_l3_records]

@@ -44,6 +44,12 @@ MUTATIONS = {
     "offset_ignored": ("backup_range(g, pool_base + pool_offset, host", "backup_range(g, pool_base, host"),
     "thread_split_drops_items": ("job[k].i1 = n * (k + 1) / threads;", "job[k].i1 = n * (k + 1) / threads - (k == 0);"),
     "page_bytes_drops_C": ("return g->L * g->C * g->T * g->H * g->B;", "return g->L * g->T * g->H * g->B;"),
+    "l3_put_indexes_file_by_slot": ("file[base + (int64_t)records[i] * rb + b] = host[(int64_t)slots[i] * rb + b];",
+                                    "file[base + (int64_t)slots[i] * rb + b] = host[(int64_t)slots[i] * rb + b];"),
+    "l3_get_drops_base": ("host[(int64_t)slots[i] * rb + b] = file[base + (int64_t)records[i] * rb + b];",
+                          "host[(int64_t)slots[i] * rb + b] = file[(int64_t)records[i] * rb + b];"),
+    "l3_put_short_record": ("for (int64_t b = 0; b < rb; ++b)\n            file[",
+                            "for (int64_t b = 0; b < rb - 1; ++b)\n            file["),
 }
 
 
