@@ -728,7 +728,9 @@ def run_ours(args):
     achieved = dom_bytes / (dom_ms / 1000) / GB
     roofline = {"bound": "host_link", "kernel": kern, "achieved": round(achieved, 2),
                 "peak": round(dom_peak, 2), "unit": "GB/s", "frac": round(achieved / dom_peak, 4),
-                "traffic": recorded_traffic("backup_dram_bytes_per_launch"),
+                # captured on the Llama-8B backup launch only; other workloads: none taken
+                "traffic": recorded_traffic("backup_dram_bytes_per_launch")
+                if w is wl.LLAMA8B else None,
                 "algorithmic_bytes_per_launch": dom_bytes,
                 "peak_source": f"pinned cudaMemcpyAsync {dom_dir} of 2 GiB measured in this run, "
                                "best of 10 (host link peak; not in MEASURED_PEAKS.json)"}
