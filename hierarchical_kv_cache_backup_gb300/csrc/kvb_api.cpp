@@ -625,19 +625,26 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
 
 // CTAs of a move kernel.  Host-link moves saturate the link with few threads
 // (measured on GB300: 16 CTAs of 256 threads reach the D2H peak, 32 the H2D
-// peak, and 64 + 64 give the best D2H + H2D mix, while more CTAs per direction
-// lose bidirectional throughput).  By default they run the same 16,384
-// threads as 16 CTAs of 1024, one per SM: whole SMs stay free for compute
-// kernels beside them, where 64 small CTAs would sit on 64 SMs and keep large
-// compute CTAs off all of them.  HBM-only moves use 4 CTAs of 256 per SM.
+// peak).  A backup and a restore running at once need more loads and stores
+// in flight across more SMs: 64 CTAs of 256 per direction reach 99.5% of the
+// bidirectional memcpy peak on every box measured, where the same 16,384
+// threads as 16 CTAs of 1024 gave 72-99.7% from box to box and run to run,
+// and 32 / 48 / 128 CTAs of 256 gave 85-93%.  With programmatic dependent
+// launch the narrow CTAs cost compute beside them no more than wide ones
+// (one-layer restores pipelined with a GEMM per layer: 3.75 ms either way;
+// write-through backups beside a chunked forward: within 1%), so backups and
+// restores default to 64 x 256.  HBM-only moves use 4 CTAs of 256 per SM.
 constexpr int kLinkCtas = 64;       // CTAs of kMoveThreads
-constexpr int kLinkWideCtas = 16;   // CTAs of kWideThreads
+constexpr int kLinkWideCtas = 16;   // CTAs of kWideThreads (cta_threads = 1024)
 // Progressive layer restores exist to run beside each layer's forward: 8 wide
 // CTAs (8 SMs) still reach 98% of the H2D peak and cut the time of a 61-layer
 // restore pipelined with a per-layer GEMM from 4.26 ms (16 CTAs) to 3.54 ms.
 constexpr int kOverlapWideCtas = 8;
 
-int link_threads() { return g_cfg.cta_threads ? (int)g_cfg.cta_threads : kWideThreads; }
+int link_threads() { return g_cfg.cta_threads ? (int)g_cfg.cta_threads : kMoveThreads; }
+int progressive_threads() {
+    return g_cfg.cta_threads ? (int)g_cfg.cta_threads : kWideThreads;
+}
 
 // Turns a plan into a progressive multi-layer plan for n items (one launch).
 kv_status plan_layer_major(Plan &p, uint32_t n, const DevState &ds, uint64_t seq0) {
@@ -1628,7 +1635,7 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
         Plan p;
         st = plan(pool->g, hs, ps, num_layers, first_layer, ds.err_dev, false, &p);
         if (st == KV_OK) st = plan_layer_major(p, n, ds, seq0);
-        p.threads = link_threads();
+        p.threads = progressive_threads();
         const int ctas = g_cfg.max_ctas ? (int)g_cfg.max_ctas
                          : p.threads == kWideThreads ? std::min(kOverlapWideCtas, ds.sms)
                                                      : default_ctas(ds, true);

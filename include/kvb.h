@@ -144,17 +144,19 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
                                no programmatic dependent launch overlapping a kernel's
                                launch with the previous kernel's end */
 
-/* Defaults: host-link moves (zero-copy backup / restore) run 16 CTAs of 1024
- * threads, one per SM, so the link saturates from 16 of the GPU's SMs and the
- * rest stay free for compute; kv_restore_layers, made to run beside compute,
- * runs 8; HBM-only moves run 4 CTAs of 256 threads per SM (bulk-copy kernel:
- * 3 per SM). */
+/* Defaults: host-link moves (zero-copy backup / restore) run 64 CTAs of 256
+ * threads (a backup and a restore at once then reach the bidirectional link
+ * peak); kv_restore_layers, made to run beside compute, runs 8 CTAs of 1024
+ * threads (8 whole SMs); HBM-only moves run 4 CTAs of 256 threads per SM
+ * (bulk-copy kernel: 3 per SM).  cta_threads = 1024 gives backups and
+ * restores 16 CTAs of 1024 (whole SMs, fewer of them), 256 gives progressive
+ * restores 64 CTAs of 256. */
 typedef struct {
     uint32_t mode;           /* kv_mode                                         */
     uint32_t max_ctas;       /* CTA cap of the transfer kernel; 0 = default     */
     uint64_t staging_bytes;  /* STAGED: device staging bytes; 0 = default       */
     uint32_t flags;          /* KV_CFG_* bits                                   */
-    uint32_t cta_threads;    /* host-link CTA size: 0 = default (1024), 256, 1024 */
+    uint32_t cta_threads;    /* host-link CTA size: 0 = default, 256, 1024      */
 } kv_config;
 
 /* ------------------------------------------------------------------ pools */
