@@ -200,6 +200,13 @@ struct DevState {
     uint64_t staging_bytes = 0;
     cudaEvent_t staging_free[2] = {nullptr, nullptr};
     bool staging_used[2] = {false, false};
+    // STAGED ops of several chunks: each half is two ping-pong buffers; the HBM
+    // kernels run on side[half] (a backup's and a restore's apart, so the two
+    // can run at once) while the copy engine works on the caller's stream
+    cudaStream_t side[2] = {nullptr, nullptr};
+    cudaEvent_t op_start = nullptr;          // caller's stream at the op's start
+    cudaEvent_t moved[2][2] = {};            // [half][buffer]: kernel done with it
+    cudaEvent_t copied[2][2] = {};           // [half][buffer]: copy engine done with it
 };
 
 std::mutex g_mu;
@@ -746,11 +753,21 @@ kv_status ensure_staging(DevState &s) {
                                       (unsigned long long)want, cudaGetErrorString(e));
     s.staging = (char *)p;
     s.staging_bytes = want;
-    for (int h = 0; h < 2; ++h)
-        if (s.staging_free[h] == nullptr) {
-            e = cudaEventCreateWithFlags(&s.staging_free[h], cudaEventDisableTiming);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(staging)");
+    auto make_event = [](cudaEvent_t *ev) {
+        return *ev != nullptr ? cudaSuccess : cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    };
+    for (int h = 0; h < 2; ++h) {
+        e = make_event(&s.staging_free[h]);
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = make_event(&s.moved[h][b]);
+            if (e == cudaSuccess) e = make_event(&s.copied[h][b]);
         }
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(staging)");
+    }
+    if (e == cudaSuccess) e = make_event(&s.op_start);
+    for (int h = 0; h < 2 && e == cudaSuccess; ++h)
+        if (s.side[h] == nullptr) e = cudaStreamCreateWithFlags(&s.side[h], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e, "staging stream / events");
     return KV_OK;
 }
 
@@ -942,29 +959,51 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     } else if (n > 0) {
         st = ensure_staging(ds);
         if (st != KV_OK) return st;
+        // STAGED: the op is cut into chunks (layer groups x item slices) that fit
+        // one of the half's two ping-pong buffers.  Backup: the gather of chunk k
+        // (HBM kernel, side stream) runs while chunk k-1 crosses the host link
+        // (copy engine, caller's stream); restore: the copy of chunk k runs while
+        // chunk k-1 is scattered.  Events order each buffer's reuse; the op ends
+        // on the caller's stream (its fence and the half's staging_free event).
         const int half = backup ? 0 : 1;
-        char *stg = ds.staging + (uint64_t)half * (ds.staging_bytes / 2);
         const uint64_t half_bytes = ds.staging_bytes / 2;
+        const uint64_t buf_bytes = (half_bytes / 2) & ~(uint64_t)255;
+        char *const bufs[2] = {ds.staging + (uint64_t)half * half_bytes,
+                               ds.staging + (uint64_t)half * half_bytes + buf_bytes};
         const uint64_t layer_bytes = pool->g.C * pool->g.cb;        // one layer of one page
         // layers per group: the whole range if one page fits, else as many as fit
-        const uint32_t gl = (uint32_t)std::min<uint64_t>(nl, half_bytes / layer_bytes);
+        const uint32_t gl = (uint32_t)std::min<uint64_t>(nl, buf_bytes / layer_bytes);
         if (gl == 0)
-            return fail(KV_ERR_NO_MEMORY, "staging half of %llu bytes holds no layer of %llu bytes",
-                        (unsigned long long)half_bytes, (unsigned long long)layer_bytes);
+            return fail(KV_ERR_NO_MEMORY, "staging buffer of %llu bytes holds no layer of %llu "
+                        "bytes", (unsigned long long)buf_bytes, (unsigned long long)layer_bytes);
         const uint64_t lb = (uint64_t)gl * layer_bytes;              // staged bytes per item
-        const uint64_t fit = half_bytes / lb;                         // items per staging fill
-        if (ds.staging_used[half]) {
-            cudaError_t e = cudaStreamWaitEvent(stream, ds.staging_free[half], 0);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent(staging)");
+        const uint32_t fit = (uint32_t)std::min<uint64_t>(buf_bytes / lb, n);   // items per fill
+        const uint64_t chunks = (uint64_t)((nl + gl - 1) / gl) * ((n + fit - 1) / fit);
+        const bool pipelined = chunks > 1;
+        cudaStream_t ks = pipelined ? ds.side[half] : stream;        // kernels' stream
+        auto ck = [](cudaError_t e, const char *what) {
+            return e == cudaSuccess ? KV_OK : cuda_fail(e, what);
+        };
+        if (ds.staging_used[half])
+            st = ck(cudaStreamWaitEvent(stream, ds.staging_free[half], 0),
+                    "cudaStreamWaitEvent(staging)");
+        if (st == KV_OK && pipelined) {
+            st = ck(cudaEventRecord(ds.op_start, stream), "cudaEventRecord(staging start)");
+            if (st == KV_OK)
+                st = ck(cudaStreamWaitEvent(ks, ds.op_start, 0), "cudaStreamWaitEvent(staging)");
         }
+        if (st != KV_OK) return st;
         const Side ps = pool_side(*pool);
         static thread_local std::vector<int32_t> idx;
+        uint64_t k = 0;
         for (uint32_t la = l0; la < l0 + nl; la += gl) {
             const uint32_t g_n = std::min(gl, l0 + nl - la);          // layers in this group
             const uint64_t host_off = (uint64_t)la * layer_bytes;
             const uint64_t gb = (uint64_t)g_n * layer_bytes;
-            for (uint32_t i0 = 0; i0 < n; i0 += (uint32_t)std::min<uint64_t>(fit, n)) {
-                const uint32_t m = (uint32_t)std::min<uint64_t>(fit, n - i0);
+            for (uint32_t i0 = 0; i0 < n; i0 += fit, ++k) {
+                const uint32_t m = std::min(fit, n - i0);
+                const int bi = (int)(k & 1);
+                char *stg = bufs[bi];
                 const Side ss = staging_side(stg, pool->g, host->heads, g_n, la, m);
                 const int kernel = hbm_kernel(pool->g, ps, ss);
                 Plan p;
@@ -973,20 +1012,46 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                 if (st != KV_OK) return st;
                 const int ctas = default_ctas(ds, false, kernel);
                 if (backup) {
-                    st = run_moves(p, a + i0, nullptr, m, ctas, stream, true);
+                    if (pipelined && k >= 2)   // chunk k-2's copy has left this buffer
+                        st = ck(cudaStreamWaitEvent(ks, ds.copied[half][bi], 0), "staging wait");
+                    if (st == KV_OK) st = run_moves(p, a + i0, nullptr, m, ctas, ks, true);
+                    if (st == KV_OK && pipelined) {
+                        st = ck(cudaEventRecord(ds.moved[half][bi], ks), "staging record");
+                        if (st == KV_OK)
+                            st = ck(cudaStreamWaitEvent(stream, ds.moved[half][bi], 0),
+                                    "staging wait");
+                    }
                     if (st == KV_OK)
                         st = staged_copies(*host, stg, b + i0, m, gb, host_off, true, stream);
+                    if (st == KV_OK && pipelined)
+                        st = ck(cudaEventRecord(ds.copied[half][bi], stream), "staging record");
                 } else {
-                    st = staged_copies(*host, stg, a + i0, m, gb, host_off, false, stream);
-                    if (st == KV_OK) {
-                        // staging item k -> dst page b[i0 + k]: a = staging index, b = page
-                        idx.resize(m);
-                        for (uint32_t k = 0; k < m; ++k) idx[k] = (int32_t)k;
-                        st = run_moves(p, idx.data(), b + i0, m, ctas, stream, false);
+                    if (pipelined && k >= 2)   // chunk k-2's scatter has read this buffer
+                        st = ck(cudaStreamWaitEvent(stream, ds.moved[half][bi], 0), "staging wait");
+                    if (st == KV_OK)
+                        st = staged_copies(*host, stg, a + i0, m, gb, host_off, false, stream);
+                    if (st == KV_OK && pipelined) {
+                        st = ck(cudaEventRecord(ds.copied[half][bi], stream), "staging record");
+                        if (st == KV_OK)
+                            st = ck(cudaStreamWaitEvent(ks, ds.copied[half][bi], 0),
+                                    "staging wait");
                     }
+                    if (st == KV_OK) {
+                        // staging item j -> dst page b[i0 + j]: a = staging index, b = page
+                        idx.resize(m);
+                        for (uint32_t j = 0; j < m; ++j) idx[j] = (int32_t)j;
+                        st = run_moves(p, idx.data(), b + i0, m, ctas, ks, false);
+                    }
+                    if (st == KV_OK && pipelined)
+                        st = ck(cudaEventRecord(ds.moved[half][bi], ks), "staging record");
                 }
                 if (st != KV_OK) return st;
             }
+        }
+        if (pipelined && !backup) {   // the last scatters end on the caller's stream too
+            for (int bi = 0; bi < 2 && st == KV_OK; ++bi)
+                st = ck(cudaStreamWaitEvent(stream, ds.moved[half][bi], 0), "staging wait");
+            if (st != KV_OK) return st;
         }
         cudaError_t e = cudaEventRecord(ds.staging_free[half], stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
