@@ -119,22 +119,27 @@ def recorded_traffic(key):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """nvidia-smi clock / throttle samples over the timed region.  nvidia-smi is
+    started before the warm-up (its start-up touches the driver) and every line
+    is timestamped; summary() keeps the samples taken between mark() and
+    stop()."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.1
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(int(1000 * self.PERIOD_S))],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -144,9 +149,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def __exit__(self, *a):
+    def mark(self):
+        self.t0 = time.monotonic()
+
+    def stop(self):
+        self.t1 = time.monotonic()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -155,12 +164,20 @@ class ClockSampler:
                 self.proc.kill()
             self.t.join(timeout=5)
 
+    def window_lines(self):
+        t0 = self.t0 if self.t0 is not None else 0.0
+        t1 = (self.t1 if self.t1 is not None else time.monotonic()) + self.PERIOD_S
+        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1]
+        if not inside:   # a window shorter than one period: the first sample after it began
+            inside = [ln for ts, ln in self.lines if ts >= t0][:1]
+        return inside
+
     def summary(self):
         if self.proc is None:
             return {"unavailable": "nvidia-smi not found"}
         sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.window_lines():
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -430,6 +447,7 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    clk = ClockSampler(local).start()   # before the warm-up: its start-up is not timed
     for k in range(args.warmup):
         step(k)
     barrier()
@@ -437,15 +455,16 @@ def run_ours(args):
     # ---- timed region: device clock (CUDA events on the launching stream)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     l0 = kvb.kv_launch_count()
-    with ClockSampler(local) as clk:
-        barrier()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(s_a)
-        for k in range(args.steps):
-            step(k, evs[k])
-        t_end.record(s_a)
-        barrier()
+    barrier()
+    clk.mark()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(s_a)
+    for k in range(args.steps):
+        step(k, evs[k])
+    t_end.record(s_a)
+    barrier()
+    clk.stop()
     launches = kvb.kv_launch_count() - l0
     elapsed = dist_max(t_start.elapsed_time(t_end) / 1000, dist, dev)
     b_ms = [e[0].elapsed_time(e[1]) for e in evs]

@@ -632,15 +632,17 @@ kv_status plan(const Geo &g, const Side &src, const Side &dst, uint32_t nl, uint
 
 // CTAs of a move kernel.  Host-link moves saturate the link with few threads
 // (measured on GB300: 16 CTAs of 256 threads reach the D2H peak, 32 the H2D
-// peak).  A backup and a restore running at once need more loads and stores
-// in flight across more SMs: 64 CTAs of 256 per direction reach 99.5% of the
-// bidirectional memcpy peak on every box measured, where the same 16,384
-// threads as 16 CTAs of 1024 gave 72-99.7% from box to box and run to run,
-// and 32 / 48 / 128 CTAs of 256 gave 85-93%.  With programmatic dependent
-// launch the narrow CTAs cost compute beside them no more than wide ones
-// (one-layer restores pipelined with a GEMM per layer: 3.75 ms either way;
-// write-through backups beside a chunked forward: within 1%), so backups and
-// restores default to 64 x 256.  HBM-only moves use 4 CTAs of 256 per SM.
+// peak; every shape from 8 x 1024 to 64 x 256 reaches both solo peaks).  The
+// shape matters when a backup and a restore run at once, and there the best
+// shape depends on the kernel variant: moves that change head order (the
+// TRT-LLM HND pool) reach 338-341 GB/s, 99-100% of the bidirectional memcpy
+// peak, with 64 CTAs of 256 per direction on every box measured (16 x 1024:
+// 246-338 from box to box), while identity moves reach 322-326 GB/s with 16
+// CTAs of 1024 (64 x 256: 305-310; more warps in flight per direction, e.g.
+// 32 x 1024 or 128 x 256, lose on every layout: 292-301).  Compute beside the
+// moves runs as fast with either shape (one-layer restores pipelined with a
+// GEMM per layer: 3.75 ms; write-through backups: within 1%).  HBM-only moves
+// use 4 CTAs of 256 per SM.
 constexpr int kLinkCtas = 64;       // CTAs of kMoveThreads
 constexpr int kLinkWideCtas = 16;   // CTAs of kWideThreads (cta_threads = 1024)
 // Progressive layer restores exist to run beside each layer's forward: 8 wide
@@ -648,7 +650,10 @@ constexpr int kLinkWideCtas = 16;   // CTAs of kWideThreads (cta_threads = 1024)
 // restore pipelined with a per-layer GEMM from 4.26 ms (16 CTAs) to 3.54 ms.
 constexpr int kOverlapWideCtas = 8;
 
-int link_threads() { return g_cfg.cta_threads ? (int)g_cfg.cta_threads : kMoveThreads; }
+int link_threads(bool transpose) {
+    if (g_cfg.cta_threads) return (int)g_cfg.cta_threads;
+    return transpose ? kMoveThreads : kWideThreads;
+}
 int progressive_threads() {
     return g_cfg.cta_threads ? (int)g_cfg.cta_threads : kWideThreads;
 }
@@ -675,12 +680,13 @@ kv_status plan_layer_major(Plan &p, uint32_t n, const DevState &ds, uint64_t seq
     return KV_OK;
 }
 
-int default_ctas(const DevState &s, bool touches_host, int kernel = PK_REG) {
+int default_ctas(const DevState &s, bool touches_host, int kernel = PK_REG,
+                 int link_cta_threads = kMoveThreads) {
     if (g_cfg.max_ctas != 0) return (int)g_cfg.max_ctas;
     if (kernel == PK_BULK) return 3 * s.sms;   // 3 x 64 KiB rings fit one SM's shared memory
     if (kernel == PK_TSP) return s.sms;        // one 192 KiB ring per SM
     if (!touches_host) return 4 * s.sms;
-    return link_threads() == kWideThreads ? std::min(kLinkWideCtas, s.sms)
+    return link_cta_threads == kWideThreads ? std::min(kLinkWideCtas, s.sms)
                                           : std::min(kLinkCtas, 4 * s.sms);
 }
 
@@ -947,9 +953,10 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             p.d.skip_word = ds.status_dev + fs.k;
             p.d.skip_tag = fs.seq;
         }
-        p.threads = link_threads();
+        p.threads = link_threads(p.d.transpose != 0);
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
-        st = run_moves(p, a, b, n, default_ctas(ds, true), stream, false, &ds, &fs);
+        st = run_moves(p, a, b, n, default_ctas(ds, true, PK_REG, p.threads), stream, false, &ds,
+                       &fs);
         if (st != KV_OK) return st;
         fused = true;
     } else if (n > 0 && g_cfg.mode == KV_MODE_COPY_ENGINE) {
@@ -1703,7 +1710,7 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
         p.threads = progressive_threads();
         const int ctas = g_cfg.max_ctas ? (int)g_cfg.max_ctas
                          : p.threads == kWideThreads ? std::min(kOverlapWideCtas, ds.sms)
-                                                     : default_ctas(ds, true);
+                                                     : default_ctas(ds, true, PK_REG, p.threads);
         if (st == KV_OK) st = run_moves(p, host_slots, dst_pages, n, ctas, stream, false);
         if (st != KV_OK) return st;
     } else {

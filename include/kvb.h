@@ -144,13 +144,14 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
                                no programmatic dependent launch overlapping a kernel's
                                launch with the previous kernel's end */
 
-/* Defaults: host-link moves (zero-copy backup / restore) run 64 CTAs of 256
- * threads (a backup and a restore at once then reach the bidirectional link
+/* Defaults: host-link moves (zero-copy backup / restore) run 16 CTAs of 1024
+ * threads when pool and tier share a head order and 64 CTAs of 256 when the
+ * move changes it (the shapes with which a backup and a restore running at
+ * once come closest to the bidirectional link peak; either reaches the solo
  * peak); kv_restore_layers, made to run beside compute, runs 8 CTAs of 1024
  * threads (8 whole SMs); HBM-only moves run 4 CTAs of 256 threads per SM
- * (bulk-copy kernel: 3 per SM).  cta_threads = 1024 gives backups and
- * restores 16 CTAs of 1024 (whole SMs, fewer of them), 256 gives progressive
- * restores 64 CTAs of 256. */
+ * (bulk-copy kernel: 3 per SM).  cta_threads = 256 or 1024 forces that CTA
+ * size on every host-link move (64 CTAs of 256, 16 of 1024). */
 typedef struct {
     uint32_t mode;           /* kv_mode                                         */
     uint32_t max_ctas;       /* CTA cap of the transfer kernel; 0 = default     */
