@@ -60,11 +60,12 @@ kv_status cuda_fail(cudaError_t e, const char *what) {
 // Host-side failure drills ("[PP + HiCache] Add PP Prefetch Tickets",
 // §Targeted fault-injection validation: injected allocation failures must fall
 // back and leave the service running).  The next `count` passes through a
-// point fail as if the CUDA call there had failed; nothing touches the GPU.
+// point fail as if the CUDA call there had failed ("launch_nth": only the
+// count-th pass from now fails); nothing touches the GPU.
 enum FaultPoint { FP_STAGING_ALLOC, FP_FENCE_RESERVE, FP_LAUNCH, FP_IPC_OPEN, FP_HOST_REGISTER,
-                  FP_COUNT };
+                  FP_LAUNCH_NTH, FP_COUNT };
 const char *const kFaultNames[FP_COUNT] = {"staging_alloc", "fence_reserve", "launch", "ipc_open",
-                                           "host_register"};
+                                           "host_register", "launch_nth"};
 std::atomic<uint32_t> g_fault[FP_COUNT];
 std::once_flag g_fault_env_once;
 
@@ -93,7 +94,7 @@ bool fault_hit(FaultPoint p) {
     std::call_once(g_fault_env_once, load_fault_env);
     uint32_t c = g_fault[p].load();
     while (c > 0)
-        if (g_fault[p].compare_exchange_weak(c, c - 1)) return true;
+        if (g_fault[p].compare_exchange_weak(c, c - 1)) return p == FP_LAUNCH_NTH ? c == 1 : true;
     return false;
 }
 
@@ -737,8 +738,10 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
         const uint32_t per_cta = (p.bulk || p.tsp) ? 1u : (uint32_t)(p.threads / 32);
         const uint64_t need = ((uint64_t)p.d.total_segs + per_cta - 1) / per_cta;
         const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
-        if (i0 == 0 && fault_hit(FP_LAUNCH))
+        if ((i0 == 0 && fault_hit(FP_LAUNCH)) || fault_hit(FP_LAUNCH_NTH)) {
+            p.d.pdl = pdl0;
             return fail(KV_ERR_CUDA, "launch of the move kernel: injected failure");
+        }
         cudaError_t e = p.tsp    ? launch_tsp(p.d, ids, ctas, stream)
                         : p.bulk ? launch_bulk(p.d, ids, ctas, stream)
                                  : launch_move(p.d, ids, ctas, p.threads, stream);
@@ -1014,6 +1017,16 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         if (st != KV_OK) return st;
         const Side ps = pool_side(*pool);
         static thread_local std::vector<int32_t> idx;
+        // A failure after chunks were enqueued: the caller's stream still waits for
+        // every kernel already on the side stream and marks the half busy until
+        // then, so the next op of this direction cannot reuse a buffer in use.
+        auto fail_after_enqueue = [&](kv_status err) {
+            if (pipelined && cudaEventRecord(ds.op_start, ks) == cudaSuccess)
+                (void)cudaStreamWaitEvent(stream, ds.op_start, 0);
+            if (cudaEventRecord(ds.staging_free[half], stream) == cudaSuccess)
+                ds.staging_used[half] = true;
+            return err;
+        };
         uint64_t k = 0;
         for (uint32_t la = l0; la < l0 + nl; la += gl) {
             const uint32_t g_n = std::min(gl, l0 + nl - la);          // layers in this group
@@ -1028,7 +1041,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                 Plan p;
                 st = plan(pool->g, backup ? ps : ss, backup ? ss : ps, g_n, la, ds.err_dev, backup,
                           &p, kernel);
-                if (st != KV_OK) return st;
+                if (st != KV_OK) return k ? fail_after_enqueue(st) : st;
                 const int ctas = default_ctas(ds, false, kernel);
                 if (backup) {
                     if (pipelined && k >= 2)   // chunk k-2's copy has left this buffer
@@ -1064,13 +1077,13 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                     if (st == KV_OK && pipelined)
                         st = ck(cudaEventRecord(ds.moved[half][bi], ks), "staging record");
                 }
-                if (st != KV_OK) return st;
+                if (st != KV_OK) return fail_after_enqueue(st);
             }
         }
         if (pipelined && !backup) {   // the last scatters end on the caller's stream too
             for (int bi = 0; bi < 2 && st == KV_OK; ++bi)
                 st = ck(cudaStreamWaitEvent(stream, ds.moved[half][bi], 0), "staging wait");
-            if (st != KV_OK) return st;
+            if (st != KV_OK) return fail_after_enqueue(st);
         }
         cudaError_t e = cudaEventRecord(ds.staging_free[half], stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");

@@ -501,8 +501,10 @@ KVB_API uint32_t kv_abi_version(void);
  * injected allocation failure must fall back and leave the service running).
  * The next `count` passes through `point` fail as if the CUDA call there had
  * failed -- "staging_alloc" (NO_MEMORY), "fence_reserve" (NO_MEMORY),
- * "launch" (CUDA, before anything of the op is enqueued), "ipc_open" (CUDA),
- * "host_register" (CUDA); count 0 disarms.  The environment variable
+ * "launch" (CUDA, at an op's first kernel launch), "ipc_open" (CUDA),
+ * "host_register" (CUDA), "launch_nth" (CUDA: only the count-th move-kernel
+ * launch from now fails, possibly in the middle of an op -- what the op had
+ * enqueued before it still runs, and later ops wait for it); count 0 disarms.  The environment variable
  * KVB_FAULT="point:count[,point:count]" arms points at first use.  Nothing
  * here touches the GPU.  Errors: INVALID_ARG for an unknown point. */
 KVB_API kv_status kv_fault_inject(const char *point, uint32_t count);

@@ -201,5 +201,5 @@ def test_fault_injection_points_without_gpu():
         kvb.kv_host_register(0x10000, 1 << 20, 4, 0, lay())
     assert e.value.status == kvb.KV_ERR_CUDA and "injected" in kvb.kv_last_error()
     kvb.kv_fault_inject("host_register", 0)
-    for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open"):
+    for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open", "launch_nth"):
         kvb.kv_fault_inject(p, 0)

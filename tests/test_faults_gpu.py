@@ -27,7 +27,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def rig():
     r = Rig(wl.LLAMA8B.geom.with_(P=48, L=4), 16, seed=61)
     yield r
-    for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open", "host_register"):
+    for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open", "host_register",
+              "launch_nth"):
         kvb.kv_fault_inject(p, 0)
     r.close()
 
@@ -136,3 +137,60 @@ def test_injected_ipc_open_failure_then_import():
     finally:
         done.set()
         p.join(120)
+
+
+@pytest.mark.parametrize("mode,kind,n,nth", [
+    (kvb.KV_MODE_STAGED, "backup", 200, 3),      # 7 chunks of 32 pages: the 3rd launch fails
+    (kvb.KV_MODE_STAGED, "restore", 200, 4),
+    (kvb.KV_MODE_ZERO_COPY, "backup", 2100, 2),  # two launches: the second fails
+    (kvb.KV_MODE_ZERO_COPY, "restore", 2100, 2),
+])
+def test_failure_in_the_middle_of_an_op_then_the_engine_recovers(mode, kind, n, nth):
+    """A launch that fails after part of an op was enqueued: the op reports
+    CUDA, what it enqueued before still completes, nothing else is touched,
+    and the following ops (which may reuse the staging buffers) are exact."""
+    g = wl.Geometry(L=2, C=2, P=3 * n + 100, T=16, H=2, B=128)   # three disjoint page sets
+    rig = Rig(g, 2 * n, seed=77)
+    old = kvb.kv_config_get()
+    try:
+        kvb.kv_config_set(mode, 0, 2 << 20)       # 512 KiB ping-pong buffers: many chunks
+        r = np.random.default_rng(5)
+        pages = r.permutation(g.P).astype(np.int32)
+        a_src, b_src, dst = pages[:n], pages[n:2 * n], pages[2 * n:3 * n]
+        slots_a = np.arange(n, dtype=np.int32)
+        slots_b = np.arange(n, 2 * n, dtype=np.int32)
+        snap = rig.snapshot()
+        kvb.kv_fault_inject("launch_nth", nth)
+        with pytest.raises(kvb.KvError) as e:
+            if kind == "backup":
+                kvb.kv_backup(rig.pool, rig.hostt, a_src, slots_a)
+            else:
+                kvb.kv_restore(rig.pool, rig.hostt, slots_a, dst)
+        assert e.value.status == kvb.KV_ERR_CUDA
+        torch.cuda.synchronize()
+        after = rig.snapshot()
+        # the failed op wrote only where it was allowed to (backup: slots_a; restore: dst)
+        if kind == "backup":
+            assert np.array_equal(after[0], snap[0])
+            keep = np.ones(after[1].size, bool)
+            keep[:n * g.page_bytes] = False
+            assert np.array_equal(after[1][keep], snap[1][keep])
+        else:
+            assert np.array_equal(after[1], snap[1])
+            from gpu_rig import oracle_geom
+            import oracle
+            moved = snap[0].copy()
+            oracle.restore(oracle_geom(g), moved, snap[1], slots_a, dst, threads=8)
+            untouched = np.flatnonzero(moved == snap[0])
+            assert np.array_equal(after[0][untouched], snap[0][untouched])
+        # the engine keeps serving, exactly: a backup and a restore through the same path
+        want = rig.expect_backup(after, b_src, slots_b)
+        kvb.kv_fence_wait(kvb.kv_backup(rig.pool, rig.hostt, b_src, slots_b), 60_000_000_000)
+        rig.assert_equal(want)
+        want = rig.expect_restore(want, slots_b, dst)
+        kvb.kv_fence_wait(kvb.kv_restore(rig.pool, rig.hostt, slots_b, dst), 60_000_000_000)
+        rig.assert_equal(want)
+    finally:
+        kvb.kv_fault_inject("launch_nth", 0)
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+        rig.close()
