@@ -618,3 +618,37 @@ def test_restore_when_ready_waits_and_gives_up():
         rig.assert_equal(snap2)
     finally:
         rig.close()
+
+
+@pytest.mark.parametrize("cfg_mode", [kvb.KV_MODE_STAGED, kvb.KV_MODE_COPY_ENGINE],
+                         ids=["staged", "copy_engine"])
+def test_gated_ops_run_zero_copy_in_every_mode(cfg_mode):
+    """Ready-gated BACKUP and RESTORE take the zero-copy path whatever the mode:
+    each waits for its word, then equals the oracle (TRT-LLM-shaped HND pool at
+    an offset, whole-prefix backup, one-layer restore)."""
+    g = wl.TRTLLM.geom.with_(P=24, L=6)
+    rig = Rig(g, 8, pool_offset=wl.TRTLLM.pool_offset, seed=31)
+    old = kvb.kv_config_get()
+    word = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    try:
+        kvb.kv_config_set(cfg_mode, 0, 4 << 20)
+        src, slots, dst = [3, 9, 20], [0, 5, 7], [1, 2, 4]
+        snap = rig.snapshot()
+        want = rig.expect_backup(snap, src, slots)
+        s = torch.cuda.Stream()
+        f = kvb.kv_backup_when_ready(rig.pool, rig.hostt, src, slots, word.data_ptr(), 1,
+                                     20_000_000_000, s.cuda_stream)
+        assert kvb.kv_fence_query(f) == kvb.KV_ERR_TIMEOUT          # gated
+        word[0] = 1
+        kvb.kv_fence_wait(f, 20_000_000_000)
+        rig.assert_equal(want)
+        want = rig.expect_restore(want, slots, dst, layer=4)
+        f = kvb.kv_restore_when_ready(rig.pool, rig.hostt, slots, dst, word.data_ptr(), 2,
+                                      20_000_000_000, 4, s.cuda_stream)
+        assert kvb.kv_fence_query(f) == kvb.KV_ERR_TIMEOUT
+        word[0] = 2
+        kvb.kv_fence_wait(f, 20_000_000_000)
+        rig.assert_equal(want)
+    finally:
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+        rig.close()
