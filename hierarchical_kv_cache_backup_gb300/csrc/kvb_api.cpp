@@ -208,6 +208,14 @@ struct DevState {
     cudaEvent_t op_start = nullptr;          // caller's stream at the op's start
     cudaEvent_t moved[2][2] = {};            // [half][buffer]: kernel done with it
     cudaEvent_t copied[2][2] = {};           // [half][buffer]: copy engine done with it
+    // Progressive restores of more than kMaxItems pages: their ids go through a
+    // pinned buffer and a device buffer (a then b, n each) instead of the launch
+    int32_t *gids = nullptr;                 // device
+    int32_t *gids_host = nullptr;            // pinned
+    uint64_t gids_cap = 0;                   // int32 entries in each
+    cudaEvent_t gids_copied = nullptr;       // the pinned -> device copy is done
+    cudaEvent_t gids_free = nullptr;         // the kernel reading the device ids is done
+    bool gids_used = false;
 };
 
 std::mutex g_mu;
@@ -660,10 +668,11 @@ int progressive_threads() {
 }
 
 // Turns a plan into a progressive multi-layer plan for n items (one launch).
-kv_status plan_layer_major(Plan &p, uint32_t n, const DevState &ds, uint64_t seq0) {
+kv_status plan_layer_major(Plan &p, uint32_t n, const DevState &ds, uint64_t seq0,
+                           bool device_ids = false) {
     MoveDesc &d = p.d;
     const uint64_t pls = (uint64_t)n * d.C * d.segs;
-    if (n > p.max_items || pls * d.nl > 0x7fffffffull || pls == 0)
+    if ((n > p.max_items && !device_ids) || pls * d.nl > 0x7fffffffull || pls == 0)
         return fail(KV_ERR_OUT_OF_RANGE, "%u pages x %u layers is too large for one progressive "
                     "restore", n, d.nl);
     d.layer_major = 1;
@@ -709,6 +718,21 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
                     cudaStream_t stream, bool b_is_index, const DevState *ds = nullptr,
                     const FenceSlot *fence = nullptr) {
     static thread_local MoveIds ids;
+    if (p.d.gid_a != nullptr) {   // ids already in device memory: one launch for all n
+        p.d.fence_word = nullptr;
+        p.d.fence_count = nullptr;
+        p.d.n = n;
+        p.d.total_segs = n * p.d.nl * p.d.C * p.d.segs;
+        const uint32_t per_cta = (uint32_t)(p.threads / 32);
+        const uint64_t need = ((uint64_t)p.d.total_segs + per_cta - 1) / per_cta;
+        const int ctas = (int)std::max<uint64_t>(1, std::min<uint64_t>(need, (uint64_t)ctas_cap));
+        if (fault_hit(FP_LAUNCH) || fault_hit(FP_LAUNCH_NTH))
+            return fail(KV_ERR_CUDA, "launch of the move kernel: injected failure");
+        cudaError_t e = launch_move(p.d, ids, ctas, p.threads, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "launch of the move kernel");
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        return KV_OK;
+    }
     // Only an op's first launch overlaps its start with the previous kernel's
     // end (programmatic dependent launch); the further slices of an op above
     // kMaxItems pages launch plainly: with a move in the other direction running
@@ -789,6 +813,58 @@ kv_status ensure_staging(DevState &s) {
     for (int h = 0; h < 2 && e == cudaSuccess; ++h)
         if (s.side[h] == nullptr) e = cudaStreamCreateWithFlags(&s.side[h], cudaStreamNonBlocking);
     if (e != cudaSuccess) return cuda_fail(e, "staging stream / events");
+    return KV_OK;
+}
+
+// Puts the ids of a progressive restore of more than kMaxItems pages into the
+// device buffer (a at [0, n), b at [n, 2n)): host copy into the pinned buffer,
+// then one copy to the device on `stream`.  The previous large restore's kernel
+// must be done with the device buffer (stream wait on gids_free) and its copy
+// done with the pinned buffer (host wait on gids_copied, normally long done).
+kv_status stage_ids(DevState &s, const int32_t *a, const int32_t *b, uint32_t n,
+                    cudaStream_t stream) {
+    const uint64_t need = 2ull * n;
+    cudaError_t e = cudaSuccess;
+    auto make_event = [](cudaEvent_t *ev) {
+        return *ev != nullptr ? cudaSuccess : cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    };
+    e = make_event(&s.gids_copied);
+    if (e == cudaSuccess) e = make_event(&s.gids_free);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(ids)");
+    if (s.gids_used) {
+        e = cudaEventSynchronize(s.gids_copied);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, s.gids_free, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "waiting for the id buffers");
+    }
+    if (need > s.gids_cap) {
+        if (s.gids_used) {   // nothing may still read the old buffers
+            e = cudaEventSynchronize(s.gids_free);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize(ids)");
+        }
+        if (s.gids) cudaFree(s.gids);
+        if (s.gids_host) cudaFreeHost(s.gids_host);
+        s.gids = nullptr;
+        s.gids_host = nullptr;
+        s.gids_cap = 0;
+        const uint64_t cap = std::max<uint64_t>(need, 1ull << 16);
+        void *dptr = nullptr, *hptr = nullptr;
+        e = cudaMalloc(&dptr, cap * sizeof(int32_t));
+        if (e == cudaSuccess) e = cudaHostAlloc(&hptr, cap * sizeof(int32_t), cudaHostAllocDefault);
+        if (e != cudaSuccess) {
+            if (dptr) cudaFree(dptr);
+            return fail(KV_ERR_NO_MEMORY, "id buffers of %llu entries: %s",
+                        (unsigned long long)cap, cudaGetErrorString(e));
+        }
+        s.gids = (int32_t *)dptr;
+        s.gids_host = (int32_t *)hptr;
+        s.gids_cap = cap;
+    }
+    std::memcpy(s.gids_host, a, (size_t)n * sizeof(int32_t));
+    std::memcpy(s.gids_host + n, b, (size_t)n * sizeof(int32_t));
+    e = cudaMemcpyAsync(s.gids, s.gids_host, need * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        stream);
+    if (e == cudaSuccess) e = cudaEventRecord(s.gids_copied, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "copying the ids to the device");
     return KV_OK;
 }
 
@@ -1694,9 +1770,6 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
         return fail(KV_ERR_OUT_OF_RANGE, "layers [%u, %u + %u) are not inside [0, %llu) or exceed "
                     "%d", first_layer, first_layer, num_layers, (unsigned long long)pool->g.L,
                     kRing / 2);
-    if (n > (uint32_t)kMaxItems)
-        return fail(KV_ERR_OUT_OF_RANGE, "n = %u exceeds the %d pages of one progressive restore",
-                    n, kMaxItems);
     kv_status st = check_op(pool->g, host->num_slots, 1, host_slots, dst_pages, n, -1);
     if (st != KV_OK) return st;
     const int d = pool->device;
@@ -1731,12 +1804,25 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
         const Side ps = pool_side(*pool), hs = host_side(*host);
         Plan p;
         st = plan(pool->g, hs, ps, num_layers, first_layer, ds.err_dev, false, &p);
-        if (st == KV_OK) st = plan_layer_major(p, n, ds, seq0);
+        // above one launch's id capacity the ids go through device memory, so
+        // that one kernel still publishes every layer of the whole op in order
+        const bool device_ids = st == KV_OK && n > p.max_items;
+        if (st == KV_OK) st = plan_layer_major(p, n, ds, seq0, device_ids);
+        if (st == KV_OK && device_ids) {
+            st = stage_ids(ds, host_slots, dst_pages, n, stream);
+            p.d.gid_a = ds.gids;
+            p.d.gid_b = ds.gids + n;
+        }
         p.threads = progressive_threads();
         const int ctas = g_cfg.max_ctas ? (int)g_cfg.max_ctas
                          : p.threads == kWideThreads ? std::min(kOverlapWideCtas, ds.sms)
                                                      : default_ctas(ds, true, PK_REG, p.threads);
         if (st == KV_OK) st = run_moves(p, host_slots, dst_pages, n, ctas, stream, false);
+        if (st == KV_OK && device_ids) {
+            cudaError_t e2 = cudaEventRecord(ds.gids_free, stream);
+            if (e2 != cudaSuccess) return cuda_fail(e2, "cudaEventRecord(ids)");
+            ds.gids_used = true;
+        }
         if (st != KV_OK) return st;
     } else {
         for (uint32_t j = 0; j < num_layers; ++j) {   // nothing to move: mark every layer

@@ -96,6 +96,10 @@ struct MoveDesc {
     // previous kernel on its stream finishes; it waits (griddepcontrol.wait)
     // for that kernel's completion before touching memory.
     uint32_t pdl;
+    // Ids in device memory (item i: gid_a[i], gid_b[i]) instead of the launch's
+    // parameter block, for one move kernel over more items than a parameter
+    // block holds (progressive restores of more than kMaxItems pages).
+    const int32_t *gid_a, *gid_b;
 };
 
 // Ids of one launch, inside the kernel's parameter block.  Launches use the

@@ -225,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
         }
         ++cur_count;
         const uint64_t l = d.l0 + lr;
-        const uint32_t ia = (uint32_t)ids.a[item];
-        const uint32_t ib = (uint32_t)ids.b[item];
+        const uint32_t ia = d.gid_a ? (uint32_t)__ldg(d.gid_a + item) : (uint32_t)ids.a[item];
+        const uint32_t ib = d.gid_a ? (uint32_t)__ldg(d.gid_b + item) : (uint32_t)ids.b[item];
         if (ia >= d.src.id_limit || ib >= d.dst.id_limit) {
             // Host validation makes this unreachable; never touch memory for a bad id.
             if (lane == 0 && d.err != nullptr) *(volatile uint32_t *)d.err = 1u;
@@ -571,7 +571,8 @@ FastDiv make_fastdiv(uint32_t d) {
 template <int kCap, int kThreads>
 static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
     IdsT<kCap> p;
-    for (uint32_t i = 0; i < d.n; ++i) {
+    const uint32_t in_block = d.gid_a ? 0u : d.n;   // ids in device memory: none in the block
+    for (uint32_t i = 0; i < in_block; ++i) {
         p.a[i] = ids.a[i];
         p.b[i] = ids.b[i];
     }
@@ -600,7 +601,7 @@ static cudaError_t launch_cap(const MoveDesc &d, const MoveIds &ids, int ctas, c
 template <int kThreads>
 static cudaError_t launch_threads(const MoveDesc &d, const MoveIds &ids, int ctas,
                                   cudaStream_t stream) {
-    if (d.n <= 64) return launch_cap<64, kThreads>(d, ids, ctas, stream);
+    if (d.gid_a != nullptr || d.n <= 64) return launch_cap<64, kThreads>(d, ids, ctas, stream);
     if (d.n <= 512) return launch_cap<512, kThreads>(d, ids, ctas, stream);
     return launch_cap<kMaxItems, kThreads>(d, ids, ctas, stream);
 }
@@ -640,7 +641,7 @@ static cudaError_t launch_bulk_cap(const MoveDesc &d, const MoveIds &ids, int ct
 
 cudaError_t launch_bulk(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
     (void)cudaGetLastError();
-    if (d.n > (uint32_t)kMaxItems || d.transpose) return cudaErrorInvalidValue;
+    if (d.n > (uint32_t)kMaxItems || d.transpose || d.gid_a != nullptr) return cudaErrorInvalidValue;
     if (d.n <= 64) return launch_bulk_cap<64>(d, ids, ctas, stream);
     if (d.n <= 512) return launch_bulk_cap<512>(d, ids, ctas, stream);
     return launch_bulk_cap<kMaxItems>(d, ids, ctas, stream);
@@ -687,7 +688,8 @@ static cudaError_t launch_tsp_cap(const MoveDesc &d, const MoveIds &ids, int cta
 
 cudaError_t launch_tsp(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStream_t stream) {
     (void)cudaGetLastError();
-    if (d.n > (uint32_t)kMaxItems || !d.transpose || d.segs != 1 || d.cb16 * 16u > kTspMaxChunk)
+    if (d.n > (uint32_t)kMaxItems || !d.transpose || d.segs != 1 || d.cb16 * 16u > kTspMaxChunk ||
+        d.gid_a != nullptr)
         return cudaErrorInvalidValue;
     if (d.n <= 64) return launch_tsp_cap<64>(d, ids, ctas, stream);
     if (d.n <= 512) return launch_tsp_cap<512>(d, ids, ctas, stream);
@@ -697,7 +699,8 @@ cudaError_t launch_tsp(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStre
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int threads,
                         cudaStream_t stream) {
     (void)cudaGetLastError();   // report this launch's error, not an earlier call's
-    if (d.n > (uint32_t)kMaxItems) return cudaErrorInvalidValue;
+    if (d.n > (uint32_t)kMaxItems && d.gid_a == nullptr) return cudaErrorInvalidValue;
+    if ((d.gid_a == nullptr) != (d.gid_b == nullptr)) return cudaErrorInvalidValue;
     if (threads == kWideThreads) return launch_threads<kWideThreads>(d, ids, ctas, stream);
     if (threads == kMoveThreads) return launch_threads<kMoveThreads>(d, ids, ctas, stream);
     return cudaErrorInvalidValue;

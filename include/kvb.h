@@ -296,7 +296,12 @@ KVB_API kv_status kv_restore(kv_pool pool, kv_host host, const int32_t *host_slo
  * first_layer + j are all in place, so layer j's fence implies every earlier
  * one; a compute stream waits for one layer with kv_fence_stream_wait, which
  * waits on the GPU for that fence word while later layers are still moving.
- * Limits: n <= 2048, 1 <= num_layers <= 2048, first_layer + num_layers <= L.
+ * Limits: 1 <= num_layers <= 2048, first_layer + num_layers <= L, and
+ * n x num_layers x components x (page-layer chunk / 4 KiB) below 2^31.  Up to
+ * 2048 pages the ids travel in the launch; above, the call copies them into a
+ * library device buffer (through a library pinned buffer, on `stream`) and
+ * still runs one kernel; the next such call waits for that kernel on the GPU
+ * before reusing the buffer.
  * Errors: as kv_restore. */
 KVB_API kv_status kv_restore_layers(kv_pool pool, kv_host host, const int32_t *host_slots,
                                     const int32_t *dst_pages, uint32_t n, uint32_t first_layer,

@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
-from gpu_rig import Rig  # noqa: E402
+import oracle  # noqa: E402
+from gpu_rig import Rig, oracle_geom  # noqa: E402
 from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
 from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
 
@@ -651,4 +652,66 @@ def test_gated_ops_run_zero_copy_in_every_mode(cfg_mode):
         rig.assert_equal(want)
     finally:
         kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+        rig.close()
+
+
+def test_restore_layers_above_one_launch_capacity():
+    """More than 2,048 pages in one progressive restore: the ids go through the
+    library's device buffer and one kernel publishes every layer.  A second
+    large call on another stream, issued at once, reuses that buffer; both end
+    as the oracle says, and every layer fence of both completes."""
+    g = wl.Geometry(L=8, C=2, P=6200, T=16, H=2, B=128)
+    na, nb = 3000, 2500
+    rig = Rig(g, na + nb, seed=43)
+    try:
+        r = np.random.default_rng(43)
+        pages = r.permutation(g.P).astype(np.int32)
+        dst_a, dst_b = pages[:na], pages[na:na + nb]
+        slots_a = r.permutation(na).astype(np.int32)
+        slots_b = (na + r.permutation(nb)).astype(np.int32)
+        snap = rig.snapshot()
+        want = rig.expect_restore(snap, slots_a, dst_a)
+        want = rig.expect_restore(want, slots_b, dst_b)
+        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        fa = kvb.kv_restore_layers(rig.pool, rig.hostt, slots_a, dst_a, 0, g.L, sa.cuda_stream)
+        fb = kvb.kv_restore_layers(rig.pool, rig.hostt, slots_b, dst_b, 0, g.L, sb.cuda_stream)
+        for f in fa + fb:
+            kvb.kv_fence_wait(f, 60_000_000_000)
+        rig.assert_equal(want)
+    finally:
+        rig.close()
+
+
+def test_restore_layers_above_capacity_on_a_split_pool():
+    """2,049 pages (one above a launch's id capacity) restored progressively
+    into a pool kept as one buffer per (layer, component)."""
+    g = wl.Geometry(L=3, C=2, P=4200, T=8, H=2, B=64)
+    n = 2049
+    rig = Rig(g, n, seed=44, register=False)
+    bufs = [torch.empty(g.P * g.T * g.H * g.B, dtype=torch.uint8, device="cuda")
+            for _ in range(g.L * g.C)]
+    for k, b in enumerate(bufs):
+        wl.fill_random_(b, 100 + k)
+    try:
+        lay = rig.layout
+        pool = kvb.kv_pool_register_split(lay, [b.data_ptr() for b in bufs])
+        tier = kvb.kv_host_register(rig.host.data_ptr(), rig.host.numel(), n, g.host_heads, lay)
+        r = np.random.default_rng(44)
+        dst = r.permutation(g.P)[:n].astype(np.int32)
+        slots = r.permutation(n).astype(np.int32)
+        torch.cuda.synchronize()
+        # the split pool equals a contiguous layer-first pool [L][C][P][T][H][B]
+        flat = torch.cat(bufs).cpu().numpy()
+        host = rig.host.numpy().copy()
+        want = flat.copy()
+        oracle.restore(oracle_geom(g), want, host, slots, dst, threads=8)
+        fences = kvb.kv_restore_layers(pool, tier, slots, dst, 0, g.L)
+        for f in fences:
+            kvb.kv_fence_wait(f, 60_000_000_000)
+        torch.cuda.synchronize()
+        got = torch.cat(bufs).cpu().numpy()
+        assert np.array_equal(got, want)
+        kvb.kv_pool_close(pool)
+        kvb.kv_host_close(tier)
+    finally:
         rig.close()
