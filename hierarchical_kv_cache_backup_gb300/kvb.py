@@ -174,6 +174,8 @@ def _ids(x):
 
 
 def make_layout(L, C, P, T, H, B, order=KV_LAYER_FIRST, heads=KV_NHD, elem_bytes=2) -> kv_layout:
+    """A kv_layout: L layers, C components, P pages, T tokens per page, H heads, B bytes per
+    head vector; order / heads of the device pool."""
     return kv_layout(L, C, P, T, H, B, order, heads, elem_bytes, 0)
 
 
@@ -181,6 +183,8 @@ def make_layout(L, C, P, T, H, B, order=KV_LAYER_FIRST, heads=KV_NHD, elem_bytes
 
 def kv_pool_register(layout: kv_layout, base: int, offset: int = 0, instance_id: int = 0,
                      generation: int = 0) -> int:
+    """Registers a pool that starts `offset` bytes after device pointer `base`; returns its
+    handle."""
     out = ctypes.c_void_p()
     _check(_lib.kv_pool_register(ctypes.byref(layout), base, offset, instance_id, generation,
                                  ctypes.byref(out)))
@@ -198,36 +202,45 @@ def kv_pool_register_split(layout: kv_layout, bases, instance_id: int = 0,
 
 
 def kv_pool_export(pool: int) -> kv_ipc_desc:
+    """The pool as a kv_ipc_desc (IPC handle of its allocation, offset, size, identity) for
+    another process."""
     d = kv_ipc_desc()
     _check(_lib.kv_pool_export(pool, ctypes.byref(d)))
     return d
 
 
 def kv_pool_import(desc: kv_ipc_desc) -> int:
+    """Maps a pool exported by another process (one mapping per allocation, refcounted);
+    returns its handle."""
     out = ctypes.c_void_p()
     _check(_lib.kv_pool_import(ctypes.byref(desc), ctypes.byref(out)))
     return out.value
 
 
 def kv_pool_close(pool: int) -> None:
+    """Closes a pool handle (the last close of an imported allocation unmaps it)."""
     _check(_lib.kv_pool_close(pool))
 
 
 def kv_pool_retire(instance_id: int, min_generation: int) -> None:
+    """Refuses, from now on, pools of `instance_id` older than `min_generation` (KV_ERR_STALE)."""
     _check(_lib.kv_pool_retire(instance_id, min_generation))
 
 
 def kv_pool_info(pool: int):
+    """Returns (layout, device address of the pool, bytes) of a pool handle."""
     lay, ptr, nb = kv_layout(), ctypes.c_void_p(), ctypes.c_uint64()
     _check(_lib.kv_pool_info(pool, ctypes.byref(lay), ctypes.byref(ptr), ctypes.byref(nb)))
     return lay, ptr.value, nb.value
 
 
 def desc_to_bytes(d: kv_ipc_desc) -> bytes:
+    """The kv_ipc_desc as bytes (to send to another process)."""
     return ctypes.string_at(ctypes.addressof(d), ctypes.sizeof(d))
 
 
 def desc_from_bytes(b: bytes) -> kv_ipc_desc:
+    """A kv_ipc_desc from the bytes desc_to_bytes produced."""
     if len(b) != ctypes.sizeof(kv_ipc_desc):
         raise ValueError(f"descriptor must be {ctypes.sizeof(kv_ipc_desc)} bytes, got {len(b)}")
     return kv_ipc_desc.from_buffer_copy(b)
@@ -237,6 +250,8 @@ def desc_from_bytes(b: bytes) -> kv_ipc_desc:
 
 def kv_host_register(host: int, nbytes: int, num_slots: int, host_heads: int,
                      pool_layout: kv_layout) -> int:
+    """Registers a pinned, device-mapped host tier of `num_slots` page slots; returns its
+    handle."""
     out = ctypes.c_void_p()
     _check(_lib.kv_host_register(host, nbytes, num_slots, host_heads, ctypes.byref(pool_layout),
                                  ctypes.byref(out)))
@@ -244,12 +259,15 @@ def kv_host_register(host: int, nbytes: int, num_slots: int, host_heads: int,
 
 
 def kv_host_close(host: int) -> None:
+    """Closes a host tier handle."""
     _check(_lib.kv_host_close(host))
 
 
 # -------------------------------------------------------------- operations
 
 def kv_backup(pool: int, host: int, src_pages, host_slots, stream=None) -> int:
+    """BACKUP: host slot host_slots[i] <- page src_pages[i], every layer; enqueued on
+    `stream`; returns the fence."""
     a, pa = _ids(src_pages)
     b, pb = _ids(host_slots)
     if a.size != b.size:
@@ -274,6 +292,9 @@ def kv_restore_layers(pool: int, host: int, host_slots, dst_pages, first_layer: 
 
 def kv_backup_when_ready(pool: int, host: int, src_pages, host_slots, ready_word: int,
                          ready_value: int, ready_timeout_ns: int, stream=None) -> int:
+    """BACKUP that starts on the GPU once the 64-bit word at `ready_word` reaches
+    `ready_value` (bounded wait; on time-out it moves nothing and its fence reports ABORTED);
+    returns the fence."""
     a, pa = _ids(src_pages)
     b, pb = _ids(host_slots)
     if a.size != b.size:
@@ -287,6 +308,8 @@ def kv_backup_when_ready(pool: int, host: int, src_pages, host_slots, ready_word
 def kv_restore_when_ready(pool: int, host: int, host_slots, dst_pages, ready_word: int,
                           ready_value: int, ready_timeout_ns: int, layer: int = -1,
                           stream=None) -> int:
+    """RESTORE gated like kv_backup_when_ready on its host data having landed; returns the
+    fence."""
     a, pa = _ids(host_slots)
     b, pb = _ids(dst_pages)
     if a.size != b.size:
@@ -298,6 +321,8 @@ def kv_restore_when_ready(pool: int, host: int, host_slots, dst_pages, ready_wor
 
 
 def kv_restore(pool: int, host: int, host_slots, dst_pages, layer: int = -1, stream=None) -> int:
+    """RESTORE: page dst_pages[i] <- host slot host_slots[i], every layer (layer = -1) or one
+    layer; returns the fence."""
     a, pa = _ids(host_slots)
     b, pb = _ids(dst_pages)
     if a.size != b.size:
@@ -309,6 +334,7 @@ def kv_restore(pool: int, host: int, host_slots, dst_pages, layer: int = -1, str
 
 def kv_device_gather(pool: int, buf: int, buf_bytes: int, buf_heads: int, src_pages,
                      stream=None) -> int:
+    """Pool pages -> a device buffer in host-tier layout (HBM only); returns the fence."""
     a, pa = _ids(src_pages)
     f = ctypes.c_uint64()
     _check(_lib.kv_device_gather(pool, buf, buf_bytes, buf_heads, pa, a.size, stream,
@@ -318,6 +344,8 @@ def kv_device_gather(pool: int, buf: int, buf_bytes: int, buf_heads: int, src_pa
 
 def kv_device_scatter(pool: int, buf: int, buf_bytes: int, buf_heads: int, dst_pages,
                       layer: int = -1, stream=None) -> int:
+    """A device buffer in host-tier layout -> pool pages (every layer, or one); returns the
+    fence."""
     a, pa = _ids(dst_pages)
     f = ctypes.c_uint64()
     _check(_lib.kv_device_scatter(pool, buf, buf_bytes, buf_heads, pa, a.size, layer, stream,
@@ -345,20 +373,25 @@ def kv_op_validate(layout: kv_layout, num_slots: int, kind: int, a, b, layer: in
 # ------------------------------------------------------------------ fences
 
 def kv_fence_query(fence: int) -> int:
+    """Status of a fence without waiting: KV_OK done, KV_ERR_TIMEOUT not yet, KV_ERR_ABORTED
+    gave up."""
     return _lib.kv_fence_query(fence)
 
 
 def kv_fence_wait(fence: int, timeout_ns: int = 60_000_000_000) -> None:
+    """Waits (host) up to `timeout_ns` for a fence; raises KvError on time-out or abort."""
     _check(_lib.kv_fence_wait(fence, timeout_ns))
 
 
 def kv_fence_stream_wait(fence: int, stream=None) -> None:
+    """Makes `stream` wait on the GPU until the fence completes."""
     _check(_lib.kv_fence_stream_wait(fence, stream))
 
 
 # --------------------------------------------------------------- utilities
 
 def kv_config_get() -> kv_config:
+    """The process-wide kv_config (mode, CTA cap, staging bytes, flags, CTA size)."""
     c = kv_config()
     _check(_lib.kv_config_get(ctypes.byref(c)))
     return c
@@ -366,25 +399,30 @@ def kv_config_get() -> kv_config:
 
 def kv_config_set(mode: int = KV_MODE_ZERO_COPY, max_ctas: int = 0, staging_bytes: int = 0,
                   flags: int = 0, cta_threads: int = 0):
+    """Sets the process-wide kv_config for operations issued afterwards."""
     _check(_lib.kv_config_set(ctypes.byref(kv_config(mode, max_ctas, staging_bytes, flags,
                                                      cta_threads))))
 
 
 def kv_layout_page_bytes(layout: kv_layout) -> int:
+    """Bytes of one page (L * C * T * H * B) of a layout."""
     out = ctypes.c_uint64()
     _check(_lib.kv_layout_page_bytes(ctypes.byref(layout), ctypes.byref(out)))
     return out.value
 
 
 def kv_launch_count() -> int:
+    """Kernels the library has launched so far (all devices)."""
     return _lib.kv_launch_count()
 
 
 def kv_last_error() -> str:
+    """Message of this thread's last failing call."""
     return _lib.kv_last_error().decode(errors="replace")
 
 
 def kv_abi_version() -> int:
+    """ABI version of the loaded library."""
     return _lib.kv_abi_version()
 
 
@@ -392,6 +430,8 @@ def kv_abi_version() -> int:
 
 def make_ring_op(kind: int, a, b, pool_index: int = 0, layer: int = -1,
                  operation_id: int = 0) -> kv_ring_op:
+    """A descriptor for the shared-memory ring: kind 0 BACKUP (a = pages, b = slots) or 1
+    RESTORE (a = slots, b = pages)."""
     a_, _ = _ids(a)
     b_, _ = _ids(b)
     if a_.size != b_.size or a_.size > KV_RING_MAX_IDS:
@@ -405,22 +445,27 @@ def make_ring_op(kind: int, a, b, pool_index: int = 0, layer: int = -1,
 
 
 def kv_ring_create(name: str, slots: int) -> int:
+    """Creates a named shared-memory descriptor ring of `slots` entries (the submitting side);
+    returns its handle."""
     out = ctypes.c_void_p()
     _check(_lib.kv_ring_create(name.encode(), slots, ctypes.byref(out)))
     return out.value
 
 
 def kv_ring_attach(name: str) -> int:
+    """Attaches to a ring another process created (the serving side); returns its handle."""
     out = ctypes.c_void_p()
     _check(_lib.kv_ring_attach(name.encode(), ctypes.byref(out)))
     return out.value
 
 
 def kv_ring_close(ring: int) -> None:
+    """Closes a ring handle (the creator also unlinks the name)."""
     _check(_lib.kv_ring_close(ring))
 
 
 def kv_ring_submit(ring: int, op: kv_ring_op, timeout_ns: int = 10_000_000_000) -> int:
+    """Publishes a descriptor; returns its ticket (waits up to `timeout_ns` for a free slot)."""
     t = ctypes.c_uint64()
     _check(_lib.kv_ring_submit(ring, ctypes.byref(op), timeout_ns, ctypes.byref(t)))
     return t.value
@@ -435,6 +480,8 @@ def kv_ring_wait(ring: int, ticket: int, timeout_ns: int = 10_000_000_000) -> in
 
 def kv_ring_serve(ring: int, pools, host: int, stream=None, max_ops: int = 1,
                   idle_timeout_ns: int = 1_000_000_000) -> int:
+    """Serves up to `max_ops` descriptors through kv_backup / kv_restore on `stream`; the GPU
+    completes each ticket; returns how many."""
     arr = (ctypes.c_void_p * max(1, len(pools)))(*pools)
     served = ctypes.c_uint32()
     _check(_lib.kv_ring_serve(ring, arr, len(pools), host, stream, max_ops, idle_timeout_ns,
@@ -443,12 +490,14 @@ def kv_ring_serve(ring: int, pools, host: int, stream=None, max_ops: int = 1,
 
 
 def kv_ring_pop(ring: int, timeout_ns: int = 1_000_000_000):
+    """Takes the next descriptor (server side); returns (ticket, op)."""
     op, t = kv_ring_op(), ctypes.c_uint64()
     _check(_lib.kv_ring_pop(ring, timeout_ns, ctypes.byref(op), ctypes.byref(t)))
     return t.value, op
 
 
 def kv_ring_complete(ring: int, ticket: int, status: int = KV_OK) -> None:
+    """Completes a ticket from the CPU with a status (server side)."""
     _check(_lib.kv_ring_complete(ring, ticket, status))
 
 
@@ -456,6 +505,8 @@ def kv_ring_complete(ring: int, ticket: int, status: int = KV_OK) -> None:
 
 def kv_l3_open(fd: int, base_offset: int, record_bytes: int, num_records: int,
                threads: int = 0) -> int:
+    """An L3 record store over file descriptor `fd`: `num_records` records of `record_bytes`
+    from `base_offset`; returns its handle."""
     out = ctypes.c_void_p()
     _check(_lib.kv_l3_open(fd, base_offset, record_bytes, num_records, threads,
                            ctypes.byref(out)))
@@ -463,6 +514,7 @@ def kv_l3_open(fd: int, base_offset: int, record_bytes: int, num_records: int,
 
 
 def kv_l3_close(store: int) -> None:
+    """Closes an L3 record store (stops its worker threads; the caller closes the fd)."""
     _check(_lib.kv_l3_close(store))
 
 
@@ -485,6 +537,8 @@ def kv_l3_get(store: int, host: int, host_slots: int, records, slots) -> None:
 
 
 def kv_fault_inject(point: str, count: int = 1) -> None:
+    """Arms a host-side fault point ("staging_alloc", "fence_reserve", "launch", "launch_nth",
+    "ipc_open", "host_register"); count 0 disarms."""
     _check(_lib.kv_fault_inject(point.encode(), count))
 
 
