@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--workload", choices=["llama8b", "mla_fp8", "trtllm_ipc"], default="llama8b")
     p.add_argument("--mode", choices=["zero_copy", "staged", "copy_engine"], default="zero_copy")
     p.add_argument("--max-ctas", type=int, default=0)
+    p.add_argument("--staging-mib", type=int, default=0,
+                   help="STAGED mode: device staging buffer in MiB (0 = library default)")
     p.add_argument("--cta-threads", type=int, default=0, choices=[0, 256, 1024],
                    help="threads per CTA of host-link moves (0 = library default)")
     p.add_argument("--no-bulk", action="store_true",
@@ -314,7 +316,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     mode = {"zero_copy": kvb.KV_MODE_ZERO_COPY, "staged": kvb.KV_MODE_STAGED,
             "copy_engine": kvb.KV_MODE_COPY_ENGINE}[args.mode]
-    kvb.kv_config_set(mode, args.max_ctas, 0, (kvb.KV_CFG_NO_BULK if args.no_bulk else 0) |
+    kvb.kv_config_set(mode, args.max_ctas, args.staging_mib << 20,
+                      (kvb.KV_CFG_NO_BULK if args.no_bulk else 0) |
                       (kvb.KV_CFG_NO_PDL if args.no_pdl else 0), args.cta_threads)
 
     w = {"llama8b": wl.LLAMA8B, "mla_fp8": wl.MLA_FP8, "trtllm_ipc": wl.TRTLLM}[args.workload]
