@@ -83,3 +83,48 @@ def test_backup_put_get_restore_chain(wname):
         kvb.kv_l3_close(store)
         os.close(fd)
         rig.close()
+
+
+def test_prefetch_from_l3_then_gated_restore():
+    """The storage-prefetch flow: a RESTORE is enqueued first and waits on the
+    GPU for a ready word; a host thread gets the records from the L3 store into
+    the host slots and then sets the word; the restore then runs.  The pool
+    equals the oracle's restore of the records' pages."""
+    import threading
+    g = wl.LLAMA8B.geom.with_(P=40, L=4)
+    S, R, n = 16, 24, 6
+    pb = g.page_bytes
+    r = np.random.default_rng(9)
+    rig = Rig(g, S, seed=9)
+    fd = os.memfd_create("kvb_l3_prefetch")
+    records = np.random.default_rng(10).integers(0, 256, R * pb, dtype=np.uint8)
+    os.pwrite(fd, records.tobytes(), 0)
+    store = kvb.kv_l3_open(fd, 0, pb, R, 4)
+    word = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    try:
+        recs = r.permutation(R)[:n].astype(np.int32)
+        slots = r.permutation(S)[:n].astype(np.int32)
+        dst = r.permutation(g.P)[:n].astype(np.int32)
+        snap = rig.snapshot()
+        # expected: the slots hold the records, then the restore moves them
+        host_want = snap[1].copy()
+        oracle.l3_get(records, pb, recs, slots, host_want)
+        pool_want = snap[0].copy()
+        oracle.restore(oracle_geom(g), pool_want, host_want, slots, dst)
+        s = torch.cuda.Stream()
+        f = kvb.kv_restore_when_ready(rig.pool, rig.hostt, slots, dst, word.data_ptr(), 1,
+                                      30_000_000_000, -1, s.cuda_stream)
+
+        def prefetch():
+            kvb.kv_l3_get(store, rig.host.data_ptr(), S, recs, slots)
+            word[0] = 1                                  # host data landed: release the gate
+
+        th = threading.Thread(target=prefetch)
+        th.start()
+        th.join(60)
+        kvb.kv_fence_wait(f, 30_000_000_000)
+        rig.assert_equal((pool_want, host_want))
+    finally:
+        kvb.kv_l3_close(store)
+        os.close(fd)
+        rig.close()
