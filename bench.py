@@ -18,6 +18,7 @@ the timed region, and the CPU oracle timed on the host cores as a baseline.
 from __future__ import annotations
 
 import argparse
+import atexit
 import hashlib
 import json
 import os
@@ -145,9 +146,14 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            atexit.register(self._kill)   # an exception before stop() leaves no sampler behind
         except OSError:
             self.proc = None
         return self
+
+    def _kill(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
 
     def _read(self):
         for line in self.proc.stdout:
