@@ -103,3 +103,64 @@ def test_random_case_matches_the_oracle(case):
     finally:
         kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
         rig.close()
+
+
+@pytest.mark.parametrize("case", range(CASES // 2))
+def test_random_split_pool_case_matches_the_oracle(case):
+    """The same draws on a layer-first pool held as one device buffer per
+    (layer, component): compared through the contiguous pool those buffers
+    form ([L][C][P][T][H][B] cut at every (l, c))."""
+    r, g, _, op, mode, flags, threads, staging = draw(9000 + case)
+    g = wl.Geometry(L=g.L, C=g.C, P=g.P, T=g.T, H=g.H, B=g.B, order=wl.LAYER_FIRST,
+                    dev_heads=g.dev_heads, host_heads=g.host_heads)
+    if mode == kvb.KV_MODE_STAGED and g.C * g.T * g.H * g.B > staging // 4:
+        mode = kvb.KV_MODE_ZERO_COPY
+    S = int(r.integers(1, g.P + 3))
+    n = int(r.integers(0, min(g.P, S) + 1))
+    src = r.integers(0, g.P, n).astype(np.int32)
+    slots = r.permutation(S)[:n].astype(np.int32)
+    dst = r.permutation(g.P)[:n].astype(np.int32)
+    layer = int(r.integers(0, g.L))
+    chunk_bytes = g.P * g.T * g.H * g.B
+    bufs = [torch.empty(chunk_bytes, dtype=torch.uint8, device="cuda") for _ in range(g.L * g.C)]
+    for k, b in enumerate(bufs):
+        wl.fill_random_(b, 9500 + 10 * case + k)
+    host = torch.empty(S * g.page_bytes, dtype=torch.uint8, pin_memory=True)
+    wl.fill_random_(host, 9400 + case)
+    lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B, g.order, g.dev_heads, g.elem_bytes)
+    old = kvb.kv_config_get()
+    pool = kvb.kv_pool_register_split(lay, [b.data_ptr() for b in bufs])
+    tier = kvb.kv_host_register(host.data_ptr(), host.numel(), S, g.host_heads, lay)
+    og = oracle_geom(g)
+    try:
+        kvb.kv_config_set(mode, 0, staging, flags, threads)
+        torch.cuda.synchronize()
+        flat, hst = torch.cat(bufs).cpu().numpy(), host.numpy().copy()
+        if op in ("backup", "gather"):
+            if op == "backup":
+                oracle.backup(og, flat, hst, src, slots)
+                kvb.kv_fence_wait(kvb.kv_backup(pool, tier, src, slots), 20_000_000_000)
+            else:
+                buf = torch.zeros(max(1, n) * g.page_bytes, dtype=torch.uint8, device="cuda")
+                want_buf = np.zeros(buf.numel(), dtype=np.uint8)
+                oracle.backup(og, flat, want_buf, src, np.arange(n))
+                kvb.kv_fence_wait(kvb.kv_device_gather(pool, buf.data_ptr(), buf.numel(),
+                                                       g.host_heads, src), 20_000_000_000)
+                torch.cuda.synchronize()
+                assert np.array_equal(buf.cpu().numpy(), want_buf)
+        elif op == "restore_layers":
+            for l in range(g.L):
+                oracle.restore(og, flat, hst, slots, dst, layer=l)
+            for f in kvb.kv_restore_layers(pool, tier, slots, dst, 0, g.L):
+                kvb.kv_fence_wait(f, 20_000_000_000)
+        else:   # restore, restore_layer, scatter (as a one-layer restore from the tier)
+            lay_ = layer if op != "restore" else -1
+            oracle.restore(og, flat, hst, slots, dst, layer=lay_)
+            kvb.kv_fence_wait(kvb.kv_restore(pool, tier, slots, dst, lay_), 20_000_000_000)
+        torch.cuda.synchronize()
+        assert np.array_equal(torch.cat(bufs).cpu().numpy(), flat), "split pool"
+        assert np.array_equal(host.numpy(), hst), "host tier"
+    finally:
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+        kvb.kv_pool_close(pool)
+        kvb.kv_host_close(tier)
