@@ -1169,11 +1169,11 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
 }
 
 // Device gather (kind 0) / scatter (kind 1) between the pool and a caller's
-// device buffer in host-tier layout.  g_mu held.
+// device buffer in host-tier layout.  g_mu held.  fence == NULL: stream order
+// only -- no fence is reserved and the kernel skips the fused completion.
 kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t buf_heads, int kind,
                        const int32_t *pages, uint32_t n, int32_t layer, void *stream_v,
                        kv_fence *fence) {
-    if (fence == nullptr) return fail(KV_ERR_INVALID_ARG, "fence output pointer is NULL");
     if (pool_h == nullptr) return fail(KV_ERR_INVALID_ARG, "pool handle is NULL");
     PoolObj *pool = find_pool(pool_h);
     if (pool == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
@@ -1219,22 +1219,26 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
                   kernel);
         if (st != KV_OK) return st;
         FenceSlot fs;
-        st = reserve_fence(d, &fs);
-        if (st != KV_OK) return st;
+        if (fence != nullptr) {
+            st = reserve_fence(d, &fs);
+            if (st != KV_OK) return st;
+        }
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
         const int ctas = default_ctas(ds, false, kernel);
+        const DevState *fds = fence != nullptr ? &ds : nullptr;
+        const FenceSlot *ffs = fence != nullptr ? &fs : nullptr;
         if (kind == 0) {
-            st = run_moves(p, pages, nullptr, n, ctas, stream, true, &ds, &fs);
+            st = run_moves(p, pages, nullptr, n, ctas, stream, true, fds, ffs);
         } else {
             static thread_local std::vector<int32_t> idx;
             idx.resize(n);
             for (uint32_t k = 0; k < n; ++k) idx[k] = (int32_t)k;
-            st = run_moves(p, idx.data(), pages, n, ctas, stream, false, &ds, &fs);
+            st = run_moves(p, idx.data(), pages, n, ctas, stream, false, fds, ffs);
         }
-        if (st != KV_OK) return st;
+        if (st != KV_OK || fence == nullptr) return st;
         return commit_fence(d, fs, false, stream, fence);
     }
-    return issue_fence(d, stream, fence);
+    return fence != nullptr ? issue_fence(d, stream, fence) : KV_OK;
 }
 
 }  // namespace

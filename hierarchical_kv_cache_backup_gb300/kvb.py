@@ -333,23 +333,24 @@ def kv_restore(pool: int, host: int, host_slots, dst_pages, layer: int = -1, str
 
 
 def kv_device_gather(pool: int, buf: int, buf_bytes: int, buf_heads: int, src_pages,
-                     stream=None) -> int:
-    """Pool pages -> a device buffer in host-tier layout (HBM only); returns the fence."""
+                     stream=None, fence: bool = True) -> int:
+    """Pool pages -> a device buffer in host-tier layout (HBM only); returns the fence
+    (0 with fence=False: ordered by the stream only, no fence word)."""
     a, pa = _ids(src_pages)
     f = ctypes.c_uint64()
     _check(_lib.kv_device_gather(pool, buf, buf_bytes, buf_heads, pa, a.size, stream,
-                                 ctypes.byref(f)))
+                                 ctypes.byref(f) if fence else None))
     return f.value
 
 
 def kv_device_scatter(pool: int, buf: int, buf_bytes: int, buf_heads: int, dst_pages,
-                      layer: int = -1, stream=None) -> int:
+                      layer: int = -1, stream=None, fence: bool = True) -> int:
     """A device buffer in host-tier layout -> pool pages (every layer, or one); returns the
-    fence."""
+    fence (0 with fence=False: ordered by the stream only)."""
     a, pa = _ids(dst_pages)
     f = ctypes.c_uint64()
     _check(_lib.kv_device_scatter(pool, buf, buf_bytes, buf_heads, pa, a.size, layer, stream,
-                                  ctypes.byref(f)))
+                                  ctypes.byref(f) if fence else None))
     return f.value
 
 

@@ -317,7 +317,10 @@ KVB_API kv_status kv_restore_layers(kv_pool pool, kv_host host, const int32_t *h
  * kv_device_scatter: page dst_pages[i] <- item i (every layer, or only
  * `layer`).  Checks as kv_backup / kv_restore; buf must be 16-B aligned and
  * buf_bytes >= n x item bytes (OUT_OF_RANGE); DUPLICATE for a page written
- * twice by a scatter.  HBM-bound: one read and one write of every byte. */
+ * twice by a scatter.  HBM-bound: one read and one write of every byte.
+ * `fence` may be NULL: the op is then ordered only by `stream` (no fence is
+ * reserved and the kernel skips its fused completion, ~2% faster); with a
+ * fence it completes like a backup's. */
 KVB_API kv_status kv_device_gather(kv_pool pool, void *buf, uint64_t buf_bytes, uint32_t buf_heads,
                                    const int32_t *src_pages, uint32_t n, void *stream,
                                    kv_fence *fence);

@@ -715,3 +715,37 @@ def test_restore_layers_above_capacity_on_a_split_pool():
         kvb.kv_host_close(tier)
     finally:
         rig.close()
+
+
+def test_device_gather_scatter_without_a_fence():
+    """fence=NULL: the ops are ordered by their stream alone (no fence word, no
+    fused completion); a gather, a scatter of its result into other pages and a
+    second gather in one stream equal the oracle."""
+    g = wl.LLAMA8B.geom.with_(P=40, L=6)
+    n = 7
+    r = np.random.default_rng(12)
+    rig = Rig(g, 1, seed=12)
+    buf = torch.empty(n * g.page_bytes, dtype=torch.uint8, device="cuda")
+    buf2 = torch.empty_like(buf)
+    try:
+        src = r.permutation(g.P)[:n].astype(np.int32)
+        dst = np.setdiff1d(np.arange(g.P), src)[:n].astype(np.int32)
+        snap = rig.snapshot()
+        og = oracle_geom(g)
+        want_buf = np.zeros(buf.numel(), dtype=np.uint8)
+        oracle.backup(og, snap[0], want_buf, src, np.arange(n))
+        want_pool = snap[0].copy()
+        oracle.restore(og, want_pool, want_buf, np.arange(n), dst)
+        s = torch.cuda.Stream()
+        assert kvb.kv_device_gather(rig.pool, buf.data_ptr(), buf.numel(), 0, src,
+                                    s.cuda_stream, fence=False) == 0
+        kvb.kv_device_scatter(rig.pool, buf.data_ptr(), buf.numel(), 0, dst, -1, s.cuda_stream,
+                              fence=False)
+        kvb.kv_device_gather(rig.pool, buf2.data_ptr(), buf2.numel(), 0, dst, s.cuda_stream,
+                             fence=False)
+        s.synchronize()
+        assert np.array_equal(buf.cpu().numpy(), want_buf)
+        assert np.array_equal(buf2.cpu().numpy(), want_buf)     # the scattered pages read back
+        rig.assert_equal((want_pool, snap[1]))
+    finally:
+        rig.close()

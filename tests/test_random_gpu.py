@@ -87,8 +87,11 @@ def test_random_case_matches_the_oracle(case):
             if op == "gather":
                 want_buf = np.zeros(max(1, n) * pb, dtype=np.uint8)
                 oracle.backup(og, snap[0], want_buf, src, np.arange(n), pool_offset=offset)
-                kvb.kv_fence_wait(kvb.kv_device_gather(rig.pool, buf.data_ptr(), buf.numel(),
-                                                       g.host_heads, src), 20_000_000_000)
+                with_fence = case % 2 == 0             # odd cases: stream order only
+                f = kvb.kv_device_gather(rig.pool, buf.data_ptr(), buf.numel(), g.host_heads,
+                                         src, fence=with_fence)
+                if with_fence:
+                    kvb.kv_fence_wait(f, 20_000_000_000)
                 torch.cuda.synchronize()
                 assert np.array_equal(buf[:n * pb].cpu().numpy(), want_buf[:n * pb])
                 rig.assert_equal(snap)
@@ -97,9 +100,12 @@ def test_random_case_matches_the_oracle(case):
                 buf[:data.size].copy_(torch.from_numpy(data))
                 want = (snap[0].copy(), snap[1])
                 oracle.restore(og, want[0], data, np.arange(n), dst, pool_offset=offset)
-                kvb.kv_fence_wait(kvb.kv_device_scatter(rig.pool, buf.data_ptr(), buf.numel(),
-                                                        g.host_heads, dst), 20_000_000_000)
-                rig.assert_equal(want)
+                with_fence = case % 2 == 0
+                f = kvb.kv_device_scatter(rig.pool, buf.data_ptr(), buf.numel(), g.host_heads,
+                                          dst, fence=with_fence)
+                if with_fence:
+                    kvb.kv_fence_wait(f, 20_000_000_000)
+                rig.assert_equal(want)                 # (synchronizes the device)
     finally:
         kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
         rig.close()
