@@ -24,9 +24,12 @@
  *
  * Conventions for every call:
  *   - Status codes only.  Nothing aborts, throws or traps across this ABI.
- *     A call that returns an error has had no side effect: validation runs
- *     before anything is enqueued ([LMC] §发送端校验).  kv_last_error() gives
- *     a readable message (thread-local) for the last failing call.
+ *     A call rejected by validation (INVALID_ARG, OUT_OF_RANGE, DUPLICATE,
+ *     ALIGNMENT, LAYOUT, STALE, CLOSED) has had no side effect: validation
+ *     runs before anything is enqueued ([LMC] §发送端校验).  A CUDA call that
+ *     fails part-way through an op (CUDA) may leave the part already
+ *     enqueued to complete, inside the op's own targets.  kv_last_error()
+ *     gives a readable message (thread-local) for the last failing call.
  *   - Device pointers are plain CUDA device addresses; host pointers are
  *     plain host addresses.  Streams are cudaStream_t values passed as void*
  *     (NULL = the legacy default stream).
