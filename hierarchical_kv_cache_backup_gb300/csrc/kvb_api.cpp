@@ -865,6 +865,9 @@ kv_status stage_ids(DevState &s, const int32_t *a, const int32_t *b, uint32_t n,
                         stream);
     if (e == cudaSuccess) e = cudaEventRecord(s.gids_copied, stream);
     if (e != cudaSuccess) return cuda_fail(e, "copying the ids to the device");
+    // From here the next large restore waits for this copy (host buffer) and for
+    // gids_free, which the caller records after its launch, failed or not.
+    s.gids_used = true;
     return KV_OK;
 }
 
@@ -1026,12 +1029,22 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     FenceSlot fs;
     st = reserve_fence(d, &fs);
     if (st != KV_OK) return st;
-    if (ready != nullptr) {
+    // A gate on the stream records a give-up under the op's sequence number.  Once
+    // it is launched, a failure further on must not hand that number to the next
+    // op (whose moves the stale record would skip): the number is consumed.
+    bool gated = false;
+    auto gate = [&]() -> kv_status {
         cudaError_t e = launch_gate(ready, ready_value, ready_timeout_ns, ds.status_dev + fs.k,
                                     fs.seq, stream);
         if (e != cudaSuccess) return cuda_fail(e, "launch of the ready-fence gate");
         g_launches.fetch_add(1, std::memory_order_relaxed);
-    }
+        gated = true;
+        return KV_OK;
+    };
+    auto bail = [&](kv_status err) {
+        if (gated) g_next_seq = fs.seq + 1;
+        return err;
+    };
     bool fused = false;
 
     if (n > 0 && (g_cfg.mode == KV_MODE_ZERO_COPY || ready != nullptr)) {
@@ -1041,6 +1054,8 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                   /*iter_dst=*/backup, &p);
         if (st != KV_OK) return st;
         if (ready != nullptr) {
+            st = gate();
+            if (st != KV_OK) return st;
             p.d.skip_word = ds.status_dev + fs.k;
             p.d.skip_tag = fs.seq;
         }
@@ -1048,8 +1063,11 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
         st = run_moves(p, a, b, n, default_ctas(ds, true, PK_REG, p.threads), stream, false, &ds,
                        &fs);
-        if (st != KV_OK) return st;
+        if (st != KV_OK) return bail(st);
         fused = true;
+    } else if (ready != nullptr) {   // an empty gated op: its fence follows the gate
+        st = gate();
+        if (st != KV_OK) return st;
     } else if (n > 0 && g_cfg.mode == KV_MODE_COPY_ENGINE) {
         st = backup ? ce_copies(*pool, *host, true, a, b, n, nl, l0, stream)
                     : ce_copies(*pool, *host, false, b, a, n, nl, l0, stream);
@@ -1165,7 +1183,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
         ds.staging_used[half] = true;
     }
-    return commit_fence(d, fs, !fused, stream, fence);
+    return bail(commit_fence(d, fs, !fused, stream, fence));
 }
 
 // Device gather (kind 0) / scatter (kind 1) between the pool and a caller's
@@ -1579,6 +1597,21 @@ kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out) {
         if (it == g_maps.end()) cudaIpcCloseMemHandle(base);
         return fail(KV_ERR_ALIGNMENT, "imported pool start %p is not 16-byte aligned", (void *)start);
     }
+    {   // the descriptor's extent must lie inside the allocation the handle maps
+        uintptr_t ab = 0;
+        size_t as = 0;
+        DeviceGuard guard(device);
+        st = address_range(base, &ab, &as);
+        if (st == KV_OK && (desc->alloc_offset > as || desc->nbytes > as - desc->alloc_offset))
+            st = fail(KV_ERR_OUT_OF_RANGE, "descriptor extent (offset %llu + %llu bytes) overruns "
+                      "the imported allocation of %llu bytes",
+                      (unsigned long long)desc->alloc_offset, (unsigned long long)desc->nbytes,
+                      (unsigned long long)as);
+        if (st != KV_OK) {
+            if (it == g_maps.end()) cudaIpcCloseMemHandle(base);
+            return st;
+        }
+    }
     PoolObj *p = new (std::nothrow) PoolObj{g, desc->layout, start, desc->nbytes, device,
                                             desc->instance_id, desc->generation, true, key};
     if (p == nullptr) {
@@ -1731,23 +1764,9 @@ kv_status kv_backup_when_ready(kv_pool pool, kv_host host, const int32_t *src_pa
                                const int32_t *host_slots, uint32_t n, const uint64_t *ready_word,
                                uint64_t ready_value, uint64_t ready_timeout_ns, void *stream,
                                kv_fence *fence) {
-    if (ready_word == nullptr) return fail(KV_ERR_INVALID_ARG, "ready_word is NULL");
-    if (((uintptr_t)ready_word) % 8 != 0)
-        return fail(KV_ERR_ALIGNMENT, "ready_word %p is not 8-byte aligned", (const void *)ready_word);
-    if (ready_timeout_ns > kMaxReadyTimeoutNs)
-        return fail(KV_ERR_INVALID_ARG, "ready_timeout_ns %llu exceeds the %llu ns limit",
-                    (unsigned long long)ready_timeout_ns, (unsigned long long)kMaxReadyTimeoutNs);
-    cudaPointerAttributes attr;
-    cudaError_t e = cudaPointerGetAttributes(&attr, ready_word);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(ready_word)");
     const void *dev_word = nullptr;
-    if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged)
-        dev_word = ready_word;
-    else if (attr.type == cudaMemoryTypeHost)
-        dev_word = attr.devicePointer;
-    if (dev_word == nullptr)
-        return fail(KV_ERR_INVALID_ARG, "ready_word %p is not visible to the GPU (use device or "
-                    "pinned mapped host memory)", (const void *)ready_word);
+    kv_status st = ready_word_dev(ready_word, ready_timeout_ns, &dev_word);
+    if (st != KV_OK) return st;
     std::lock_guard<std::mutex> lk(g_mu);
     return issue(pool, host, 0, src_pages, host_slots, n, -1, stream, fence,
                  (const unsigned long long *)dev_word, ready_value, ready_timeout_ns);
@@ -1812,8 +1831,10 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
         // that one kernel still publishes every layer of the whole op in order
         const bool device_ids = st == KV_OK && n > p.max_items;
         if (st == KV_OK) st = plan_layer_major(p, n, ds, seq0, device_ids);
+        bool staged = false;
         if (st == KV_OK && device_ids) {
             st = stage_ids(ds, host_slots, dst_pages, n, stream);
+            staged = st == KV_OK;
             p.d.gid_a = ds.gids;
             p.d.gid_b = ds.gids + n;
         }
@@ -1822,10 +1843,9 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
                          : p.threads == kWideThreads ? std::min(kOverlapWideCtas, ds.sms)
                                                      : default_ctas(ds, true, PK_REG, p.threads);
         if (st == KV_OK) st = run_moves(p, host_slots, dst_pages, n, ctas, stream, false);
-        if (st == KV_OK && device_ids) {
+        if (staged) {   // the id buffers are busy up to here in stream order, launched or not
             cudaError_t e2 = cudaEventRecord(ds.gids_free, stream);
             if (e2 != cudaSuccess) return cuda_fail(e2, "cudaEventRecord(ids)");
-            ds.gids_used = true;
         }
         if (st != KV_OK) return st;
     } else {

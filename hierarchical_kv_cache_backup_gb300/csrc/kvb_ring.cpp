@@ -137,6 +137,16 @@ void bind(RingObj *o) {
     o->ops = (kv_ring_op *)(b + o->h->entry_off);
 }
 
+// The completion and entry regions of a header lie, in order and page-aligned,
+// between the header page and the end of the segment.
+bool regions_fit(const RingHeader *h) {
+    const uint64_t comp_end = h->comp_off + (uint64_t)h->slots * sizeof(CompRec);
+    const uint64_t entry_end = h->entry_off + (uint64_t)h->slots * sizeof(kv_ring_op);
+    return h->comp_off >= kPage && h->comp_off % kPage == 0 && h->entry_off % kPage == 0 &&
+           h->comp_off <= h->total_bytes && h->entry_off <= h->total_bytes &&
+           comp_end <= h->entry_off && entry_end <= h->total_bytes;
+}
+
 uint32_t slot_of(const RingObj *o, uint64_t t) { return (uint32_t)((t - 1) % o->h->slots); }
 
 // CPU completion of ticket t with status s (error record first, then done).
@@ -210,7 +220,7 @@ kv_status kv_ring_attach(const char *name, kv_ring *out) {
     RingHeader *h = (RingHeader *)base;
     if (__atomic_load_n(&h->magic, __ATOMIC_ACQUIRE) != kRingMagic || h->version != kRingVersion ||
         h->entry_bytes != sizeof(kv_ring_op) || h->total_bytes != (uint64_t)sb.st_size ||
-        h->slots < 2 || h->slots > kMaxSlots) {
+        h->slots < 2 || h->slots > kMaxSlots || !regions_fit(h)) {
         munmap(base, (size_t)sb.st_size);
         close(fd);
         return err(KV_ERR_INVALID_ARG, "segment is not a ring of this version");
@@ -304,12 +314,21 @@ kv_status kv_ring_pop(kv_ring r, uint64_t timeout_ns, kv_ring_op *op, uint64_t *
     }
     const kv_ring_op &e = o->ops[slot_of(o, t)];
     std::memcpy(op, &e, offsetof(kv_ring_op, a));
-    const uint32_t n = op->n <= KV_RING_MAX_IDS ? op->n : 0;
+    // The entry comes from another process's memory: a descriptor that
+    // kv_ring_submit would have refused is taken and failed here, not served.
+    const bool malformed = op->n > KV_RING_MAX_IDS || op->kind > KV_RING_OP_RESTORE;
+    const uint32_t n = malformed ? 0 : op->n;
     std::memcpy(op->a, e.a, n * sizeof(int32_t));
     std::memcpy(op->b, e.b, n * sizeof(int32_t));
     __atomic_store_n(&h->server_pid, (int64_t)getpid(), __ATOMIC_RELAXED);
     st(&h->head, t);   // the slot may now be refilled (after t completes)
     *ticket = t;
+    if (malformed) {
+        op->n = 0;
+        complete_cpu(o, t, KV_ERR_INVALID_ARG);
+        return err(KV_ERR_INVALID_ARG, "descriptor with an unknown kind or n above "
+                   "KV_RING_MAX_IDS: taken and completed with INVALID_ARG");
+    }
     return KV_OK;
 }
 
@@ -350,6 +369,10 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
         uint64_t t = 0;
         kv_status s = kv_ring_pop(r, k == 0 ? idle_timeout_ns : 0, &op, &t);
         if (s == KV_ERR_TIMEOUT) break;
+        if (s == KV_ERR_INVALID_ARG && t != 0) {   // malformed: already completed by pop
+            ++*served;
+            continue;
+        }
         if (s != KV_OK) return s;
         ++*served;
         if (op.pool_index >= npools) {

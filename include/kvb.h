@@ -203,7 +203,9 @@ KVB_API kv_status kv_pool_export(kv_pool pool, kv_ipc_desc *out);
  * peer access when the allocation is not yet mapped; pool = mapped base +
  * alloc_offset.  Must run in a process other than the exporter.  A
  * descriptor whose generation is below the retired floor of its instance is
- * refused with STALE.  Errors: INVALID_ARG, LAYOUT, ALIGNMENT, STALE, CUDA,
+ * refused with STALE; one whose extent (alloc_offset + nbytes) overruns the
+ * mapped allocation, with OUT_OF_RANGE (a mapping opened for it is closed
+ * again).  Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, STALE, CUDA,
  * NO_MEMORY. */
 KVB_API kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out);
 
@@ -397,7 +399,7 @@ typedef struct {
  * slots, name exists), NO_MEMORY. */
 KVB_API kv_status kv_ring_create(const char *name, uint32_t slots, kv_ring *out);
 /* Attaches to an existing ring.  Errors: INVALID_ARG (no such ring, wrong
- * magic or version). */
+ * magic or version, or a header whose regions do not fit the segment). */
 KVB_API kv_status kv_ring_attach(const char *name, kv_ring *out);
 /* Detaches (and unlinks, for the creator; unregisters the completion page
  * from CUDA, for a server).  Errors: CLOSED. */
@@ -425,7 +427,11 @@ KVB_API kv_status kv_ring_serve(kv_ring ring, const kv_pool *pools, uint32_t npo
                                 void *stream, uint32_t max_ops, uint64_t idle_timeout_ns,
                                 uint32_t *served);
 /* Server without a GPU (tests, or a server that moves bytes some other way):
- * takes the next descriptor (waiting up to timeout_ns; TIMEOUT if none) ... */
+ * takes the next descriptor (waiting up to timeout_ns; TIMEOUT if none) ...
+ * A descriptor that kv_ring_submit would refuse (unknown kind, n above
+ * KV_RING_MAX_IDS: written into the shared segment some other way) is taken,
+ * completed with INVALID_ARG and reported as INVALID_ARG with *ticket set and
+ * op->n = 0; kv_ring_serve counts it as served and moves on. */
 KVB_API kv_status kv_ring_pop(kv_ring ring, uint64_t timeout_ns, kv_ring_op *op,
                               uint64_t *ticket);
 /* ... and completes a ticket from the CPU with the given status. */
@@ -449,7 +455,11 @@ typedef struct kv_l3_s *kv_l3;
  * threads move the bytes (0 = 8, at most 64).  The file is not resized: a put
  * past its end grows it, a get past its end fails with KV_ERR_IO.  If the
  * caller opened fd with O_DIRECT, buffers, offsets and record_bytes must meet
- * its alignment or calls fail with KV_ERR_IO.
+ * its alignment or calls fail with KV_ERR_IO.  A regular file or memfd opened
+ * read-write without O_DIRECT is mapped once and calls copy through the
+ * mapping; other descriptors take one pwritev / preadv per run of records.
+ * While the store is open nobody else may shrink the file below a record in
+ * use: a mapped store touching a page past the end would take SIGBUS.
  * Errors: INVALID_ARG (fd not open / not a file or block device, zero sizes,
  * threads > 64), OUT_OF_RANGE (num_records > 2^31 or offsets overflow),
  * NO_MEMORY. */
@@ -460,7 +470,8 @@ KVB_API kv_status kv_l3_close(kv_l3 store);
 
 /* PUT: record records[i] <- host slot slots[i], for i < n.  Synchronous:
  * returns once every byte is written to the descriptor (no fsync).  Runs of
- * consecutive records go out as one pwritev each, spread over the workers.
+ * consecutive records go out as one copy (or one pwritev) each, spread over
+ * the workers.
  * Checks before any write: ids in range (slots < host_slots, records <
  * num_records), no record named twice.  The host slots must not be written
  * meanwhile (wait for the backup's fence first).
@@ -469,7 +480,7 @@ KVB_API kv_status kv_l3_close(kv_l3 store);
 KVB_API kv_status kv_l3_put(kv_l3 store, const void *host, uint64_t host_slots,
                             const int32_t *slots, const int32_t *records, uint32_t n);
 /* GET: host slot slots[i] <- record records[i], for i < n.  Synchronous; runs
- * of consecutive records come in as one preadv each.  Checks as for PUT, with
+ * of consecutive records come in as one copy (or one preadv) each.  Checks as for PUT, with
  * no slot named twice.  Restore from the slots only after this returns (or
  * gate the restore with kv_restore_when_ready on a word set afterwards).
  * Errors: CLOSED, INVALID_ARG, OUT_OF_RANGE, DUPLICATE (nothing read);

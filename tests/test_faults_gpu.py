@@ -194,3 +194,27 @@ def test_failure_in_the_middle_of_an_op_then_the_engine_recovers(mode, kind, n, 
         kvb.kv_fault_inject("launch_nth", 0)
         kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
         rig.close()
+
+
+def test_gated_op_failing_after_its_gate_does_not_poison_the_next_op(rig):
+    """A gated backup whose move launch fails after its gate was enqueued: the
+    gate still runs and, its ready word never arriving, records a give-up
+    under the op's sequence number.  That number must not pass to the next op:
+    the following gated backup, its ready word set, moves its pages exactly
+    and its fence reports success, not ABORTED."""
+    word = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+    snap = rig.snapshot()
+    kvb.kv_fault_inject("launch", 1)
+    with pytest.raises(kvb.KvError) as e:
+        kvb.kv_backup_when_ready(rig.pool, rig.hostt, [3, 9], [0, 5], word.data_ptr(), 1,
+                                 50_000_000)                   # 50 ms, never satisfied
+    assert e.value.status == kvb.KV_ERR_CUDA
+    torch.cuda.synchronize()                                   # the stale gate has given up
+    rig.assert_equal(snap)
+    word[0] = 1
+    want = rig.expect_backup(snap, [11, 4], [2, 6])
+    f = kvb.kv_backup_when_ready(rig.pool, rig.hostt, [11, 4], [2, 6], word.data_ptr(), 1,
+                                 1_000_000_000)
+    kvb.kv_fence_wait(f, 20_000_000_000)
+    assert kvb.kv_fence_query(f) == kvb.KV_OK
+    rig.assert_equal(want)

@@ -152,6 +152,22 @@ def test_exporter_exit_keeps_mapping_alive_and_generations():
                       pool_offset=desc.alloc_offset)
         assert np.array_equal(host.numpy(), want)
         kvb.kv_host_close(tier)
+        # a descriptor whose extent overruns the mapped allocation is refused, and
+        # the mapping the live pool holds is unaffected
+        far = kvb.desc_from_bytes(kvb.desc_to_bytes(desc))
+        far.alloc_offset = 1 << 40
+        big = kvb.desc_from_bytes(kvb.desc_to_bytes(desc))
+        big.layout.num_pages = 1 << 20
+        big.nbytes = (1 << 20) * g.page_bytes
+        for bad in (far, big):
+            with pytest.raises(kvb.KvError) as e:
+                kvb.kv_pool_import(bad)
+            assert e.value.status == kvb.KV_ERR_OUT_OF_RANGE, kvb.kv_last_error()
+        host.zero_()
+        tier = kvb.kv_host_register(host.data_ptr(), host.numel(), 4, 0, lay)
+        kvb.kv_fence_wait(kvb.kv_backup(pool, tier, [0, 17, 63, 5], [3, 2, 1, 0]), 30_000_000_000)
+        assert np.array_equal(host.numpy(), want)
+        kvb.kv_host_close(tier)
         # a newer generation of the same instance retires this one
         kvb.kv_pool_retire(99, 6)
         with pytest.raises(kvb.KvError) as e:

@@ -162,3 +162,62 @@ def test_argument_errors():
     with pytest.raises(kvb.KvError) as e:                         # unlinked by its creator
         kvb.kv_ring_attach(name)
     assert e.value.status == kvb.KV_ERR_INVALID_ARG
+
+
+def _shm_view(name):
+    import mmap
+    fd = os.open("/dev/shm" + name, os.O_RDWR)
+    try:
+        return mmap.mmap(fd, os.fstat(fd).st_size)
+    finally:
+        os.close(fd)
+
+
+def test_malformed_descriptor_in_shared_memory_is_failed_not_served():
+    """An entry kv_ring_submit would refuse (written into the segment directly)
+    is taken, completed with INVALID_ARG for the submitter, and reported to
+    the server with its ticket; the ring keeps working."""
+    import struct
+    name = ring_name()
+    sub = kvb.kv_ring_create(name, 4)
+    srv = kvb.kv_ring_attach(name)
+    m = _shm_view(name)
+    try:
+        slots, entry_bytes, _, entry_off = struct.unpack_from("<IIQQ", m, 8)
+        assert slots == 4
+        for field, value in ((8, kvb.KV_RING_MAX_IDS + 1), (0, 7)):   # n, then kind
+            t = kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [1], [2]))
+            struct.pack_into("<I", m, entry_off + ((t - 1) % slots) * entry_bytes + field, value)
+            with pytest.raises(kvb.KvError) as e:
+                kvb.kv_ring_pop(srv)
+            assert e.value.status == kvb.KV_ERR_INVALID_ARG
+            assert kvb.kv_ring_wait(sub, t) == kvb.KV_ERR_INVALID_ARG
+        t = kvb.kv_ring_submit(sub, kvb.make_ring_op(1, [5, 6], [7, 8], layer=-1))
+        t2, got = kvb.kv_ring_pop(srv)
+        assert t2 == t and got.n == 2 and list(got.a[:2]) == [5, 6]
+        kvb.kv_ring_complete(srv, t2, kvb.KV_OK)
+        assert kvb.kv_ring_wait(sub, t) == kvb.KV_OK
+    finally:
+        m.close()
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+
+
+def test_attach_refuses_a_header_whose_regions_overrun_the_segment():
+    import struct
+    name = ring_name()
+    sub = kvb.kv_ring_create(name, 4)
+    m = _shm_view(name)
+    try:
+        comp_off, entry_off, total = struct.unpack_from("<QQQ", m, 16)
+        for off, bad in ((16, total + 4096), (24, total), (24, comp_off)):
+            orig = struct.unpack_from("<Q", m, off)[0]
+            struct.pack_into("<Q", m, off, bad)
+            with pytest.raises(kvb.KvError) as e:
+                kvb.kv_ring_attach(name)
+            assert e.value.status == kvb.KV_ERR_INVALID_ARG
+            struct.pack_into("<Q", m, off, orig)
+        kvb.kv_ring_close(kvb.kv_ring_attach(name))               # intact again: attaches
+    finally:
+        m.close()
+        kvb.kv_ring_close(sub)
