@@ -162,9 +162,19 @@ _I32 = np.dtype(np.int32)
 def _ids(x):
     """An int32 C-contiguous view or copy of `x` and its address (None if empty).
     Arrays that already qualify pass through; the address comes from the buffer
-    protocol (cheaper than ndarray.ctypes on every call)."""
+    protocol (cheaper than ndarray.ctypes on every call).  Anything else is
+    converted only if it is a one-dimensional list of integers inside the int32
+    range: a wider id is refused, never wrapped into another page's id."""
     if type(x) is not np.ndarray or x.dtype != _I32 or not x.flags.c_contiguous:
-        x = np.ascontiguousarray(x, dtype=np.int32)
+        a = np.asarray(x)
+        if a.ndim > 1:
+            raise ValueError(f"ids must be one-dimensional, got shape {a.shape}")
+        if a.size:
+            if a.dtype.kind not in "iu":
+                raise TypeError(f"ids must be integers, got dtype {a.dtype}")
+            if a.dtype != _I32 and (int(a.min()) < -2**31 or int(a.max()) >= 2**31):
+                raise ValueError("ids outside the int32 range")
+        x = np.ascontiguousarray(a, dtype=np.int32).reshape(-1)
     if x.size == 0:
         return x, None
     try:
@@ -364,11 +374,13 @@ def kv_backup_staged_noalloc(pool: int, host: int, src_pages, host_slots, stream
 
 
 def kv_op_validate(layout: kv_layout, num_slots: int, kind: int, a, b, layer: int = -1) -> int:
-    """Returns the status (does not raise)."""
+    """Returns the library's status for the op (does not raise for it); id lists of
+    different lengths raise ValueError, as for the operations themselves."""
     a_, pa = _ids(a)
     b_, pb = _ids(b)
-    n = min(a_.size, b_.size)
-    return _lib.kv_op_validate(ctypes.byref(layout), num_slots, kind, pa, pb, n, layer)
+    if a_.size != b_.size:
+        raise ValueError("the two id lists differ in length")
+    return _lib.kv_op_validate(ctypes.byref(layout), num_slots, kind, pa, pb, a_.size, layer)
 
 
 # ------------------------------------------------------------------ fences

@@ -203,3 +203,22 @@ def test_fault_injection_points_without_gpu():
     kvb.kv_fault_inject("host_register", 0)
     for p in ("staging_alloc", "fence_reserve", "launch", "ipc_open", "launch_nth"):
         kvb.kv_fault_inject(p, 0)
+
+
+def test_id_lists_are_refused_rather_than_wrapped():
+    """The binding passes int32 ids; a wider id or a non-integer is refused,
+    never wrapped or truncated into another page's id."""
+    a, p = kvb._ids(np.array([3, 1, 2], dtype=np.int32))
+    assert p is not None and a.dtype == np.int32
+    b, _ = kvb._ids([5, 2**31 - 1, -1])                     # converted, in range
+    assert b.dtype == np.int32 and b.tolist() == [5, 2**31 - 1, -1]
+    c, pc = kvb._ids([])
+    assert c.size == 0 and pc is None
+    for bad, exc in (([2**31], ValueError), (np.array([2**32 + 5], np.int64), ValueError),
+                     ([-2**31 - 1], ValueError), ([1.0, 2.0], TypeError),
+                     (np.array([True]), TypeError), ([[1, 2]], ValueError)):
+        with pytest.raises(exc):
+            kvb._ids(bad)
+    lay = kvb.make_layout(2, 2, 64, 16, 2, 128)
+    with pytest.raises(ValueError):                         # before the C call
+        kvb.kv_op_validate(lay, 16, 0, [2**32 + 3], [0], -1)
