@@ -1,10 +1,11 @@
 """Builds the engine's shared library (libkvb.so) in-tree for sm_103a.
 
-Two translation units (the host engine and the kernels) compile in parallel
-with nvcc, then link into ``lib/libkvb.so`` with the CUDA runtime linked
-statically, so the library loads on a machine without a GPU and exports the
-C ABI of ``include/kvb.h``.  ``-Xptxas -v`` output of the kernels goes to
-``_build/ptxas.log`` (registers, spills, shared memory).
+The translation units (host engine, kernels, allocation-free backup,
+descriptor ring, L3 record store) compile in parallel with nvcc, then link
+into ``lib/libkvb.so`` with the CUDA runtime linked statically, so the library
+loads on a machine without a GPU and exports the C ABI of ``include/kvb.h``.
+``-Xptxas -v`` output of each ``.cu`` file goes to
+``_build/<file>.ptxas.log`` (registers, spills, shared memory).
 """
 from __future__ import annotations
 
