@@ -761,6 +761,57 @@ def run_ours(args):
                    "backup_us_median": round(1e6 * statistics.median(lat_b), 1),
                    "restore_us_median": round(1e6 * statistics.median(lat_r), 1),
                    "backup_us_p99": round(1e6 * sorted(lat_b)[int(0.99 * len(lat_b))], 1)}
+        # ---- descriptor ring round trip (submit -> ticket complete) for the same
+        # tiny backups, served by a host thread (kv_ring_serve: pop, validate,
+        # launch, GPU completion) and by the GPU-resident server
+        # (kv_ring_serve_device: no host thread, no launch per descriptor)
+        ring_lat = {}
+        iters = 400
+        ops = [kvb.make_ring_op(0, srcs[i % 4], slot_sets[i % 2], operation_id=i)
+               for i in range(iters)]
+        for kind in ("host", "device"):
+            name = f"/kvbbench_{os.getpid()}_{kind}"
+            sub = kvb.kv_ring_create(name, 64)
+            srv = kvb.kv_ring_attach(name)
+            rs = torch.cuda.Stream(device=dev)
+            stop = threading.Event()
+            served = [0]
+
+            def serve_loop():
+                while not stop.is_set() and served[0] < iters:
+                    served[0] += kvb.kv_ring_serve(srv, [tpool], ttier, rs.cuda_stream, 64,
+                                                   200_000_000)
+
+            th, fence = None, None
+            if kind == "host":
+                th = threading.Thread(target=serve_loop, daemon=True)
+                th.start()
+            else:
+                fence = kvb.kv_ring_serve_device(srv, [tpool], ttier, rs.cuda_stream, iters,
+                                                 2_000_000_000)
+            lat = []
+            for i in range(iters):
+                t0 = time.perf_counter()
+                tk = kvb.kv_ring_submit(sub, ops[i])
+                st = kvb.kv_ring_wait(sub, tk, 10_000_000_000)
+                lat.append(time.perf_counter() - t0)
+                if st != kvb.KV_OK:
+                    raise RuntimeError(f"ring {kind} op {i}: status {st}")
+            if fence is not None:
+                kvb.kv_fence_wait(fence, 30_000_000_000)
+            stop.set()
+            if th is not None:
+                th.join(10)
+            rs.synchronize()
+            kvb.kv_ring_close(srv)
+            kvb.kv_ring_close(sub)
+            lat = lat[50:]
+            ring_lat[f"{kind}_served_us_median"] = round(1e6 * statistics.median(lat), 1)
+            ring_lat[f"{kind}_served_us_p99"] = round(1e6 * sorted(lat)[int(0.99 * len(lat))], 1)
+        ring_lat["workload"] = ("tiny: 8 pages x 16 KiB (128 KiB) backup per descriptor, submit "
+                                "to ticket complete on the host clock, one descriptor in flight, "
+                                "4 page sets in rotation, L2 warm")
+        latency["ring_round_trip"] = ring_lat
         kvb.kv_pool_close(tpool)
         kvb.kv_host_close(ttier)
         del talloc, thost

@@ -1,7 +1,7 @@
 """Builds the engine's shared library (libkvb.so) in-tree for sm_103a.
 
 The translation units (host engine, kernels, allocation-free backup,
-descriptor ring, L3 record store) compile in parallel with nvcc, then link
+descriptor ring and its resident server kernel, L3 record store) compile in parallel with nvcc, then link
 into ``lib/libkvb.so`` with the CUDA runtime linked statically, so the library
 loads on a machine without a GPU and exports the C ABI of ``include/kvb.h``.
 ``-Xptxas -v`` output of each ``.cu`` file goes to
@@ -22,8 +22,10 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libkvb.so")
 
-SOURCES = ["kvb_api.cpp", "kvb_kernels.cu", "kvb_noalloc.cu", "kvb_ring.cpp", "kvb_l3.cpp"]
-HEADERS = [os.path.join(CSRC, "kvb_internal.h"), os.path.join(INCLUDE, "kvb.h")]
+SOURCES = ["kvb_api.cpp", "kvb_kernels.cu", "kvb_noalloc.cu", "kvb_ring.cpp", "kvb_ring_kernels.cu",
+           "kvb_l3.cpp"]
+HEADERS = [os.path.join(CSRC, "kvb_internal.h"), os.path.join(CSRC, "kvb_ring_internal.h"),
+           os.path.join(INCLUDE, "kvb.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-Xcompiler", "-fvisibility=hidden",

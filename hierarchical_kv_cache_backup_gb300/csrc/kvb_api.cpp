@@ -13,6 +13,7 @@
 //         §发送端校验, §重建生命周期与引用计数, §为什么不做_share_cuda_回退.
 #include "kvb.h"
 #include "kvb_internal.h"
+#include "kvb_ring_internal.h"
 
 #include <cuda.h>   // CUresult / CUdeviceptr types only; the function comes from the runtime
 #include <cuda_runtime.h>
@@ -315,6 +316,11 @@ kv_status init_device(int d) {
     DevState &s = g_dev[d];
     if (s.init) return KV_OK;
     DeviceGuard guard(d);
+    // every kernel loaded before the first launch: a lazy load behind a waiting
+    // kernel (gate, resident server) would wait for that kernel to end
+    cudaError_t e0 = preload_kernels();
+    if (e0 == cudaSuccess) e0 = preload_ring_kernels();
+    if (e0 != cudaSuccess) return cuda_fail(e0, "loading the library's kernels");
     // mapped pinned table: kRing fence words, kRing status words, the error word
     const size_t table = 2 * kRing * sizeof(unsigned long long) + 64;
     void *mem = nullptr;
@@ -1273,6 +1279,81 @@ int pool_device_of(const void *pool_handle, int *device) {
     if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
     *device = p->device;
     return KV_OK;
+}
+
+int ring_server_view(const kv_pool *pools, uint32_t npools, kv_host host_h, RingPoolK *table,
+                     Side *host_side_out, uint32_t *num_slots, int *device) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (npools == 0 || pools == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "a resident server needs at least one pool");
+    if (host_h == nullptr) return fail(KV_ERR_INVALID_ARG, "host handle is NULL");
+    HostObj *host = find_host(host_h);
+    if (host == nullptr) return fail(KV_ERR_CLOSED, "host handle is closed or unknown");
+    int dev = -1;
+    for (uint32_t i = 0; i < npools; ++i) {
+        PoolObj *p = pools[i] != nullptr ? find_pool(pools[i]) : nullptr;
+        if (p == nullptr) return fail(KV_ERR_CLOSED, "pool %u of the table is closed or unknown", i);
+        auto fl = g_floor.find(p->instance_id);
+        if (fl != g_floor.end() && p->generation < fl->second)
+            return fail(KV_ERR_STALE, "pool %u: generation %llu of instance %llu is retired", i,
+                        (unsigned long long)p->generation, (unsigned long long)p->instance_id);
+        if (!same_slot_geometry(p->g, host->g))
+            return fail(KV_ERR_LAYOUT, "pool %u and the host tier have different page geometry", i);
+        if (dev >= 0 && p->device != dev)
+            return fail(KV_ERR_INVALID_ARG, "the pools of one server live on different devices");
+        dev = p->device;
+        const Geo &g = p->g;
+        RingPoolK &k = table[i];
+        k = RingPoolK{};
+        k.pool = pool_side(*p);
+        k.L = (uint32_t)g.L;
+        k.C = (uint32_t)g.C;
+        k.P = (uint32_t)std::min<uint64_t>(g.P, 0xffffffffull);
+        k.H = (uint32_t)g.H;
+        k.T = (uint32_t)g.T;
+        k.B16 = (uint32_t)(g.B / 16);
+        k.cb16 = (uint32_t)(g.cb / 16);
+        k.segs = (k.cb16 + kSegPieces - 1) / kSegPieces;
+        // the segments of the largest descriptor (every id, every layer) must count in 32 bits
+        if ((uint64_t)KV_RING_MAX_IDS * g.L * g.C * k.segs > 0xffffffffull)
+            return fail(KV_ERR_LAYOUT, "pool %u: a descriptor of %d pages would need more than "
+                        "2^32 warp segments", i, KV_RING_MAX_IDS);
+        k.transpose = (g.heads != host->heads && g.H > 1 && g.T > 1) ? 1u : 0u;
+        k.div_segs = make_fastdiv(k.segs);
+        k.div_lc_all = make_fastdiv(k.L * k.C);
+        k.div_lc_one = make_fastdiv(k.C);
+        k.div_c = make_fastdiv(k.C);
+        k.div_b16 = make_fastdiv(k.B16);
+        k.div_T = make_fastdiv(k.T);
+        k.div_H = make_fastdiv(k.H);
+    }
+    // The fence state must exist before the resident kernel is launched: creating
+    // it (pinned allocation, memset) would wait for that kernel to end.
+    {
+        DeviceGuard guard(dev);
+        kv_status st = init_device(dev);
+        if (st != KV_OK) return st;
+    }
+    *host_side_out = host_side(*host);
+    *num_slots = host->num_slots;
+    *device = dev;
+    return KV_OK;
+}
+
+int ring_launch_server(int device, const RingKDesc &k, int ctas, cudaStream_t stream,
+                       kv_fence *fence) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceGuard guard(device);
+    kv_status st = init_device(device);
+    if (st != KV_OK) return st;
+    // the fence's slot (and its event) before the launch, its marker after
+    FenceSlot fs;
+    st = reserve_fence(device, &fs);
+    if (st != KV_OK) return st;
+    cudaError_t e = launch_ring_server(k, ctas, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "launch of the resident ring server");
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return commit_fence(device, fs, true, stream, fence);
 }
 
 int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_handle,

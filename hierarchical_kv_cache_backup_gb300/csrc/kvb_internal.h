@@ -112,6 +112,9 @@ struct IdsT {
 };
 using MoveIds = IdsT<kMaxItems>;
 
+// Loads every kernel of this file on the current device (lazy loading would
+// load each at its first launch, waiting for the device to go idle).
+cudaError_t preload_kernels();
 // Launch the gather/scatter kernel on `stream` with `ctas` CTAs of `threads`
 // threads (kMoveThreads or kWideThreads).
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int threads,

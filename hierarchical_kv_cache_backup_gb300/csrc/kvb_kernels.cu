@@ -696,6 +696,41 @@ cudaError_t launch_tsp(const MoveDesc &d, const MoveIds &ids, int ctas, cudaStre
     return launch_tsp_cap<kMaxItems>(d, ids, ctas, stream);
 }
 
+// Lazy loading (the CUDA default) loads a kernel's code at its first launch,
+// and the load waits for the device to go idle: a first launch queued behind a
+// kernel that waits -- a ready-fence gate, a resident ring server -- would
+// stall until that wait ends.  Every kernel here is loaded once, up front.
+cudaError_t preload_kernels() {
+    cudaFuncAttributes a;
+    const void *const fns[] = {
+        (const void *)kv_move_kernel<false, 64, kMoveThreads>,
+        (const void *)kv_move_kernel<false, 512, kMoveThreads>,
+        (const void *)kv_move_kernel<false, kMaxItems, kMoveThreads>,
+        (const void *)kv_move_kernel<true, 64, kMoveThreads>,
+        (const void *)kv_move_kernel<true, 512, kMoveThreads>,
+        (const void *)kv_move_kernel<true, kMaxItems, kMoveThreads>,
+        (const void *)kv_move_kernel<false, 64, kWideThreads>,
+        (const void *)kv_move_kernel<false, 512, kWideThreads>,
+        (const void *)kv_move_kernel<false, kMaxItems, kWideThreads>,
+        (const void *)kv_move_kernel<true, 64, kWideThreads>,
+        (const void *)kv_move_kernel<true, 512, kWideThreads>,
+        (const void *)kv_move_kernel<true, kMaxItems, kWideThreads>,
+        (const void *)kv_bulk_kernel<64>,
+        (const void *)kv_bulk_kernel<512>,
+        (const void *)kv_bulk_kernel<kMaxItems>,
+        (const void *)kv_tsp_kernel<64>,
+        (const void *)kv_tsp_kernel<512>,
+        (const void *)kv_tsp_kernel<kMaxItems>,
+        (const void *)kv_mark_kernel,
+        (const void *)kv_gate_kernel,
+    };
+    for (const void *f : fns) {
+        const cudaError_t e = cudaFuncGetAttributes(&a, f);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_move(const MoveDesc &d, const MoveIds &ids, int ctas, int threads,
                         cudaStream_t stream) {
     (void)cudaGetLastError();   // report this launch's error, not an earlier call's

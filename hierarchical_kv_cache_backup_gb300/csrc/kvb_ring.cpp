@@ -19,10 +19,13 @@
 // for ticket t only when t - slots has been taken and completed.
 #include "kvb.h"
 #include "kvb_internal.h"
+#include "kvb_ring_internal.h"
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cerrno>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <ctime>
@@ -52,16 +55,10 @@ struct RingHeader {
 };
 static_assert(sizeof(RingHeader) <= kPage, "ring header fits one page");
 
-// done: written by the GPU (or the CPU) when ticket `done` is complete.
-// err_ticket / err: written by the CPU, before done, when a ticket failed.
-struct CompRec {
-    uint64_t done;
-    uint64_t err_ticket;
-    int32_t err;
-    int32_t pad;
-    uint64_t pad2;
-};
-static_assert(sizeof(CompRec) == 32, "completion record size");
+// Completion records (kvb::CompRec): `done` is written by the GPU (or the CPU)
+// when ticket `done` is complete; err_ticket / err before it when it failed.
+using kvb::CompRec;
+constexpr uint32_t kMaxServerPools = 64;
 
 struct RingObj {
     std::string name;
@@ -73,8 +70,17 @@ struct RingObj {
     CompRec *comp;
     kv_ring_op *ops;
     std::mutex mu;                  // one submitter / one server thread at a time
-    CompRec *comp_dev = nullptr;    // device view once registered by a server
+    char *seg_dev = nullptr;        // device view of the whole segment once a server registered it
+    CompRec *comp_dev = nullptr;    // device view of the completion records
     bool registered = false;
+    // GPU-resident server (kv_ring_serve_device): scratch on its device
+    int srv_device = -1;
+    kvb::RingCtl *srv_ctl = nullptr;
+    int32_t *srv_ids = nullptr;
+    kvb::RingPoolK *srv_pools = nullptr;
+    uint32_t *srv_result = nullptr;       // mapped pinned: served, status
+    uint32_t *srv_result_dev = nullptr;
+    kv_fence srv_fence = 0;               // completes when the last resident server ended
 };
 
 std::mutex g_rings_mu;
@@ -145,6 +151,25 @@ bool regions_fit(const RingHeader *h) {
     return h->comp_off >= kPage && h->comp_off % kPage == 0 && h->entry_off % kPage == 0 &&
            h->comp_off <= h->total_bytes && h->entry_off <= h->total_bytes &&
            comp_end <= h->entry_off && entry_end <= h->total_bytes;
+}
+
+// The whole segment becomes device-visible (once): the GPU stores each
+// ticket into its completion record, and a resident server reads the header
+// and the entries too.
+kv_status register_segment(RingObj *o) {
+    if (o->registered) return KV_OK;
+    cudaError_t e = cudaHostRegister(o->base, o->bytes,
+                                     cudaHostRegisterMapped | cudaHostRegisterPortable);
+    void *dv = nullptr;
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dv, o->base, 0);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return err(KV_ERR_CUDA, "registering the ring segment with CUDA failed");
+    }
+    o->seg_dev = (char *)dv;
+    o->comp_dev = (CompRec *)(o->seg_dev + o->h->comp_off);
+    o->registered = true;
+    return KV_OK;
 }
 
 uint32_t slot_of(const RingObj *o, uint64_t t) { return (uint32_t)((t - 1) % o->h->slots); }
@@ -242,9 +267,19 @@ kv_status kv_ring_close(kv_ring r) {
         g_rings.erase(it);
     }
     kv_status s = KV_OK;
-    if (o->registered && cudaHostUnregister(o->comp) != cudaSuccess) {
+    if (o->srv_fence != 0 && kv_fence_wait(o->srv_fence, 120ull * 1000 * 1000 * 1000) == KV_ERR_TIMEOUT)
+        s = err(KV_ERR_TIMEOUT, "a resident server of this ring was still running at close");
+    if (o->srv_ctl != nullptr) {   // one allocation: control block, ids, pool table
+        int prev = -1;
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != o->srv_device) cudaSetDevice(o->srv_device);
+        cudaFree(o->srv_ctl);
+        if (prev >= 0 && prev != o->srv_device) cudaSetDevice(prev);
+    }
+    if (o->srv_result != nullptr) cudaFreeHost(o->srv_result);
+    if (o->registered && cudaHostUnregister(o->base) != cudaSuccess) {
         (void)cudaGetLastError();
-        s = err(KV_ERR_CUDA, "cudaHostUnregister of the completion page failed");
+        s = err(KV_ERR_CUDA, "cudaHostUnregister of the ring segment failed");
     }
     munmap(o->base, o->bytes);
     close(o->fd);
@@ -349,21 +384,8 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
     if (served == nullptr || (npools > 0 && pools == nullptr))
         return err(KV_ERR_INVALID_ARG, "NULL argument");
     *served = 0;
-    if (!o->registered) {
-        // The completion records become device-visible: the GPU stores each
-        // ticket there itself once its operation is complete.
-        const size_t bytes = round_page(o->h->slots * sizeof(CompRec));
-        cudaError_t e = cudaHostRegister(o->comp, bytes,
-                                         cudaHostRegisterMapped | cudaHostRegisterPortable);
-        void *dv = nullptr;
-        if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dv, o->comp, 0);
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();
-            return err(KV_ERR_CUDA, "registering the ring's completion page with CUDA failed");
-        }
-        o->comp_dev = (CompRec *)dv;
-        o->registered = true;
-    }
+    kv_status rs = register_segment(o);
+    if (rs != KV_OK) return rs;
     static thread_local kv_ring_op op;
     for (uint32_t k = 0; k < max_ops; ++k) {
         uint64_t t = 0;
@@ -403,6 +425,123 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
             complete_cpu(o, t, KV_ERR_CUDA);
         }
     }
+    return KV_OK;
+}
+
+kv_status kv_ring_serve_device(kv_ring r, const kv_pool *pools, uint32_t npools, kv_host host,
+                               void *stream, uint32_t max_ops, uint64_t idle_timeout_ns,
+                               kv_fence *fence) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (fence == nullptr) return err(KV_ERR_INVALID_ARG, "fence output pointer is NULL");
+    if (npools > kMaxServerPools) return err(KV_ERR_INVALID_ARG, "more than 64 pools");
+    if (idle_timeout_ns > 60ull * 1000 * 1000 * 1000)
+        return err(KV_ERR_INVALID_ARG, "idle_timeout_ns exceeds the 60 s limit");
+    kvb::RingPoolK table[kMaxServerPools];
+    kvb::Side host_side;
+    uint32_t num_slots = 0;
+    int device = -1;
+    kv_status st = (kv_status)kvb::ring_server_view(pools, npools, host, table, &host_side,
+                                                    &num_slots, &device);
+    if (st != KV_OK) return st;
+    std::lock_guard<std::mutex> lk(o->mu);
+    if (o->srv_fence != 0 && kv_fence_query(o->srv_fence) == KV_ERR_TIMEOUT)
+        return err(KV_ERR_INVALID_ARG, "a resident server is still running on this ring");
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != device) cudaSetDevice(device);
+    struct Restore {
+        int prev, device;
+        ~Restore() {
+            if (prev >= 0 && prev != device) cudaSetDevice(prev);
+        }
+    } restore{prev, device};
+    // Everything that may synchronize with the device (registration, allocations)
+    // happens before the launch: afterwards it would wait for the server to end.
+    st = register_segment(o);
+    if (st != KV_OK) return st;
+    auto ck = [](cudaError_t e, const char *what) {
+        if (e == cudaSuccess) return KV_OK;
+        (void)cudaGetLastError();
+        return err(KV_ERR_CUDA, what);
+    };
+    if (o->srv_ctl != nullptr && o->srv_device != device) {   // scratch of another device
+        cudaSetDevice(o->srv_device);
+        cudaFree(o->srv_ctl);
+        cudaSetDevice(device);
+        o->srv_ctl = nullptr;
+    }
+    const size_t ids_off = 256, pools_off = ids_off + 2 * KV_RING_MAX_IDS * sizeof(int32_t);
+    static_assert(sizeof(kvb::RingCtl) <= 256, "control block fits its slot");
+    if (o->srv_ctl == nullptr) {
+        void *p = nullptr;
+        st = ck(cudaMalloc(&p, pools_off + kMaxServerPools * sizeof(kvb::RingPoolK)),
+                "cudaMalloc of the resident server's scratch failed");
+        if (st != KV_OK) return st;
+        o->srv_ctl = (kvb::RingCtl *)p;
+        o->srv_ids = (int32_t *)((char *)p + ids_off);
+        o->srv_pools = (kvb::RingPoolK *)((char *)p + pools_off);
+        o->srv_device = device;
+    }
+    if (o->srv_result == nullptr) {
+        void *h = nullptr, *d = nullptr;
+        st = ck(cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable),
+                "cudaHostAlloc of the resident server's result words failed");
+        if (st != KV_OK) return st;
+        st = ck(cudaHostGetDevicePointer(&d, h, 0), "mapping the result words failed");
+        if (st != KV_OK) {
+            cudaFreeHost(h);
+            return st;
+        }
+        o->srv_result = (uint32_t *)h;
+        o->srv_result_dev = (uint32_t *)d;
+    }
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    const int ctas = std::max(1, std::min(kvb::kRingCtas, sms));
+    cudaStream_t s = (cudaStream_t)stream;
+    o->srv_result[0] = 0;
+    o->srv_result[1] = (uint32_t)KV_OK;
+    st = ck(cudaMemcpyAsync(o->srv_pools, table, npools * sizeof(kvb::RingPoolK),
+                            cudaMemcpyHostToDevice, s), "copying the pool table failed");
+    if (st == KV_OK)
+        st = ck(cudaMemsetAsync(o->srv_ctl, 0, sizeof(kvb::RingCtl), s),
+                "zeroing the control block failed");
+    if (st != KV_OK) return st;
+    kvb::RingKDesc k{};
+    k.tail = (const unsigned long long *)(o->seg_dev + offsetof(RingHeader, tail));
+    k.head = (unsigned long long *)(o->seg_dev + offsetof(RingHeader, head));
+    k.server_pid = (long long *)(o->seg_dev + offsetof(RingHeader, server_pid));
+    k.ops = (const kv_ring_op *)(o->seg_dev + o->h->entry_off);
+    k.comp = o->comp_dev;
+    k.slots = o->h->slots;
+    k.max_ops = max_ops;
+    k.first_ticket = ld(&o->h->head) + 1;
+    k.idle_ns = idle_timeout_ns;
+    k.pid = (long long)getpid();
+    k.host = host_side;
+    k.num_slots = num_slots;
+    k.npools = npools;
+    k.pools = o->srv_pools;
+    k.ctl = o->srv_ctl;
+    k.ids = o->srv_ids;
+    k.result = o->srv_result_dev;
+    st = (kv_status)kvb::ring_launch_server(device, k, ctas, s, fence);
+    if (st != KV_OK) return st;
+    o->srv_fence = *fence;
+    return KV_OK;
+}
+
+kv_status kv_ring_device_result(kv_ring r, uint32_t *served, kv_status *status) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (served == nullptr || status == nullptr) return err(KV_ERR_INVALID_ARG, "NULL argument");
+    std::lock_guard<std::mutex> lk(o->mu);
+    if (o->srv_fence == 0) return err(KV_ERR_INVALID_ARG, "no resident server was started");
+    if (kv_fence_query(o->srv_fence) == KV_ERR_TIMEOUT)
+        return err(KV_ERR_TIMEOUT, "the resident server is still running");
+    *served = __atomic_load_n(&o->srv_result[0], __ATOMIC_ACQUIRE);
+    *status = (kv_status)__atomic_load_n(&o->srv_result[1], __ATOMIC_ACQUIRE);
     return KV_OK;
 }
 

@@ -50,7 +50,8 @@ EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_p
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
            "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
            "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
-           "kv_ring_pop", "kv_ring_complete", "kv_fault_inject", "kv_l3_open", "kv_l3_close",
+           "kv_ring_pop", "kv_ring_complete", "kv_ring_serve_device", "kv_ring_device_result",
+           "kv_fault_inject", "kv_l3_open", "kv_l3_close",
            "kv_l3_put", "kv_l3_get")
 
 
@@ -135,6 +136,8 @@ def _load():
         "kv_ring_serve": (st, [vp, P(vp), u32, vp, vp, u32, u64, P(u32)]),
         "kv_ring_pop": (st, [vp, u64, P(kv_ring_op), P(u64)]),
         "kv_ring_complete": (st, [vp, u64, ctypes.c_int]),
+        "kv_ring_serve_device": (st, [vp, P(vp), u32, vp, vp, u32, u64, P(u64)]),
+        "kv_ring_device_result": (st, [vp, P(u32), P(ctypes.c_int)]),
         "kv_fault_inject": (st, [ctypes.c_char_p, u32]),
         "kv_l3_open": (st, [ctypes.c_int, u64, u64, u64, u32, P(vp)]),
         "kv_l3_close": (st, [vp]),
@@ -512,6 +515,25 @@ def kv_ring_pop(ring: int, timeout_ns: int = 1_000_000_000):
 def kv_ring_complete(ring: int, ticket: int, status: int = KV_OK) -> None:
     """Completes a ticket from the CPU with a status (server side)."""
     _check(_lib.kv_ring_complete(ring, ticket, status))
+
+
+def kv_ring_serve_device(ring: int, pools, host: int, stream=None, max_ops: int = 1,
+                         idle_timeout_ns: int = 1_000_000_000) -> int:
+    """Starts the GPU-resident server on `stream`: it takes and moves up to `max_ops`
+    descriptors (ending after `idle_timeout_ns` without one); returns the fence that completes
+    when it has ended."""
+    arr = (ctypes.c_void_p * max(1, len(pools)))(*pools)
+    f = ctypes.c_uint64()
+    _check(_lib.kv_ring_serve_device(ring, arr, len(pools), host, stream, max_ops,
+                                     idle_timeout_ns, ctypes.byref(f)))
+    return f.value
+
+
+def kv_ring_device_result(ring: int):
+    """(descriptors taken, server status) of the last resident server, once it has ended."""
+    n, s = ctypes.c_uint32(), ctypes.c_int()
+    _check(_lib.kv_ring_device_result(ring, ctypes.byref(n), ctypes.byref(s)))
+    return n.value, s.value
 
 
 # ------------------------------------------------------- L3 record store

@@ -437,6 +437,37 @@ KVB_API kv_status kv_ring_pop(kv_ring ring, uint64_t timeout_ns, kv_ring_op *op,
 /* ... and completes a ticket from the CPU with the given status. */
 KVB_API kv_status kv_ring_complete(kv_ring ring, uint64_t ticket, kv_status op_status);
 
+/* Server on the GPU ([RFC] §Device IPC data path: a high-frequency path as an
+ * NVMe-style submission / completion queue).  Enqueues on `stream` one
+ * resident kernel (a cooperative grid of 32 CTAs of 256 threads, holding 32
+ * SMs for as long as it runs) that takes
+ * descriptors from the ring itself -- polling the tail in the shared segment,
+ * which is mapped into the GPU -- checks each exactly as kv_ring_serve would
+ * (the same status for every rejected descriptor: INVALID_ARG for a kind, n,
+ * pool index or backup layer it refuses, then OUT_OF_RANGE / DUPLICATE for
+ * layers and ids in the host engine's order), moves the accepted ones
+ * zero-copy in ticket order, and completes every ticket from the GPU.  No host
+ * thread and no launch per descriptor.  The server ends after max_ops
+ * descriptors, or once idle_timeout_ns (<= 60 s) pass without a new one;
+ * every other wait inside it is bounded too.  Returns at once; *fence
+ * completes when the kernel has ended (then kv_ring_device_result).  The
+ * table (<= 64 pools, one device) and host tier are checked when it starts:
+ * live handles, no retired generation, the host tier's slot geometry; a
+ * generation retired while it runs is not seen.  One server per ring at a
+ * time (host or device); INVALID_ARG while this ring's previous resident
+ * server is still running.  The pool table and host tier must stay open, and
+ * the caller's stream is busy, until the fence completes.  While it runs, a
+ * CUDA call that synchronizes the device (cudaDeviceSynchronize, cudaFree,
+ * pinned allocations, ...) waits for the server to end.  Errors: CLOSED,
+ * INVALID_ARG, STALE, LAYOUT, CUDA. */
+KVB_API kv_status kv_ring_serve_device(kv_ring ring, const kv_pool *pools, uint32_t npools,
+                                       kv_host host, void *stream, uint32_t max_ops,
+                                       uint64_t idle_timeout_ns, kv_fence *fence);
+/* After the resident server's fence: descriptors it took (*served) and its
+ * own status (OK, or TIMEOUT if one of its bounded internal waits ran out).
+ * Errors: CLOSED, INVALID_ARG (no server started), TIMEOUT (still running). */
+KVB_API kv_status kv_ring_device_result(kv_ring ring, uint32_t *served, kv_status *status);
+
 /* ------------------------------------------------ L3 record store (files) */
 
 /* The tier below the host tier ([RFC] §Summary: the daemon's host tier with

@@ -749,3 +749,36 @@ def test_device_gather_scatter_without_a_fence():
         rig.assert_equal((want_pool, snap[1]))
     finally:
         rig.close()
+
+
+def test_gated_op_as_the_first_op_of_a_process(tmp_path):
+    """A gated backup is the first operation of a fresh process and its ready
+    word is set by the host only after the call returns: the call must not wait
+    for the gate (every kernel is loaded before the first launch, so no lazy
+    load queues behind the waiting gate), and the backup lands."""
+    import subprocess
+    import sys
+    root = __import__("os").path.dirname(__import__("os").path.dirname(__file__))
+    script = tmp_path / "first_op.py"
+    script.write_text(f"""
+import sys, time
+sys.path[:0] = [{root!r}, {str(__import__("os").path.join(root, "tests"))!r}]
+import numpy as np, torch
+from gpu_rig import Rig
+from hierarchical_kv_cache_backup_gb300 import kvb
+from hierarchical_kv_cache_backup_gb300 import workloads as wl
+rig = Rig(wl.TINY.geom, 16, seed=5)
+snap = rig.snapshot()
+word = torch.zeros(1, dtype=torch.int64, pin_memory=True)
+t0 = time.perf_counter()
+f = kvb.kv_backup_when_ready(rig.pool, rig.hostt, [3, 9], [0, 5], word.data_ptr(), 1, 20_000_000_000)
+call = time.perf_counter() - t0
+word[0] = 1
+kvb.kv_fence_wait(f, 30_000_000_000)
+rig.assert_equal(rig.expect_backup(snap, [3, 9], [0, 5]))
+print("call_s", call)
+""")
+    out = subprocess.run([sys.executable, str(script)], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stdout + out.stderr
+    call = float(out.stdout.split("call_s")[1])
+    assert call < 2.0, f"the gated call waited {call:.2f} s for its own gate"

@@ -1,0 +1,279 @@
+"""The GPU-resident ring server (kv_ring_serve_device) against the oracle and
+against the host server.
+
+One process plays both sides here (the ring's creator submits, an attached
+handle serves); the resident kernel takes each descriptor from the shared
+segment, moves the pages and completes the ticket from the GPU.  Every case
+checks the whole pool allocation and host tier against the oracle's replay of
+the accepted descriptors, and the status of every ticket -- rejected ones
+included -- against what the host server (kv_ring_serve) returns for the same
+descriptors on an identical pool."""
+import os
+import time
+import uuid
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import oracle  # noqa: E402
+from gpu_rig import Rig, oracle_geom  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
+
+WAIT = 60_000_000_000
+
+
+def ring_pair(slots):
+    name = f"/kvbdev_{os.getpid()}_{uuid.uuid4().hex[:8]}"
+    sub = kvb.kv_ring_create(name, slots)
+    return sub, kvb.kv_ring_attach(name)
+
+
+def replay(g, rig_offset, snap, ops, statuses):
+    """The oracle's pool and host tier after the accepted descriptors, in order."""
+    og = oracle_geom(g)
+    pool, host = snap[0].copy(), snap[1].copy()
+    for (kind, a, b, layer, _), st in zip(ops, statuses):
+        if st != kvb.KV_OK or len(a) == 0:
+            continue
+        if kind == kvb.KV_RING_OP_BACKUP:
+            oracle.backup(og, pool, host, a, b, pool_offset=rig_offset, threads=8)
+        else:
+            oracle.restore(og, pool, host, a, b, layer=layer, pool_offset=rig_offset, threads=8)
+    return pool, host
+
+
+def random_ops(r, g, S, count, npools=1):
+    """Seeded descriptors: backups and whole / one-layer restores, some of them
+    made invalid (ids out of range or negative, repeated write targets, a bad
+    layer, a pool index past the table, a backup with a layer)."""
+    ops = []
+    for _ in range(count):
+        kind = int(r.integers(2))
+        n = int(r.integers(0, min(12, S, g.P) + 1))
+        if kind == kvb.KV_RING_OP_BACKUP:
+            a = r.integers(0, g.P, n)
+            b = r.permutation(S)[:n]
+            layer = -1
+        else:
+            a = r.integers(0, S, n)
+            b = r.permutation(g.P)[:n]
+            layer = -1 if r.random() < 0.5 else int(r.integers(0, g.L))
+        pool_index = 0
+        x = r.random()
+        lim_a, lim_b = (g.P, S) if kind == 0 else (S, g.P)
+        if x < 0.08 and n:
+            a[r.integers(n)] = lim_a + int(r.integers(3))
+        elif x < 0.16 and n:
+            b[r.integers(n)] = lim_b + int(r.integers(3))
+        elif x < 0.24 and n >= 2:
+            i, j = sorted(r.choice(n, 2, replace=False))
+            b[j] = b[i]                                  # a later repeat
+        elif x < 0.28 and n:
+            b[r.integers(n)] = -1 - int(r.integers(5))
+        elif x < 0.32:
+            layer = g.L if kind == 1 else 0             # out of range / backup with a layer
+        elif x < 0.36:
+            layer = -2
+        elif x < 0.40:
+            pool_index = npools + int(r.integers(2))
+        ops.append((kind, a.astype(np.int64), b.astype(np.int64), layer, pool_index))
+    return ops
+
+
+def submit_all(sub, ops):
+    return [kvb.kv_ring_submit(sub, kvb.make_ring_op(k, a, b, pool_index=pi, layer=ly,
+                                                     operation_id=i), WAIT)
+            for i, (k, a, b, ly, pi) in enumerate(ops)]
+
+
+def run_device(g, w_offset, seed, S, ops, stream, max_ops=None, idle_ns=2_000_000_000):
+    rig = Rig(g, S, pool_offset=w_offset, seed=seed)
+    sub, srv = ring_pair(max(2, len(ops)))
+    try:
+        snap = rig.snapshot()
+        fence = kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream,
+                                         max_ops or len(ops), idle_ns)
+        tickets = submit_all(sub, ops)
+        statuses = [kvb.kv_ring_wait(sub, t, WAIT) for t in tickets]
+        kvb.kv_fence_wait(fence, WAIT)
+        served, st = kvb.kv_ring_device_result(srv)
+        after = rig.snapshot()
+        return snap, after, statuses, (served, st)
+    finally:
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        rig.close()
+
+
+def run_host(g, w_offset, seed, S, ops, stream):
+    rig = Rig(g, S, pool_offset=w_offset, seed=seed)
+    sub, srv = ring_pair(max(2, len(ops)))
+    try:
+        snap = rig.snapshot()
+        tickets = submit_all(sub, ops)
+        served = kvb.kv_ring_serve(srv, [rig.pool], rig.hostt, stream.cuda_stream, len(ops),
+                                   1_000_000_000)
+        statuses = [kvb.kv_ring_wait(sub, t, WAIT) for t in tickets]
+        stream.synchronize()
+        return snap, rig.snapshot(), statuses, served
+    finally:
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        rig.close()
+
+
+@pytest.mark.parametrize("wname", ["tiny", "llama8b", "mla_fp8", "trtllm_ipc"])
+def test_device_server_matches_the_oracle(wname):
+    """A fixed sequence -- two backups, a whole restore, a one-layer restore, an
+    empty descriptor and five rejected ones -- through the resident server."""
+    w = {x.name: x for x in wl.WORKLOADS}[wname]
+    g = w.geom.with_(P=min(w.geom.P, 96))
+    n = min(24, g.P // 3)
+    S = n + 4
+    r = np.random.default_rng(w.seed + 5)
+    src = r.permutation(g.P)[:n]
+    dst = np.setdiff1d(np.arange(g.P), src)[r.permutation(g.P - n)[:n]]
+    slots = r.permutation(S)[:n]
+    ops = [(0, src[:n // 2], slots[:n // 2], -1, 0),
+           (0, src[n // 2:], slots[n // 2:], -1, 0),
+           (1, slots, dst, -1, 0),
+           (1, slots[:3], src[:3], g.L - 1, 0),
+           (0, src[:0], slots[:0], -1, 0),
+           (1, slots[:2], np.array([1, g.P]), -1, 0),          # OUT_OF_RANGE
+           (1, slots[:3], np.array([4, 5, 4]), -1, 0),         # DUPLICATE
+           (0, src[:1], slots[:1], -1, 3),                     # INVALID_ARG: pool index
+           (0, src[:1], slots[:1], 0, 0),                      # INVALID_ARG: backup with a layer
+           (1, slots[:1], src[:1], g.L, 0)]                    # OUT_OF_RANGE: layer
+    stream = torch.cuda.Stream()
+    snap, after, statuses, (served, st) = run_device(g, w.pool_offset, w.seed, S, ops, stream)
+    assert statuses == [0, 0, 0, 0, 0, kvb.KV_ERR_OUT_OF_RANGE, kvb.KV_ERR_DUPLICATE,
+                        kvb.KV_ERR_INVALID_ARG, kvb.KV_ERR_INVALID_ARG, kvb.KV_ERR_OUT_OF_RANGE]
+    assert (served, st) == (len(ops), kvb.KV_OK)
+    want = replay(g, w.pool_offset, snap, ops, statuses)
+    assert np.array_equal(after[0], want[0]), "pool allocation differs from the oracle"
+    assert np.array_equal(after[1], want[1]), "host tier differs from the oracle"
+
+
+CASES = int(os.environ.get("KVB_RING_DEVICE_CASES", "24"))
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_device_server_agrees_with_host_server_on_random_descriptors(case):
+    """Seeded geometries and descriptor lists, run once through the host server
+    and once through the resident server on identical pools: the same status
+    for every ticket, and both results equal the oracle's replay."""
+    r = np.random.default_rng(4000 + case)
+    order, dev, host = (int(x) for x in r.integers(0, 2, 3))
+    g = wl.Geometry(L=int(r.integers(1, 5)), C=int(r.integers(1, 3)), P=int(r.integers(8, 60)),
+                    T=int(r.integers(1, 33)), H=int(r.integers(1, 9)), B=16 * int(r.integers(1, 17)),
+                    order=order, dev_heads=dev, host_heads=host)
+    S = int(r.integers(4, 24))
+    offset = 16 * int(r.integers(0, 64))
+    ops = random_ops(r, g, S, int(r.integers(4, 14)))
+    stream = torch.cuda.Stream()
+    h_snap, h_after, h_st, h_served = run_host(g, offset, 100 + case, S, ops, stream)
+    d_snap, d_after, d_st, (served, st) = run_device(g, offset, 100 + case, S, ops, stream)
+    assert d_st == h_st, (d_st, h_st)
+    assert (served, st) == (len(ops), kvb.KV_OK) and h_served == len(ops)
+    want = replay(g, offset, d_snap, ops, d_st)
+    assert np.array_equal(d_after[0], want[0]) and np.array_equal(d_after[1], want[1])
+    assert np.array_equal(h_after[0], want[0]) and np.array_equal(h_after[1], want[1])
+
+
+def test_device_server_ends_when_idle_and_refuses_a_second_server():
+    g = wl.TINY.geom
+    rig = Rig(g, 16, seed=31)
+    sub, srv = ring_pair(4)
+    stream = torch.cuda.Stream()
+    try:
+        snap = rig.snapshot()
+        t0 = time.perf_counter()
+        fence = kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream, 100,
+                                         300_000_000)
+        with pytest.raises(kvb.KvError) as e:                 # one resident server per ring
+            kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream, 1, 1000)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+        with pytest.raises(kvb.KvError) as e:                 # no result while it runs
+            kvb.kv_ring_device_result(srv)
+        assert e.value.status == kvb.KV_ERR_TIMEOUT
+        ops = [(0, [5, 9], [0, 3], -1, 0), (1, [0, 3], [20, 21], 0, 0)]
+        tickets = submit_all(sub, ops)
+        assert [kvb.kv_ring_wait(sub, t, WAIT) for t in tickets] == [0, 0]
+        kvb.kv_fence_wait(fence, WAIT)
+        assert time.perf_counter() - t0 >= 0.3                # ended by the idle bound
+        assert kvb.kv_ring_device_result(srv) == (2, kvb.KV_OK)
+        want = replay(g, 0, snap, ops, [0, 0])
+        rig.assert_equal(want)
+        # a second server on the same ring takes up at the next ticket
+        fence = kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream, 1,
+                                         WAIT // 100)
+        t = kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [7], [9]))
+        assert kvb.kv_ring_wait(sub, t, WAIT) == kvb.KV_OK
+        kvb.kv_fence_wait(fence, WAIT)
+        assert kvb.kv_ring_device_result(srv) == (1, kvb.KV_OK)
+        want = replay(g, 0, want, [(0, [7], [9], -1, 0)], [0])
+        rig.assert_equal(want)
+        # limits checked before anything is enqueued
+        for args, status in (((srv, [], rig.hostt), kvb.KV_ERR_INVALID_ARG),
+                             ((srv, [rig.pool], 0), kvb.KV_ERR_INVALID_ARG)):
+            with pytest.raises(kvb.KvError) as e:
+                kvb.kv_ring_serve_device(*args, stream.cuda_stream, 1, 1000)
+            assert e.value.status == status
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream, 1,
+                                     61_000_000_000)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    finally:
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        rig.close()
+
+
+def test_device_server_with_two_pools_and_a_split_pool():
+    """A table of two pools (one contiguous page-first HND, one split layer-first
+    NHD of the same slot geometry); descriptors pick their pool by index."""
+    ga = wl.Geometry(L=3, C=2, P=40, T=16, H=4, B=64, order=wl.PAGE_FIRST, dev_heads=wl.HND)
+    gb = ga.with_(order=wl.LAYER_FIRST, dev_heads=wl.NHD)
+    S = 12
+    rig = Rig(ga, S, pool_offset=32, seed=41)
+    chunk = gb.P * gb.T * gb.H * gb.B
+    bufs = [torch.empty(chunk, dtype=torch.uint8, device="cuda") for _ in range(gb.L * gb.C)]
+    for k, b in enumerate(bufs):
+        wl.fill_random_(b, 4200 + k)
+    lay_b = kvb.make_layout(gb.L, gb.C, gb.P, gb.T, gb.H, gb.B, gb.order, gb.dev_heads)
+    pool_b = kvb.kv_pool_register_split(lay_b, [b.data_ptr() for b in bufs])
+    sub, srv = ring_pair(8)
+    stream = torch.cuda.Stream()
+    try:
+        snap = rig.snapshot()
+        flat = torch.cat(bufs).cpu().numpy()
+        fence = kvb.kv_ring_serve_device(srv, [rig.pool, pool_b], rig.hostt, stream.cuda_stream,
+                                         4, WAIT // 10)
+        ops = [(0, [3, 17, 39], [0, 1, 2], -1, 0),     # pool 0 -> slots 0..2
+               (1, [0, 1, 2], [5, 6, 7], -1, 1),       # slots -> split pool pages 5..7
+               (0, [11, 12], [3, 4], -1, 1),           # split pool -> slots 3, 4
+               (1, [3, 4], [30, 31], 1, 0)]            # layer 1 of slots 3, 4 -> pool 0
+        tickets = submit_all(sub, ops)
+        assert [kvb.kv_ring_wait(sub, t, WAIT) for t in tickets] == [0, 0, 0, 0]
+        kvb.kv_fence_wait(fence, WAIT)
+        assert kvb.kv_ring_device_result(srv) == (4, kvb.KV_OK)
+        oa, ob = oracle_geom(ga), oracle_geom(gb)
+        pool_a, host = snap[0].copy(), snap[1].copy()
+        oracle.backup(oa, pool_a, host, [3, 17, 39], [0, 1, 2], pool_offset=32)
+        oracle.restore(ob, flat, host, [0, 1, 2], [5, 6, 7])
+        oracle.backup(ob, flat, host, [11, 12], [3, 4])
+        oracle.restore(oa, pool_a, host, [3, 4], [30, 31], layer=1, pool_offset=32)
+        rig.assert_equal((pool_a, host))
+        assert np.array_equal(torch.cat(bufs).cpu().numpy(), flat), "split pool"
+    finally:
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        kvb.kv_pool_close(pool_b)
+        rig.close()

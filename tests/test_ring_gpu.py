@@ -3,7 +3,8 @@
 The scheduler process owns the pool (a raw allocation at a byte offset) and the
 decisions; a second process -- the data plane -- imports the pool through CUDA
 IPC, owns the pinned host tier and serves BACKUP / RESTORE descriptors from the
-shared-memory ring; the GPU completes each ticket in shared memory.  The
+shared-memory ring -- from a host thread, or with the GPU-resident server --
+and the GPU completes each ticket in shared memory.  The
 scheduler checks its pool against the CPU oracle and sees the data plane's
 errors come back through the ring."""
 import multiprocessing as mp
@@ -27,7 +28,7 @@ from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _data_plane(ring_name, desc_bytes, geom_kw, slots, expected_ops, q):
+def _data_plane(ring_name, desc_bytes, geom_kw, slots, expected_ops, q, server="host"):
     try:
         import sys
         sys.path[:0] = [ROOT]
@@ -43,6 +44,13 @@ def _data_plane(ring_name, desc_bytes, geom_kw, slots, expected_ops, q):
         ring = k.kv_ring_attach(ring_name)
         stream = t.cuda.Stream()
         served = 0
+        if server == "device":   # the resident kernel serves; its first op in this process
+            f = k.kv_ring_serve_device(ring, [pool], tier, stream.cuda_stream, expected_ops,
+                                       10_000_000_000)
+            k.kv_fence_wait(f, 120_000_000_000)
+            served, st = k.kv_ring_device_result(ring)
+            if st != k.KV_OK:
+                raise RuntimeError(f"resident server status {st}")
         while served < expected_ops:
             n = k.kv_ring_serve(ring, [pool], tier, stream.cuda_stream, 8, 30_000_000_000)
             if n == 0:
@@ -57,8 +65,9 @@ def _data_plane(ring_name, desc_bytes, geom_kw, slots, expected_ops, q):
         q.put(("error", repr(e)))
 
 
-@pytest.mark.parametrize("wname", ["trtllm_ipc", "llama8b"])
-def test_scheduler_and_data_plane_over_the_ring(wname):
+@pytest.mark.parametrize("wname,server", [("trtllm_ipc", "host"), ("llama8b", "host"),
+                                          ("trtllm_ipc", "device"), ("llama8b", "device")])
+def test_scheduler_and_data_plane_over_the_ring(wname, server):
     w = {x.name: x for x in wl.WORKLOADS}[wname]
     g = w.geom.with_(P=96)
     n = 24
@@ -73,11 +82,13 @@ def test_scheduler_and_data_plane_over_the_ring(wname):
     geom_kw = dict(L=g.L, C=g.C, P=g.P, T=g.T, H=g.H, B=g.B, order=g.order,
                    dev_heads=g.dev_heads, host_heads=g.host_heads)
     ops_total = 6
+    # the scheduler's own GPU work happens before the data plane starts and after
+    # it has ended: its context never competes with the resident server's
+    snap = rig.snapshot()
     p = ctx.Process(target=_data_plane, args=(name, kvb.desc_to_bytes(kvb.kv_pool_export(pool)),
-                                              geom_kw, n, ops_total, q))
+                                              geom_kw, n, ops_total, q, server))
     p.start()
     try:
-        snap = rig.snapshot()
         src = r.permutation(g.P)[:n]
         dst = np.setdiff1d(np.arange(g.P), src)[r.permutation(g.P - n)[:n]]
         slots = r.permutation(n)
