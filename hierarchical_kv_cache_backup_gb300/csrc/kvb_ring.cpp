@@ -267,8 +267,14 @@ kv_status kv_ring_close(kv_ring r) {
         g_rings.erase(it);
     }
     kv_status s = KV_OK;
-    if (o->srv_fence != 0 && kv_fence_wait(o->srv_fence, 120ull * 1000 * 1000 * 1000) == KV_ERR_TIMEOUT)
-        s = err(KV_ERR_TIMEOUT, "a resident server of this ring was still running at close");
+    if (o->srv_fence != 0 && kv_fence_query(o->srv_fence) == KV_ERR_TIMEOUT) {
+        // a resident server still reads the segment: ask it to stop, and never
+        // unmap under it (if it has not ended in time, everything is left mapped)
+        __atomic_store_n(&o->srv_result[2], 1u, __ATOMIC_RELEASE);
+        if (kv_fence_wait(o->srv_fence, 120ull * 1000 * 1000 * 1000) == KV_ERR_TIMEOUT)
+            return err(KV_ERR_TIMEOUT, "the ring's resident server did not stop: the ring is "
+                       "closed but its memory stays mapped");
+    }
     if (o->srv_ctl != nullptr) {   // one allocation: control block, ids, pool table
         int prev = -1;
         if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
@@ -502,6 +508,7 @@ kv_status kv_ring_serve_device(kv_ring r, const kv_pool *pools, uint32_t npools,
     cudaStream_t s = (cudaStream_t)stream;
     o->srv_result[0] = 0;
     o->srv_result[1] = (uint32_t)KV_OK;
+    __atomic_store_n(&o->srv_result[2], 0u, __ATOMIC_RELEASE);   // no stop request
     st = ck(cudaMemcpyAsync(o->srv_pools, table, npools * sizeof(kvb::RingPoolK),
                             cudaMemcpyHostToDevice, s), "copying the pool table failed");
     if (st == KV_OK)
@@ -529,6 +536,15 @@ kv_status kv_ring_serve_device(kv_ring r, const kv_pool *pools, uint32_t npools,
     st = (kv_status)kvb::ring_launch_server(device, k, ctas, s, fence);
     if (st != KV_OK) return st;
     o->srv_fence = *fence;
+    return KV_OK;
+}
+
+kv_status kv_ring_device_stop(kv_ring r) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    std::lock_guard<std::mutex> lk(o->mu);
+    if (o->srv_fence == 0) return err(KV_ERR_INVALID_ARG, "no resident server was started");
+    __atomic_store_n(&o->srv_result[2], 1u, __ATOMIC_RELEASE);
     return KV_OK;
 }
 

@@ -69,7 +69,8 @@ struct RingKDesc {
     // device scratch
     RingCtl *ctl;
     int32_t *ids;                     // 2 * KV_RING_MAX_IDS: a then b of the released descriptor
-    uint32_t *result;                 // mapped pinned: [0] served, [1] kv_status of the server
+    uint32_t *result;                 // mapped pinned: [0] served, [1] kv_status of the server,
+                                      // [2] set by the host: stop before the next descriptor
 };
 
 // Shape of the resident server: 32 CTAs of 256 threads (on GB300 the move

@@ -64,6 +64,11 @@ __device__ __forceinline__ int32_t ld_relaxed_sys(const int32_t *p) {
     asm volatile("ld.relaxed.sys.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ uint32_t ld_relaxed_sys_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t *p) {
     int32_t v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -275,13 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
     while (served < k.max_ops) {
         const uint64_t t = k.first_ticket + served;
         const uint32_t slot = (uint32_t)((t - 1) % k.slots);
-        // wait for the descriptor (idle bound)
+        // wait for the descriptor (idle bound) unless the host asked the server
+        // to stop; the stop word is loaded first so both loads are in flight
         if (tid == 0) {
             int go = 0;
             const unsigned long long deadline = now_ns() + k.idle_ns;
             const unsigned long long max_polls = k.idle_ns / 64ull + 4096ull;
             for (unsigned long long polls = 0;; ++polls) {
-                if (ld_acquire_sys(k.tail) >= t) { go = 1; break; }
+                const uint32_t stop = ld_relaxed_sys_u32(k.result + 2);
+                const unsigned long long tail = ld_acquire_sys(k.tail);
+                if (stop != 0) break;
+                if (tail >= t) { go = 1; break; }
                 if (polls >= max_polls || now_ns() > deadline) break;
             }
             s_flag = go;

@@ -51,6 +51,7 @@ EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_p
            "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
            "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
            "kv_ring_pop", "kv_ring_complete", "kv_ring_serve_device", "kv_ring_device_result",
+           "kv_ring_device_stop",
            "kv_fault_inject", "kv_l3_open", "kv_l3_close",
            "kv_l3_put", "kv_l3_get")
 
@@ -138,6 +139,7 @@ def _load():
         "kv_ring_complete": (st, [vp, u64, ctypes.c_int]),
         "kv_ring_serve_device": (st, [vp, P(vp), u32, vp, vp, u32, u64, P(u64)]),
         "kv_ring_device_result": (st, [vp, P(u32), P(ctypes.c_int)]),
+        "kv_ring_device_stop": (st, [vp]),
         "kv_fault_inject": (st, [ctypes.c_char_p, u32]),
         "kv_l3_open": (st, [ctypes.c_int, u64, u64, u64, u32, P(vp)]),
         "kv_l3_close": (st, [vp]),
@@ -527,6 +529,11 @@ def kv_ring_serve_device(ring: int, pools, host: int, stream=None, max_ops: int 
     _check(_lib.kv_ring_serve_device(ring, arr, len(pools), host, stream, max_ops,
                                      idle_timeout_ns, ctypes.byref(f)))
     return f.value
+
+
+def kv_ring_device_stop(ring: int) -> None:
+    """Asks the ring's resident server to end before its next descriptor (returns at once)."""
+    _check(_lib.kv_ring_device_stop(ring))
 
 
 def kv_ring_device_result(ring: int):

@@ -401,8 +401,10 @@ KVB_API kv_status kv_ring_create(const char *name, uint32_t slots, kv_ring *out)
 /* Attaches to an existing ring.  Errors: INVALID_ARG (no such ring, wrong
  * magic or version, or a header whose regions do not fit the segment). */
 KVB_API kv_status kv_ring_attach(const char *name, kv_ring *out);
-/* Detaches (and unlinks, for the creator; unregisters the completion page
- * from CUDA, for a server).  Errors: CLOSED. */
+/* Detaches (and unlinks, for the creator; unregisters the segment from CUDA,
+ * for a server).  A resident server still running on this handle is asked to
+ * stop and waited for (bounded); if it has not ended, TIMEOUT and the memory
+ * stays mapped.  Errors: CLOSED, TIMEOUT. */
 KVB_API kv_status kv_ring_close(kv_ring ring);
 
 /* Submitter: copies `op` into the next slot and publishes it; waits up to
@@ -467,6 +469,12 @@ KVB_API kv_status kv_ring_serve_device(kv_ring ring, const kv_pool *pools, uint3
  * own status (OK, or TIMEOUT if one of its bounded internal waits ran out).
  * Errors: CLOSED, INVALID_ARG (no server started), TIMEOUT (still running). */
 KVB_API kv_status kv_ring_device_result(kv_ring ring, uint32_t *served, kv_status *status);
+/* Asks the ring's resident server to end before it takes another descriptor
+ * (the one it is moving completes); returns at once, and the server's fence
+ * completes when it has ended.  kv_ring_close does this itself and never
+ * unmaps the segment under a running server.  Errors: CLOSED, INVALID_ARG
+ * (no server started). */
+KVB_API kv_status kv_ring_device_stop(kv_ring ring);
 
 /* ------------------------------------------------ L3 record store (files) */
 

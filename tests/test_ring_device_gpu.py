@@ -277,3 +277,41 @@ def test_device_server_with_two_pools_and_a_split_pool():
         kvb.kv_ring_close(sub)
         kvb.kv_pool_close(pool_b)
         rig.close()
+
+
+def test_device_server_stops_on_request_and_on_close():
+    """kv_ring_device_stop ends a resident server well before its idle limit,
+    after the descriptor it is moving; closing the serving handle stops a
+    running server before unmapping anything."""
+    g = wl.TINY.geom
+    rig = Rig(g, 16, seed=33)
+    sub, srv = ring_pair(4)
+    stream = torch.cuda.Stream()
+    try:
+        snap = rig.snapshot()
+        with pytest.raises(kvb.KvError) as e:                 # nothing to stop yet
+            kvb.kv_ring_device_stop(srv)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+        fence = kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream, 1000,
+                                         30_000_000_000)
+        t = kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [4, 8], [1, 2]))
+        assert kvb.kv_ring_wait(sub, t, WAIT) == kvb.KV_OK
+        t0 = time.perf_counter()
+        kvb.kv_ring_device_stop(srv)
+        kvb.kv_fence_wait(fence, WAIT)
+        assert time.perf_counter() - t0 < 5.0                 # not the 30 s idle limit
+        assert kvb.kv_ring_device_result(srv) == (1, kvb.KV_OK)
+        rig.assert_equal(replay(g, 0, snap, [(0, [4, 8], [1, 2], -1, 0)], [0]))
+        # a running server, then close of its handle: stopped first, then unmapped
+        kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream, 1000,
+                                 30_000_000_000)
+        t0 = time.perf_counter()
+        kvb.kv_ring_close(srv)
+        srv = None
+        assert time.perf_counter() - t0 < 5.0
+        stream.synchronize()
+    finally:
+        if srv is not None:
+            kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        rig.close()
