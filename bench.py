@@ -812,6 +812,59 @@ def run_ours(args):
                                 "to ticket complete on the host clock, one descriptor in flight, "
                                 "4 page sets in rotation, L2 warm")
         latency["ring_round_trip"] = ring_lat
+        # ---- descriptor ring throughput: each step is the Llama-8B step as 8
+        # descriptors (4 backups of 128 pages, then 4 restores of 128 pages), all
+        # submitted at once, host clock from the first submit to the last ticket
+        ring_tp = {}
+        steps_r = 6
+        per = w.n // 4
+        for kind in ("host", "device"):
+            name = f"/kvbbenchtp_{os.getpid()}_{kind}"
+            sub = kvb.kv_ring_create(name, 16)
+            srv = kvb.kv_ring_attach(name)
+            rs = torch.cuda.Stream(device=dev)
+            stop = threading.Event()
+            served = [0]
+
+            def serve_loop():
+                while not stop.is_set() and served[0] < 8 * steps_r:
+                    served[0] += kvb.kv_ring_serve(srv, [pool], tier, rs.cuda_stream, 64,
+                                                   200_000_000)
+
+            th, fence = None, None
+            if kind == "host":
+                th = threading.Thread(target=serve_loop, daemon=True)
+                th.start()
+            else:
+                fence = kvb.kv_ring_serve_device(srv, [pool], tier, rs.cuda_stream, 8 * steps_r,
+                                                 5_000_000_000)
+            times = []
+            for i in range(steps_r):
+                ids = idsets[i % R]
+                ops = [kvb.make_ring_op(0, ids.backup_src[c * per:(c + 1) * per],
+                                        ids.backup_slots[c * per:(c + 1) * per]) for c in range(4)]
+                ops += [kvb.make_ring_op(1, ids.restore_slots[c * per:(c + 1) * per],
+                                         ids.restore_dst[c * per:(c + 1) * per]) for c in range(4)]
+                t0 = time.perf_counter()
+                tks = [kvb.kv_ring_submit(sub, op) for op in ops]
+                sts = [kvb.kv_ring_wait(sub, tk, 30_000_000_000) for tk in tks]
+                times.append(time.perf_counter() - t0)
+                if any(sts):
+                    raise RuntimeError(f"ring {kind} step {i}: statuses {sts}")
+            if fence is not None:
+                kvb.kv_fence_wait(fence, 30_000_000_000)
+            stop.set()
+            if th is not None:
+                th.join(10)
+            rs.synchronize()
+            kvb.kv_ring_close(srv)
+            kvb.kv_ring_close(sub)
+            ring_tp[f"{kind}_served_gbs"] = round(2 * w.n * g.page_bytes /
+                                                  statistics.median(times[1:]) / GB, 2)
+        ring_tp["workload"] = ("Llama-8B step as 8 ring descriptors (4 x 128-page backups, then "
+                               "4 x 128-page restores; 2 GiB), all submitted at once, host clock "
+                               "from the first submit to the last ticket, median of 5 steps")
+        latency["ring_throughput"] = ring_tp
         kvb.kv_pool_close(tpool)
         kvb.kv_host_close(ttier)
         del talloc, thost
