@@ -504,7 +504,7 @@ kv_status kv_ring_serve_device(kv_ring r, const kv_pool *pools, uint32_t npools,
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    const int ctas = std::max(1, std::min(kvb::kRingCtas, sms));
+    const int ctas = 1 + std::max(1, std::min(kvb::kRingMovers, sms - 1));   // leader + movers
     cudaStream_t s = (cudaStream_t)stream;
     o->srv_result[0] = 0;
     o->srv_result[1] = (uint32_t)KV_OK;

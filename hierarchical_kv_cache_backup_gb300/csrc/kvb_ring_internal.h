@@ -73,18 +73,20 @@ struct RingKDesc {
                                       // [2] set by the host: stop before the next descriptor
 };
 
-// Shape of the resident server: 32 CTAs of 256 threads (on GB300 the move
-// kernel reaches the D2H peak with 16 such CTAs and the H2D peak with 32); a
+// Shape of the resident server: one leader CTA (takes, checks and releases
+// descriptors) and 32 mover CTAs, all of 256 threads (on GB300 the move kernel
+// reaches the D2H peak with 16 such CTAs and the H2D peak with 32); a
 // 256-thread CTA leaves each thread the registers of every move variant.  The
-// server holds 32 of the SMs while it runs, idle or not.
-constexpr int kRingCtas = 32;
+// server holds 33 SMs while it runs, idle or not.
+constexpr int kRingMovers = 32;
 constexpr int kRingThreads = 256;
 
 // Loads the resident server kernel on the current device (see preload_kernels).
 cudaError_t preload_ring_kernels();
 
 // Launches the resident server as a cooperative grid of `ctas` CTAs of
-// kRingThreads threads on `stream` (every CTA resident at once).
+// kRingThreads threads on `stream` (every CTA resident at once): CTA 0 leads,
+// the other ctas - 1 (at least one) move.
 cudaError_t launch_ring_server(const RingKDesc &k, int ctas, cudaStream_t stream);
 
 // ---- engine support for the resident server (kvb_api.cpp) ----------------

@@ -4,19 +4,21 @@
 // device-memory IPC", §Device IPC data path: once the pool is registered,
 // BACKUP / RESTORE travel as descriptors, and a high-frequency path may want
 // an NVMe-style submission / completion queue.  Here the queue's consumer is
-// the GPU itself: one cooperative grid stays resident, its leader CTA polls
+// the GPU itself: one cooperative grid stays resident.  Its leader CTA polls
 // the ring's tail in the shared segment (pinned host memory mapped into the
 // GPU; on GB300 the reads are coherent over NVLink-C2C), takes each descriptor,
-// validates it exactly as the host engine does, and releases it to every CTA;
-// the grid moves the pages and the CTA that finishes last writes the ticket
-// into the slot's completion record.  No host thread and no launch per
-// operation: the submitter's descriptor store and its completion poll are
-// the only CPU work.
+// validates it exactly as the host engine does, and releases it to the mover
+// CTAs; they move the pages and the mover that finishes last writes the ticket
+// into the slot's completion record.  The leader moves nothing: while the
+// movers move descriptor t it already takes and checks t + 1.  No host thread
+// and no launch per operation: the submitter's descriptor store and its
+// completion poll are the only CPU work.
 //
-// Descriptors run one after another in ticket order (as the host server's
-// single stream runs them).  Every wait is bounded: the leader waits at most
-// idle_ns for a descriptor, then ends the server; any other wait gives up
-// after idle_ns + 5 s, records it and returns.  Nothing traps.
+// Accepted descriptors run one after another in ticket order (as the host
+// server's single stream runs them); a rejected one is completed as soon as
+// it is checked.  Every wait is bounded: the leader waits at most idle_ns for
+// a descriptor, then ends the server; any other wait gives up after idle_ns +
+// 5 s, records it and returns.  Nothing traps.
 //
 // Memory model.  Pages and host slots may be written by one descriptor and
 // read by the next inside this one launch, so payload and ids are loaded
@@ -138,9 +140,10 @@ __device__ __forceinline__ void move_loop(const Side src, const Side dst, const 
                                           const int32_t *s_b) {
     const uint32_t total = n * nl * p.C * p.segs;   // < 2^32: checked when the server starts
     const uint32_t lane = threadIdx.x & 31u;
-    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    // the mover CTAs 1 .. gridDim.x - 1 (CTA 0 is the leader)
+    const uint32_t nwarps = ((gridDim.x - 1) * blockDim.x) >> 5;
     const uint32_t hnd = kMode == 1 ? dst.hnd : src.hnd;   // head order of the walked side
-    for (uint32_t w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < total; w += nwarps) {
+    for (uint32_t w = ((blockIdx.x - 1) * blockDim.x + threadIdx.x) >> 5; w < total; w += nwarps) {
         const uint32_t chunk = fdiv(w, p.div_segs);
         const uint32_t seg = w - chunk * p.segs;
         const uint32_t item = fdiv(chunk, div_lc);
@@ -196,9 +199,9 @@ __device__ __forceinline__ void move_share(const RingKDesc &k, const RingPoolK &
         move_loop<2>(src, dst, p, n, nl, l0, div_lc, s_a, s_b);
 }
 
-// A CTA's arrival at the end of released descriptor number `rel` (1-based):
-// its stores are made visible system-wide, then counted; the last of the
-// grid's arrivals stores the ticket into the completion record.
+// A mover CTA's arrival at the end of released descriptor number `rel`
+// (1-based): its stores are made visible system-wide, then counted; the last
+// of the movers' arrivals stores the ticket into the completion record.
 __device__ __forceinline__ void arrive(const RingKDesc &k, uint32_t rel, uint64_t ticket) {
     __threadfence_system();
     __syncthreads();
@@ -208,7 +211,7 @@ __device__ __forceinline__ void arrive(const RingKDesc &k, uint32_t rel, uint64_
                      : "=r"(prev)
                      : "l"(&k.ctl->arrived)
                      : "memory");
-        if (prev + 1 == gridDim.x * rel) {
+        if (prev + 1 == (gridDim.x - 1) * rel) {
             __threadfence_system();
             st_release_sys((unsigned long long *)&k.comp[(ticket - 1) % k.slots].done, ticket);
         }
@@ -224,6 +227,112 @@ __device__ __forceinline__ void complete_failed(const RingKDesc &k, uint64_t t, 
     st_release_sys((unsigned long long *)&c.done, t);
 }
 
+// Leader, thread 0: waits (bounded) until the movers' arrivals reach `want`.
+__device__ __forceinline__ int wait_arrivals(const RingKDesc &k, uint32_t want) {
+    const unsigned long long deadline = now_ns() + kSlackNs;
+    for (unsigned long long polls = 0;; ++polls) {
+        if (ld_acquire_gpu(&k.ctl->arrived) >= want) return 1;
+        if (ld_acquire_gpu(&k.ctl->gave_up) != 0 || polls >= kSlackNs / 16ull ||
+            ((polls & 63u) == 63u && now_ns() > deadline))
+            return 0;
+        if (polls >= 4096) __nanosleep(64);
+    }
+}
+
+// Checks a descriptor exactly as the host engine would, in its order: kind,
+// n, pool index and a backup's layer (INVALID_ARG), the layer (OUT_OF_RANGE),
+// then the ids -- any source id out of range, else whichever comes first in
+// index order of a write target out of range (OUT_OF_RANGE) and a write
+// target repeated from an earlier one (DUPLICATE).  Called by every thread of
+// the leader CTA with the ids it holds (thread i: ids i, i + kThreads, ...);
+// leaves ids [0, n) in s_a / s_b.  The three shared words start as
+// "none" (0xffffffff, 0xffffffff, 0).
+__device__ int32_t check_descriptor(const RingKDesc &k, uint32_t kind, uint32_t n, uint32_t pool,
+                                    int32_t layer, const int32_t (&a_r)[kIdsPerThread],
+                                    const int32_t (&b_r)[kIdsPerThread], int32_t *s_a,
+                                    int32_t *s_b, unsigned long long *s_key,
+                                    uint32_t *s_first_bad, uint32_t *s_first_dup,
+                                    uint32_t *s_any_bad_a) {
+    if (kind > KV_RING_OP_RESTORE || n > kMaxIds || pool >= k.npools) return KV_ERR_INVALID_ARG;
+    if (kind == KV_RING_OP_BACKUP && layer != -1) return KV_ERR_INVALID_ARG;
+    if (layer < -1 || (layer >= 0 && (uint32_t)layer >= k.pools[pool].L)) return KV_ERR_OUT_OF_RANGE;
+    if (n == 0) return KV_OK;
+    const uint32_t tid = threadIdx.x;
+    const bool backup = kind == KV_RING_OP_BACKUP;
+    const uint32_t lim_a = backup ? k.pools[pool].P : k.num_slots;
+    const uint32_t lim_b = backup ? k.num_slots : k.pools[pool].P;
+#pragma unroll
+    for (int h = 0; h < kIdsPerThread; ++h) {
+        const uint32_t i = tid + h * kThreads;
+        if (i < n) {
+            s_a[i] = a_r[h];
+            s_b[i] = b_r[h];
+        }
+    }
+    if (n <= 32) {
+        // one warp, no block barrier: lane i holds id i; a repeat is a lane whose
+        // write target equals a lower lane's
+        if (tid < 32) {
+            const bool in = tid < n;
+            const int32_t a = a_r[0], b = b_r[0];
+            bool dup = false;
+            for (uint32_t j = 0; j < n; ++j) {
+                const int32_t bj = __shfl_sync(0xffffffffu, b, j);
+                dup |= in && j < tid && bj == b;
+            }
+            const unsigned bad_a = __ballot_sync(0xffffffffu, in && (a < 0 || (uint32_t)a >= lim_a));
+            const unsigned bad_b = __ballot_sync(0xffffffffu, in && (b < 0 || (uint32_t)b >= lim_b));
+            const unsigned dups = __ballot_sync(0xffffffffu, dup);
+            if (tid == 0) {
+                *s_any_bad_a = bad_a != 0u;
+                if (bad_b) *s_first_bad = (uint32_t)__ffs(bad_b) - 1u;
+                if (dups) *s_first_dup = (uint32_t)__ffs(dups) - 1u;
+            }
+        }
+    } else {
+        // sort (b, index) keys; the first repeat of a value in index order is the
+        // later of two equal neighbours; pads (index >= n) sort last, never counted
+        uint32_t m = 2;
+        while (m < n) m <<= 1;
+#pragma unroll
+        for (int h = 0; h < kIdsPerThread; ++h) {
+            const uint32_t i = tid + h * kThreads;
+            if (i < n) {
+                if (a_r[h] < 0 || (uint32_t)a_r[h] >= lim_a) *s_any_bad_a = 1u;
+                if (b_r[h] < 0 || (uint32_t)b_r[h] >= lim_b) atomicMin(s_first_bad, i);
+            }
+            if (i < m)
+                s_key[i] = i < n ? ((unsigned long long)(uint32_t)b_r[h] << 32) | i
+                                 : (0xffffffffull << 32) | i;
+        }
+        for (uint32_t size = 2; size <= m; size <<= 1)
+            for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+                __syncthreads();
+                for (uint32_t i = tid; i < m; i += kThreads) {
+                    const uint32_t j = i ^ stride;
+                    if (j > i) {
+                        const unsigned long long x = s_key[i], y = s_key[j];
+                        if ((x > y) == ((i & size) == 0)) {
+                            s_key[i] = y;
+                            s_key[j] = x;
+                        }
+                    }
+                }
+            }
+        __syncthreads();
+        for (uint32_t i = tid + 1; i < m; i += kThreads) {
+            const unsigned long long x = s_key[i], y = s_key[i - 1];
+            const uint32_t idx = (uint32_t)x;
+            if (idx < n && (x >> 32) == (y >> 32)) atomicMin(s_first_dup, idx);
+        }
+    }
+    __syncthreads();
+    if (*s_any_bad_a) return KV_ERR_OUT_OF_RANGE;
+    if (*s_first_bad < *s_first_dup) return KV_ERR_OUT_OF_RANGE;
+    if (*s_first_dup != 0xffffffffu) return KV_ERR_DUPLICATE;
+    return KV_OK;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __grid_constant__ RingKDesc k) {
     __shared__ int32_t s_a[kMaxIds], s_b[kMaxIds];
     __shared__ unsigned long long s_key[kMaxIds];   // leader: (b[i] << 32) | i, sorted
@@ -234,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
     const uint32_t tid = threadIdx.x;
 
     if (blockIdx.x != 0) {
-        // ---------------------------------------------------- worker CTAs
+        // ----------------------------------------------------- mover CTAs
         for (uint32_t r = 0;; ++r) {
             if (tid == 0) {
                 int go = 0;   // 1: descriptor r released; 0: stopped; -1: gave up
@@ -249,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
                         go = -1;
                         break;
                     }
-                    __nanosleep(128);
+                    if (polls >= 4096) __nanosleep(128);   // spin first: descriptors stream in
                 }
                 if (go < 0) atomicExch(&ctl->gave_up, 1u);
                 s_flag = go;
@@ -273,12 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
     }
 
     // -------------------------------------------------------- leader CTA
+    // Control only: it takes and checks descriptor t + 1 while the movers move
+    // descriptor t, and releases t + 1 once every mover has arrived at t's end.
     if (tid == 0) asm volatile("st.relaxed.sys.global.s64 [%0], %1;" ::"l"(k.server_pid), "l"(k.pid)
                                : "memory");
-    uint32_t served = 0, released = 0;
+    const uint32_t movers = gridDim.x - 1;
+    uint32_t taken = 0, released = 0;
     int32_t server_status = KV_OK;
-    while (served < k.max_ops) {
-        const uint64_t t = k.first_ticket + served;
+    for (;;) {
+        if (taken >= k.max_ops) break;
+        const uint64_t t = k.first_ticket + taken;
         const uint32_t slot = (uint32_t)((t - 1) % k.slots);
         // wait for the descriptor (idle bound) unless the host asked the server
         // to stop; the stop word is loaded first so both loads are in flight
@@ -315,86 +428,41 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
             s_any_bad_a = 0u;
         }
         __syncthreads();
+        ++taken;
         const uint32_t kind = s_hdr[0], n = s_hdr[1], pool = s_hdr[2];
         const int32_t layer = (int32_t)s_hdr[3];
-        // the checks of the host path, in its order
-        int32_t status = KV_OK;
-        if (kind > KV_RING_OP_RESTORE || n > kMaxIds || pool >= k.npools)
-            status = KV_ERR_INVALID_ARG;
-        else if (kind == KV_RING_OP_BACKUP && layer != -1)
-            status = KV_ERR_INVALID_ARG;
-        else if (layer < -1 || (layer >= 0 && (uint32_t)layer >= k.pools[pool].L))
-            status = KV_ERR_OUT_OF_RANGE;
-        if (status == KV_OK && n > 0) {
-            const bool backup = kind == KV_RING_OP_BACKUP;
-            const uint32_t lim_a = backup ? k.pools[pool].P : k.num_slots;
-            const uint32_t lim_b = backup ? k.num_slots : k.pools[pool].P;
-            // write targets (b) must be distinct: sort (b, index) keys, then the
-            // first repeat of a value in index order is the later of two equal
-            // neighbours; pads (index >= n) sort last and are never counted
-            uint32_t m = 2;
-            while (m < n) m <<= 1;
-#pragma unroll
-            for (int h = 0; h < kIdsPerThread; ++h) {
-                const uint32_t i = tid + h * kThreads;
-                if (i < n) {
-                    s_a[i] = a_r[h];
-                    s_b[i] = b_r[h];
-                    if (a_r[h] < 0 || (uint32_t)a_r[h] >= lim_a) s_any_bad_a = 1u;
-                    if (b_r[h] < 0 || (uint32_t)b_r[h] >= lim_b) atomicMin(&s_first_bad, i);
-                }
-                if (i < m)
-                    s_key[i] = i < n ? ((unsigned long long)(uint32_t)b_r[h] << 32) | i
-                                     : (0xffffffffull << 32) | i;
-            }
-            for (uint32_t size = 2; size <= m; size <<= 1)
-                for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-                    __syncthreads();
-                    for (uint32_t i = tid; i < m; i += kThreads) {
-                        const uint32_t j = i ^ stride;
-                        if (j > i) {
-                            const unsigned long long x = s_key[i], y = s_key[j];
-                            if ((x > y) == ((i & size) == 0)) {
-                                s_key[i] = y;
-                                s_key[j] = x;
-                            }
-                        }
-                    }
-                }
-            __syncthreads();
-            for (uint32_t i = tid + 1; i < m; i += kThreads) {
-                const unsigned long long x = s_key[i], y = s_key[i - 1];
-                const uint32_t idx = (uint32_t)x;
-                if (idx < n && (x >> 32) == (y >> 32)) atomicMin(&s_first_dup, idx);
-            }
-            __syncthreads();
-            if (s_any_bad_a) status = KV_ERR_OUT_OF_RANGE;
-            else if (s_first_bad < s_first_dup) status = KV_ERR_OUT_OF_RANGE;
-            else if (s_first_dup != 0xffffffffu) status = KV_ERR_DUPLICATE;
-        }
-        if (status != KV_OK || n == 0) {
-            // failed (or empty): completed here, nothing released
+        const int32_t status = check_descriptor(k, kind, n, pool, layer, a_r, b_r, s_a, s_b, s_key,
+                                                &s_first_bad, &s_first_dup, &s_any_bad_a);
+        if (status != KV_OK) {   // rejected: completed at once, nothing moves
             if (tid == 0) {
-                st_release_sys(k.head, t);
-                if (status != KV_OK) {
-                    complete_failed(k, t, status);
-                } else {
-                    __threadfence_system();
-                    st_release_sys((unsigned long long *)&k.comp[slot].done, t);
-                }
+                st_relaxed_sys64(k.head, t);
+                complete_failed(k, t, status);
             }
-            ++served;
             __syncthreads();
             continue;
         }
-        // release it to every CTA
-#pragma unroll
-        for (int h = 0; h < kIdsPerThread; ++h) {
-            const uint32_t i = tid + h * kThreads;
-            if (i < n) {
-                k.ids[i] = a_r[h];
-                k.ids[kMaxIds + i] = b_r[h];
+        // accepted: it runs after the one released before it has ended
+        if (tid == 0) {
+            st_relaxed_sys64(k.head, t);
+            s_done = released == 0 ? 1 : wait_arrivals(k, movers * released);
+        }
+        __syncthreads();
+        if (!s_done) {
+            server_status = KV_ERR_TIMEOUT;
+            break;
+        }
+        if (n == 0) {   // empty: complete once everything before it is
+            if (tid == 0) {
+                __threadfence_system();
+                st_release_sys((unsigned long long *)&k.comp[slot].done, t);
             }
+            __syncthreads();
+            continue;
+        }
+        // release it to the movers
+        for (uint32_t i = tid; i < n; i += kThreads) {
+            k.ids[i] = s_a[i];
+            k.ids[kMaxIds + i] = s_b[i];
         }
         __threadfence();
         __syncthreads();
@@ -405,35 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
             ctl->pool = pool;
             ctl->layer = layer;
             ctl->ticket = t;
-            st_release_sys(k.head, t);
             __threadfence();
             st_release_gpu(&ctl->gen, released);
         }
-        move_share(k, k.pools[pool], kind, n, layer, s_a, s_b);
-        arrive(k, released, t);
-        // every CTA done with it before the next descriptor reuses the scratch
-        if (tid == 0) {
-            int ok = 0;
-            const unsigned long long deadline = now_ns() + kSlackNs;
-            for (unsigned long long polls = 0;; ++polls) {
-                if (ld_acquire_gpu(&ctl->arrived) >= gridDim.x * released) { ok = 1; break; }
-                if (ld_acquire_gpu(&ctl->gave_up) != 0 || polls >= kSlackNs / 16ull ||
-                    ((polls & 63u) == 63u && now_ns() > deadline))
-                    break;
-                __nanosleep(64);
-            }
-            s_done = ok;
-        }
-        __syncthreads();
-        ++served;
-        if (!s_done) {
-            server_status = KV_ERR_TIMEOUT;
-            break;
-        }
+        __syncthreads();   // s_hdr, s_a and s_b are rewritten by the next take
     }
+    // every released descriptor ends before the movers are told to stop
     if (tid == 0) {
+        if (released > 0 && !wait_arrivals(k, movers * released)) server_status = KV_ERR_TIMEOUT;
         if (ld_acquire_gpu(&ctl->gave_up) != 0) server_status = KV_ERR_TIMEOUT;
-        st_relaxed_sys32(k.result, served);
+        st_relaxed_sys32(k.result, taken);
         st_relaxed_sys32(k.result + 1, (uint32_t)server_status);
         __threadfence_system();
         st_release_gpu(&ctl->stop, 1u);
@@ -449,7 +498,7 @@ cudaError_t preload_ring_kernels() {
 
 cudaError_t launch_ring_server(const RingKDesc &k, int ctas, cudaStream_t stream) {
     (void)cudaGetLastError();
-    if (ctas < 1) return cudaErrorInvalidValue;
+    if (ctas < 2) return cudaErrorInvalidValue;   // a leader and at least one mover
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3((unsigned)kThreads);

@@ -441,8 +441,8 @@ KVB_API kv_status kv_ring_complete(kv_ring ring, uint64_t ticket, kv_status op_s
 
 /* Server on the GPU ([RFC] §Device IPC data path: a high-frequency path as an
  * NVMe-style submission / completion queue).  Enqueues on `stream` one
- * resident kernel (a cooperative grid of 32 CTAs of 256 threads, holding 32
- * SMs for as long as it runs) that takes
+ * resident kernel (a cooperative grid of 33 CTAs of 256 threads -- a leader
+ * and 32 movers -- holding 33 SMs for as long as it runs) that takes
  * descriptors from the ring itself -- polling the tail in the shared segment,
  * which is mapped into the GPU -- checks each exactly as kv_ring_serve would
  * (the same status for every rejected descriptor: INVALID_ARG for a kind, n,
