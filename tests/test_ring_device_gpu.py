@@ -49,14 +49,15 @@ def replay(g, rig_offset, snap, ops, statuses):
     return pool, host
 
 
-def random_ops(r, g, S, count, npools=1):
+def random_ops(r, g, S, count, npools=1, n_range=(0, 12)):
     """Seeded descriptors: backups and whole / one-layer restores, some of them
     made invalid (ids out of range or negative, repeated write targets, a bad
     layer, a pool index past the table, a backup with a layer)."""
     ops = []
     for _ in range(count):
         kind = int(r.integers(2))
-        n = int(r.integers(0, min(12, S, g.P) + 1))
+        hi = min(n_range[1], S, g.P)
+        n = int(r.integers(min(n_range[0], hi), hi + 1))
         if kind == kvb.KV_RING_OP_BACKUP:
             a = r.integers(0, g.P, n)
             b = r.permutation(S)[:n]
@@ -180,6 +181,29 @@ def test_device_server_agrees_with_host_server_on_random_descriptors(case):
     stream = torch.cuda.Stream()
     h_snap, h_after, h_st, h_served = run_host(g, offset, 100 + case, S, ops, stream)
     d_snap, d_after, d_st, (served, st) = run_device(g, offset, 100 + case, S, ops, stream)
+    assert d_st == h_st, (d_st, h_st)
+    assert (served, st) == (len(ops), kvb.KV_OK) and h_served == len(ops)
+    want = replay(g, offset, d_snap, ops, d_st)
+    assert np.array_equal(d_after[0], want[0]) and np.array_equal(d_after[1], want[1])
+    assert np.array_equal(h_after[0], want[0]) and np.array_equal(h_after[1], want[1])
+
+
+@pytest.mark.parametrize("case", range(CASES // 3))
+def test_device_server_agrees_with_host_server_on_large_descriptors(case):
+    """As above with 33 to 1,024 ids per descriptor (the block-wide duplicate
+    check rather than the one-warp one), on pools of many small pages."""
+    r = np.random.default_rng(6000 + case)
+    order, dev, host = (int(x) for x in r.integers(0, 2, 3))
+    g = wl.Geometry(L=int(r.integers(1, 4)), C=int(r.integers(1, 3)),
+                    P=int(r.integers(300, 1300)), T=int(r.integers(1, 9)),
+                    H=int(r.integers(1, 5)), B=16 * int(r.integers(1, 5)),
+                    order=order, dev_heads=dev, host_heads=host)
+    S = int(r.integers(100, 1100))
+    offset = 16 * int(r.integers(0, 64))
+    ops = random_ops(r, g, S, int(r.integers(3, 9)), n_range=(33, 1024))
+    stream = torch.cuda.Stream()
+    h_snap, h_after, h_st, h_served = run_host(g, offset, 300 + case, S, ops, stream)
+    d_snap, d_after, d_st, (served, st) = run_device(g, offset, 300 + case, S, ops, stream)
     assert d_st == h_st, (d_st, h_st)
     assert (served, st) == (len(ops), kvb.KV_OK) and h_served == len(ops)
     want = replay(g, offset, d_snap, ops, d_st)
