@@ -339,3 +339,44 @@ def test_device_server_stops_on_request_and_on_close():
             kvb.kv_ring_close(srv)
         kvb.kv_ring_close(sub)
         rig.close()
+
+
+def test_two_resident_servers_at_once():
+    """Two rings, each with its own resident server on its own stream (both
+    grids resident together): backups through one ring and restores through
+    the other, over disjoint pages and slots, submitted interleaved; the pool
+    and host tier equal the oracle's."""
+    g = wl.LLAMA8B.geom.with_(P=256)
+    S = 96
+    rig = Rig(g, S, seed=51)
+    sub_a, srv_a = ring_pair(8)
+    sub_b, srv_b = ring_pair(8)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    r = np.random.default_rng(52)
+    pages = r.permutation(g.P)
+    back_src, rest_dst = pages[:96], pages[96:192]
+    back_slots, rest_slots = np.arange(0, 48), np.arange(48, 96)
+    try:
+        snap = rig.snapshot()
+        fa = kvb.kv_ring_serve_device(srv_a, [rig.pool], rig.hostt, sa.cuda_stream, 4, WAIT // 10)
+        fb = kvb.kv_ring_serve_device(srv_b, [rig.pool], rig.hostt, sb.cuda_stream, 4, WAIT // 10)
+        ta, tb = [], []
+        for c in range(4):
+            q = slice(12 * c, 12 * c + 12)
+            ta.append(kvb.kv_ring_submit(sub_a, kvb.make_ring_op(0, back_src[q], back_slots[q])))
+            tb.append(kvb.kv_ring_submit(sub_b, kvb.make_ring_op(1, rest_slots[q], rest_dst[q])))
+        assert [kvb.kv_ring_wait(sub_a, t, WAIT) for t in ta] == [0] * 4
+        assert [kvb.kv_ring_wait(sub_b, t, WAIT) for t in tb] == [0] * 4
+        kvb.kv_fence_wait(fa, WAIT)
+        kvb.kv_fence_wait(fb, WAIT)
+        assert kvb.kv_ring_device_result(srv_a) == (4, kvb.KV_OK)
+        assert kvb.kv_ring_device_result(srv_b) == (4, kvb.KV_OK)
+        og = oracle_geom(g)
+        pool, host = snap[0].copy(), snap[1].copy()
+        oracle.restore(og, pool, snap[1], rest_slots[:48], rest_dst[:48], threads=8)
+        oracle.backup(og, snap[0], host, back_src[:48], back_slots, threads=8)
+        rig.assert_equal((pool, host))
+    finally:
+        for h in (srv_a, srv_b, sub_a, sub_b):
+            kvb.kv_ring_close(h)
+        rig.close()
