@@ -878,42 +878,51 @@ def run_ours(args):
                                                   statistics.median(times[1:]) / GB, 2)
         # two rings, each with its own resident server: 4 x 64-page backups into
         # slots 0..255 through one, 4 x 64-page restores from slots 256..511
-        # through the other (disjoint pages and slots), both directions at once
-        names = [f"/kvbbenchbi_{os.getpid()}_{x}" for x in "ab"]
-        subs = [kvb.kv_ring_create(nm, 16) for nm in names]
-        srvs = [kvb.kv_ring_attach(nm) for nm in names]
-        streams = [torch.cuda.Stream(device=dev) for _ in names]
-        fences = [kvb.kv_ring_serve_device(sv, [pool], tier, st.cuda_stream, 4 * steps_r,
-                                           5_000_000_000) for sv, st in zip(srvs, streams)]
-        times = []
-        q = w.n // 8
-        for i in range(steps_r):
-            ids = idsets[i % R]
-            tks = []
-            for c in range(4):
-                sl = slice(c * q, (c + 1) * q)
-                if c == 0:
-                    t0 = time.perf_counter()
-                tks.append((0, kvb.kv_ring_submit(subs[0], kvb.make_ring_op(
-                    0, ids.backup_src[sl], np.arange(c * q, (c + 1) * q)))))
-                tks.append((1, kvb.kv_ring_submit(subs[1], kvb.make_ring_op(
-                    1, np.arange(w.n // 2 + c * q, w.n // 2 + (c + 1) * q),
-                    ids.restore_dst[sl]))))
-            sts = [kvb.kv_ring_wait(subs[j], tk, 30_000_000_000) for j, tk in tks]
-            times.append(time.perf_counter() - t0)
-            if any(sts):
-                raise RuntimeError(f"two-ring step {i}: statuses {sts}")
-        for f in fences:
-            kvb.kv_fence_wait(f, 30_000_000_000)
-        for h in srvs + subs:
-            kvb.kv_ring_close(h)
-        ring_tp["device_served_two_rings_gbs"] = round(w.n * g.page_bytes /
-                                                       statistics.median(times[1:]) / GB, 2)
+        # through the other (disjoint pages and slots), both directions at once;
+        # with the default 32 movers per server and with 64 (kv_config.max_ctas)
+        def two_rings_gbs(movers):
+            old_cfg = kvb.kv_config_get()
+            kvb.kv_config_set(old_cfg.mode, movers, old_cfg.staging_bytes, old_cfg.flags,
+                              old_cfg.cta_threads)
+            names = [f"/kvbbenchbi_{os.getpid()}_{x}{movers}" for x in "ab"]
+            subs = [kvb.kv_ring_create(nm, 16) for nm in names]
+            srvs = [kvb.kv_ring_attach(nm) for nm in names]
+            streams = [torch.cuda.Stream(device=dev) for _ in names]
+            fences = [kvb.kv_ring_serve_device(sv, [pool], tier, st.cuda_stream, 4 * steps_r,
+                                               5_000_000_000) for sv, st in zip(srvs, streams)]
+            times = []
+            q = w.n // 8
+            for i in range(steps_r):
+                ids = idsets[i % R]
+                ops_a = [kvb.make_ring_op(0, ids.backup_src[c * q:(c + 1) * q],
+                                          np.arange(c * q, (c + 1) * q)) for c in range(4)]
+                ops_b = [kvb.make_ring_op(1, np.arange(w.n // 2 + c * q, w.n // 2 + (c + 1) * q),
+                                          ids.restore_dst[c * q:(c + 1) * q]) for c in range(4)]
+                t0 = time.perf_counter()
+                tks = []
+                for oa, ob in zip(ops_a, ops_b):
+                    tks.append((0, kvb.kv_ring_submit(subs[0], oa)))
+                    tks.append((1, kvb.kv_ring_submit(subs[1], ob)))
+                sts = [kvb.kv_ring_wait(subs[j], tk, 30_000_000_000) for j, tk in tks]
+                times.append(time.perf_counter() - t0)
+                if any(sts):
+                    raise RuntimeError(f"two-ring step {i}: statuses {sts}")
+            for f in fences:
+                kvb.kv_fence_wait(f, 30_000_000_000)
+            for h in srvs + subs:
+                kvb.kv_ring_close(h)
+            kvb.kv_config_set(old_cfg.mode, old_cfg.max_ctas, old_cfg.staging_bytes,
+                              old_cfg.flags, old_cfg.cta_threads)
+            return round(w.n * g.page_bytes / statistics.median(times[1:]) / GB, 2)
+
+        ring_tp["device_served_two_rings_gbs"] = two_rings_gbs(0)
+        ring_tp["device_served_two_rings_64_movers_gbs"] = two_rings_gbs(64)
         ring_tp["workload"] = ("Llama-8B step as 8 ring descriptors (4 x 128-page backups, then "
                                "4 x 128-page restores; 2 GiB), all submitted at once, host clock "
                                "from the first submit to the last ticket, median of 5 steps; "
                                "two_rings: 4 x 64-page backups and 4 x 64-page restores on two "
-                               "rings with a resident server each, at once (1 GiB per step)")
+                               "rings with a resident server each (32 movers, or 64), at once "
+                               "(1 GiB per step)")
         latency["ring_throughput"] = ring_tp
         kvb.kv_pool_close(tpool)
         kvb.kv_host_close(ttier)

@@ -504,7 +504,11 @@ kv_status kv_ring_serve_device(kv_ring r, const kv_pool *pools, uint32_t npools,
     }
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    const int ctas = 1 + std::max(1, std::min(kvb::kRingMovers, sms - 1));   // leader + movers
+    // leader + movers: kRingMovers, or the configured CTA cap of move kernels
+    kv_config cfg{};
+    const int want = kv_config_get(&cfg) == KV_OK && cfg.max_ctas != 0 ? (int)cfg.max_ctas
+                                                                      : kvb::kRingMovers;
+    const int ctas = 1 + std::max(1, std::min(want, sms - 1));
     cudaStream_t s = (cudaStream_t)stream;
     o->srv_result[0] = 0;
     o->srv_result[1] = (uint32_t)KV_OK;

@@ -157,7 +157,8 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
  * size on every host-link move (64 CTAs of 256, 16 of 1024). */
 typedef struct {
     uint32_t mode;           /* kv_mode                                         */
-    uint32_t max_ctas;       /* CTA cap of the transfer kernel; 0 = default     */
+    uint32_t max_ctas;       /* CTA cap of the transfer kernels, and the mover
+                                CTAs of a resident ring server; 0 = default    */
     uint64_t staging_bytes;  /* STAGED: device staging bytes; 0 = default       */
     uint32_t flags;          /* KV_CFG_* bits                                   */
     uint32_t cta_threads;    /* host-link CTA size: 0 = default, 256, 1024      */
@@ -441,8 +442,9 @@ KVB_API kv_status kv_ring_complete(kv_ring ring, uint64_t ticket, kv_status op_s
 
 /* Server on the GPU ([RFC] §Device IPC data path: a high-frequency path as an
  * NVMe-style submission / completion queue).  Enqueues on `stream` one
- * resident kernel (a cooperative grid of 33 CTAs of 256 threads -- a leader
- * and 32 movers -- holding 33 SMs for as long as it runs) that takes
+ * resident kernel (a cooperative grid of CTAs of 256 threads -- a leader and
+ * 32 movers, or kv_config.max_ctas movers when that is set -- holding that
+ * many SMs for as long as it runs) that takes
  * descriptors from the ring itself -- polling the tail in the shared segment,
  * which is mapped into the GPU -- checks each exactly as kv_ring_serve would
  * (the same status for every rejected descriptor: INVALID_ARG for a kind, n,
