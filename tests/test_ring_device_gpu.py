@@ -380,3 +380,25 @@ def test_two_resident_servers_at_once():
         for h in (srv_a, srv_b, sub_a, sub_b):
             kvb.kv_ring_close(h)
         rig.close()
+
+
+@pytest.mark.parametrize("movers", [1, 7, 64])
+def test_device_server_with_other_mover_counts(movers):
+    """kv_config.max_ctas sets the resident server's mover CTAs: one, an odd
+    count and 64 give the same results and statuses as the oracle and the
+    host server."""
+    r = np.random.default_rng(7000 + movers)
+    g = wl.Geometry(L=3, C=2, P=200, T=8, H=4, B=64, order=wl.PAGE_FIRST, dev_heads=wl.HND)
+    S = 150
+    ops = random_ops(r, g, S, 10, n_range=(1, 120))
+    old = kvb.kv_config_get()
+    stream = torch.cuda.Stream()
+    try:
+        h_snap, h_after, h_st, _ = run_host(g, 48, 90 + movers, S, ops, stream)
+        kvb.kv_config_set(old.mode, movers, old.staging_bytes, old.flags, old.cta_threads)
+        d_snap, d_after, d_st, (served, st) = run_device(g, 48, 90 + movers, S, ops, stream)
+    finally:
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+    assert d_st == h_st and (served, st) == (len(ops), kvb.KV_OK)
+    want = replay(g, 48, d_snap, ops, d_st)
+    assert np.array_equal(d_after[0], want[0]) and np.array_equal(d_after[1], want[1])
