@@ -616,6 +616,44 @@ def run_ours(args):
                    "pipelined_progressive_ms": round(t_p2, 3),
                    "exposed_transfer_ms_per_layer_calls": round(t_p1 - t_c, 3),
                    "exposed_transfer_ms_progressive": round(t_p2 - t_c, 3)}
+
+        # ---- the SM budget that saturates the host link: the progressive
+        # restore (H2D) and a backup of the same 64 pages (D2H) on k whole SMs
+        # (k CTAs of 1024 threads, one per SM), alone and, for the restore,
+        # pipelined with the stand-in forward above
+        def restore_prog(i):
+            ids = idsets[i % R]
+            kvb.kv_restore_layers(pool, tier, ids.restore_slots, ids.restore_dst, 0, g.L,
+                                  s_a.cuda_stream)
+
+        def backup_pages(i):
+            ids = idsets[i % R]
+            kvb.kv_backup(pool, tier, ids.restore_dst, ids.restore_slots, s_a.cuda_stream)
+
+        cfg0 = kvb.kv_config_get()
+        budget = []
+        try:
+            for k in (1, 2, 3, 4, 6, 8, 12, 16):
+                kvb.kv_config_set(cfg0.mode, k, cfg0.staging_bytes, cfg0.flags, 1024)
+                t_rk = timed(restore_prog, s_a)
+                t_bk = timed(backup_pages, s_a)
+                t_pk = timed(lambda i: pipelined(i, True), s_a)
+                budget.append({"sms": k,
+                               "restore_gbs": round(bytes_r / t_rk * 1000 / GB, 2),
+                               "restore_pct_h2d": round(100 * bytes_r / t_rk * 1000 / GB /
+                                                        link["h2d"], 1),
+                               "backup_gbs": round(bytes_r / t_bk * 1000 / GB, 2),
+                               "backup_pct_d2h": round(100 * bytes_r / t_bk * 1000 / GB /
+                                                       link["d2h"], 1),
+                               "pipelined_progressive_ms": round(t_pk, 3)})
+        finally:
+            kvb.kv_config_set(cfg0.mode, cfg0.max_ctas, cfg0.staging_bytes, cfg0.flags,
+                              cfg0.cta_threads)
+        overlap["sm_budget"] = {
+            "what": "k CTAs of 1024 threads (k whole SMs): kv_restore_layers of 61 layers x 64 "
+                    "pages (H2D), kv_backup of the same 64 pages (D2H), each alone (median "
+                    "of 5), and the restore pipelined with the per-layer GEMMs",
+            "rows": budget}
         del A, Bm, Cm
 
     # ---- Llama-8B: write-through backup beside the prefill that fills the pages.
