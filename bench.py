@@ -638,6 +638,8 @@ def run_ours(args):
                 t_rk = timed(restore_prog, s_a)
                 t_bk = timed(backup_pages, s_a)
                 t_pk = timed(lambda i: pipelined(i, True), s_a)
+                t_lk = timed(restore_only, s_a)
+                t_qk = timed(lambda i: pipelined(i, False), s_a)
                 budget.append({"sms": k,
                                "restore_gbs": round(bytes_r / t_rk * 1000 / GB, 2),
                                "restore_pct_h2d": round(100 * bytes_r / t_rk * 1000 / GB /
@@ -645,14 +647,17 @@ def run_ours(args):
                                "backup_gbs": round(bytes_r / t_bk * 1000 / GB, 2),
                                "backup_pct_d2h": round(100 * bytes_r / t_bk * 1000 / GB /
                                                        link["d2h"], 1),
-                               "pipelined_progressive_ms": round(t_pk, 3)})
+                               "pipelined_progressive_ms": round(t_pk, 3),
+                               "per_layer_calls_gbs": round(bytes_r / t_lk * 1000 / GB, 2),
+                               "pipelined_per_layer_calls_ms": round(t_qk, 3)})
         finally:
             kvb.kv_config_set(cfg0.mode, cfg0.max_ctas, cfg0.staging_bytes, cfg0.flags,
                               cfg0.cta_threads)
         overlap["sm_budget"] = {
             "what": "k CTAs of 1024 threads (k whole SMs): kv_restore_layers of 61 layers x 64 "
-                    "pages (H2D), kv_backup of the same 64 pages (D2H), each alone (median "
-                    "of 5), and the restore pipelined with the per-layer GEMMs",
+                    "pages (H2D), kv_backup of the same 64 pages (D2H) and the 61 one-layer "
+                    "kv_restore calls, each alone (median of 5), and both restores pipelined "
+                    "with the per-layer GEMMs",
             "rows": budget}
         del A, Bm, Cm
 
