@@ -782,3 +782,67 @@ print("call_s", call)
     assert out.returncode == 0, out.stdout + out.stderr
     call = float(out.stdout.split("call_s")[1])
     assert call < 2.0, f"the gated call waited {call:.2f} s for its own gate"
+
+
+@pytest.mark.parametrize("threads", [256, 1024])
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5])
+@pytest.mark.parametrize("lay", [(0, 0, 0), (1, 1, 0), (0, 0, 1)],
+                         ids=["LF-NHD>NHD", "PF-HND>NHD", "LF-NHD>HND"])
+def test_few_ctas_match_the_oracle(lay, ctas, threads):
+    """Grids capped at 1-5 CTAs (the SM-budget shapes of the benchmark): every
+    warp walks many segments by grid stride, a progressive restore's warps take
+    every layer's tickets, and the last CTA still completes each fence.  A
+    ragged geometry (5,760-byte chunks: one full 4 KiB segment and a short one)
+    on every op kind against the oracle."""
+    order, dev, host = lay
+    g = wl.Geometry(L=3, C=2, P=40, T=24, H=5, B=48, order=order, dev_heads=dev,
+                    host_heads=host)
+    r = np.random.default_rng(1700 + 10 * ctas + threads // 256 + 100 * order + 7 * host)
+    n = 17
+    rig = Rig(g, 24, pool_offset=48, seed=1750 + ctas)
+    og = oracle_geom(g)
+    old = kvb.kv_config_get()
+    try:
+        kvb.kv_config_set(kvb.KV_MODE_ZERO_COPY, ctas, 0, 0, threads)
+        src = r.permutation(g.P)[:n].astype(np.int32)
+        slots = r.permutation(24)[:n].astype(np.int32)
+        dst = np.setdiff1d(np.arange(g.P), src)[r.permutation(g.P - n)[:n]].astype(np.int32)
+
+        snap = rig.snapshot()
+        want = rig.expect_backup(snap, src, slots)
+        kvb.kv_fence_wait(kvb.kv_backup(rig.pool, rig.hostt, src, slots), 20_000_000_000)
+        rig.assert_equal(want)
+
+        snap = rig.snapshot()
+        want = rig.expect_restore(snap, slots, dst, layer=1)
+        kvb.kv_fence_wait(kvb.kv_restore(rig.pool, rig.hostt, slots, dst, 1), 20_000_000_000)
+        rig.assert_equal(want)
+
+        dst2 = src[::-1].copy()
+        snap = rig.snapshot()
+        want = rig.expect_restore(snap, slots, dst2, layer=-1)
+        kvb.kv_fence_wait(kvb.kv_restore(rig.pool, rig.hostt, slots, dst2, -1), 20_000_000_000)
+        rig.assert_equal(want)
+
+        snap = rig.snapshot()
+        want = (snap[0].copy(), snap[1])
+        for l in range(g.L):
+            oracle.restore(og, want[0], snap[1], slots[:9], dst[:9], layer=l,
+                           pool_offset=rig.offset)
+        fences = kvb.kv_restore_layers(rig.pool, rig.hostt, slots[:9], dst[:9], 0, g.L)
+        for f in fences:
+            kvb.kv_fence_wait(f, 20_000_000_000)
+        rig.assert_equal(want)
+
+        # HBM-only gather with the same cap (bulk or transposing kernel, or the
+        # register kernel with 1024-thread CTAs)
+        pb = g.page_bytes
+        buf = torch.zeros(n * pb, dtype=torch.uint8, device="cuda")
+        want_buf = np.zeros(n * pb, dtype=np.uint8)
+        oracle.backup(og, want[0], want_buf, src, np.arange(n), pool_offset=rig.offset)
+        kvb.kv_fence_wait(kvb.kv_device_gather(rig.pool, buf.data_ptr(), buf.numel(),
+                                               g.host_heads, src), 20_000_000_000)
+        assert np.array_equal(buf.cpu().numpy(), want_buf)
+    finally:
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+        rig.close()
