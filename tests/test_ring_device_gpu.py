@@ -402,3 +402,57 @@ def test_device_server_with_other_mover_counts(movers):
     assert d_st == h_st and (served, st) == (len(ops), kvb.KV_OK)
     want = replay(g, 48, d_snap, ops, d_st)
     assert np.array_equal(d_after[0], want[0]) and np.array_equal(d_after[1], want[1])
+
+
+@pytest.mark.parametrize("case", range(4))
+def test_device_server_keeps_ticket_order_on_one_layer_restores(case):
+    """Streams of one-layer restores over a few layers -- consecutive ones at
+    the same layer into overlapping pages (the later write must win), at other
+    layers -- mixed with backups that read pages just restored and restores
+    that read slots just backed up, a large descriptor followed by a small one
+    so that a pair run out of order would show.  Bytes against the oracle's
+    replay in ticket order, every ticket OK."""
+    g = wl.Geometry(L=6, C=1, P=160, T=64, H=1, B=576, order=wl.LAYER_FIRST, dev_heads=wl.NHD,
+                    host_heads=wl.NHD)
+    S = 96
+    r = np.random.default_rng(4100 + case)
+    ops = []
+    for i in range(72):
+        x = r.random()
+        n = int(r.choice([64, 3])) if i % 2 == 0 else int(r.integers(1, 64))
+        if x < 0.12:                                     # backup of pages restored before
+            pages = r.integers(0, g.P, n)
+            ops.append((kvb.KV_RING_OP_BACKUP, pages, r.permutation(S)[:n], -1, 0))
+        elif x < 0.18:                                   # whole restore
+            ops.append((kvb.KV_RING_OP_RESTORE, r.integers(0, S, n), r.permutation(g.P)[:n],
+                        -1, 0))
+        else:                                            # one-layer restore, few layers
+            layer = int(r.integers(0, 3)) if case % 2 == 0 else int(r.integers(0, g.L))
+            dst = r.permutation(40)[:min(n, 40)]        # pages 0..39: consecutive ones overlap
+            ops.append((kvb.KV_RING_OP_RESTORE, r.integers(0, S, dst.size), dst, layer, 0))
+    stream = torch.cuda.Stream()
+    snap, after, statuses, (served, st) = run_device(g, 4096, 4200 + case, S, ops, stream)
+    assert statuses == [kvb.KV_OK] * len(ops)
+    assert (served, st) == (len(ops), kvb.KV_OK)
+    want = replay(g, 4096, snap, ops, statuses)
+    assert np.array_equal(after[0], want[0]), "pool allocation differs from the oracle"
+    assert np.array_equal(after[1], want[1]), "host tier differs from the oracle"
+
+
+def test_device_server_one_layer_restores_of_a_prefix():
+    """Every layer of a 64-page prefix as its own descriptor, layer after layer,
+    twice from different slots into the same pages: the second pass's bytes
+    win everywhere."""
+    g = wl.MLA_FP8.geom.with_(P=96)
+    S = 72
+    r = np.random.default_rng(4300)
+    dst = r.permutation(g.P)[:64]
+    ops = [(kvb.KV_RING_OP_RESTORE, r.permutation(S)[:64], dst, l, 0) for l in range(g.L)]
+    ops += [(kvb.KV_RING_OP_RESTORE, r.permutation(S)[:64], dst, l, 0) for l in range(g.L)]
+    stream = torch.cuda.Stream()
+    snap, after, statuses, (served, st) = run_device(g, 0, 4301, S, ops, stream)
+    assert statuses == [kvb.KV_OK] * len(ops)
+    assert (served, st) == (len(ops), kvb.KV_OK)
+    want = replay(g, 0, snap, ops, statuses)
+    assert np.array_equal(after[0], want[0]), "pool allocation differs from the oracle"
+    assert np.array_equal(after[1], want[1]), "host tier differs from the oracle"
