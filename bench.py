@@ -267,6 +267,36 @@ def oracle_sample(cpu_seconds: float, steps: int | None = None, n_sample: int = 
     return per_step * k / total / GB, used, sample, times
 
 
+def numpy_statement_sample(cpu_seconds: float, n_sample: int = 64, pool_pages: int = 128):
+    """Times the oracle's numpy statement (views and fancy indexing, one thread)
+    as it stands on the Llama-8B geometry: backup of n_sample random pages, then
+    restore into n_sample others.  Each call returns a new array, so a restore
+    also copies the whole pool: the figure depends on the pool's size, stated in
+    the sample.  Returns (GB/s, sample text)."""
+    from oracle import numpy_statement as nps
+
+    g = wl.LLAMA8B.geom.with_(P=pool_pages)
+    pool = np.full(g.pool_bytes, 7, dtype=np.uint8)
+    host = np.full(n_sample * g.page_bytes, 3, dtype=np.uint8)
+    r = wl.rng(wl.LLAMA8B.seed + 1)
+    per_step = 2 * n_sample * g.page_bytes
+    times = []
+    t_all = time.perf_counter()
+    while not times or (time.perf_counter() - t_all < cpu_seconds and len(times) < 200):
+        src = wl.distinct_pages(r, g.P, n_sample)
+        dst = wl.distinct_pages(r, g.P, n_sample, exclude=src)
+        slots = np.arange(n_sample, dtype=np.int32)
+        t0 = time.perf_counter()
+        host = nps.backup(pool, g, g.order, g.dev_heads, host, n_sample, g.host_heads, src, slots)
+        pool = nps.restore(pool, g, g.order, g.dev_heads, host, n_sample, g.host_heads, slots,
+                           dst, -1)
+        times.append(time.perf_counter() - t0)
+    sample = (f"{len(times)} x (backup {n_sample} random pages + restore {n_sample}) of the "
+              f"Llama-8B geometry on a {pool_pages}-page host pool ({per_step / 2**20:.0f} MiB "
+              f"moved per step; each restore also copies the {g.pool_bytes / 2**20:.0f} MiB pool)")
+    return per_step * len(times) / sum(times) / GB, sample
+
+
 def run_reference(args):
     rank, _, ws = dist_env()
     if rank != 0:
@@ -1114,6 +1144,10 @@ def run_ours(args):
                                             threads=1)
         line["cpu_baseline_single_thread"] = {"value": round(gbs1, 3), "unit": "GB/s",
                                               "cores": 1, "kind": "oracle", "sample": sample1}
+        gbs2, sample2 = numpy_statement_sample(max(1.0, args.cpu_seconds / 4))
+        line["cpu_baseline_numpy_statement"] = {"value": round(gbs2, 3), "unit": "GB/s",
+                                                "cores": 1, "kind": "oracle (numpy statement)",
+                                                "sample": sample2}
     else:
         line["cpu_baseline"] = None
     kvb.kv_pool_close(pool)

@@ -17,8 +17,8 @@ What pins what:
     [NB, NL, 2, NH, BS, HS], kv_layout HND) from the LMCache page, as a golden
     fixture.
   * ``pin_numpy_restatement`` -- the whole operation restated with numpy
-    transposes and fancy indexing on random bytes (a second, independent
-    statement of the same definition).
+    transposes and fancy indexing on random bytes (``oracle/numpy_statement.py``,
+    a second, independent statement of the same definition).
   * ``pin_invariants`` -- restore(backup(x)) is the identity, base+offset
     addressing, layer-by-layer restore equals whole-prefix restore, every device
     layout of the same logical KV gives the same host tier, threaded = serial.
@@ -38,29 +38,17 @@ import os
 import numpy as np
 
 import oracle
+from oracle import numpy_statement as nps
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
-# (order, heads) -> axis names of the device pool, row-major, before the byte axis.
-DEV_AXES = {
-    (0, 0): ("l", "c", "p", "t", "h"),   # layer-first NHD
-    (0, 1): ("l", "c", "p", "h", "t"),   # layer-first HND
-    (1, 0): ("p", "l", "c", "t", "h"),   # page-first NHD
-    (1, 1): ("p", "l", "c", "h", "t"),   # page-first HND  (TRT-LLM 6-D view)
-}
-HOST_AXES = {0: ("s", "l", "c", "t", "h"), 1: ("s", "l", "c", "h", "t")}
-LAYOUTS = [(o, d, hh) for (o, d) in DEV_AXES for hh in (0, 1)]
-
-
-def _shape(axes, dims):
-    return tuple(dims[a] for a in axes)
-
-
-def _dims(g, S=None):
-    d = {"l": g.L, "c": g.C, "p": g.P, "t": g.T, "h": g.H}
-    if S is not None:
-        d["s"] = S
-    return d
+# The numpy statement (oracle/numpy_statement.py, no code shared with the C
+# oracle): named-axis layouts, views and the two operations.
+DEV_AXES, HOST_AXES, LAYOUTS = nps.DEV_AXES, nps.HOST_AXES, nps.LAYOUTS
+_shape, _dims = nps.shape, nps.dims
+_pool_from_logical, _logical_from_pool = nps.pool_from_logical, nps.logical_from_pool
+_logical_from_host, _host_from_logical = nps.logical_from_host, nps.host_from_logical
+_np_backup, _np_restore = nps.backup, nps.restore
 
 
 def _geom(L, C, P, T, H, B, order, dev, host):
@@ -74,33 +62,6 @@ def _tag(coord, B, marker):
     v[5] = marker
     v[6:] = (np.arange(6, B) * 29 + sum(coord)) & 0xFF
     return v
-
-
-def _pool_from_logical(X, order, dev):
-    """X[p, l, c, t, h, :] -> flat pool bytes in the given device layout (numpy transpose)."""
-    src_axes = ("p", "l", "c", "t", "h")
-    perm = [src_axes.index(a) for a in DEV_AXES[(order, dev)]] + [5]
-    return np.ascontiguousarray(X.transpose(perm)).reshape(-1)
-
-
-def _logical_from_pool(pool, g, order, dev):
-    axes = DEV_AXES[(order, dev)]
-    arr = pool.reshape(_shape(axes, _dims(g)) + (g.B,))
-    perm = [axes.index(a) for a in ("p", "l", "c", "t", "h")] + [5]
-    return arr.transpose(perm)
-
-
-def _logical_from_host(host, g, S, hh):
-    axes = HOST_AXES[hh]
-    arr = host.reshape(_shape(axes, _dims(g, S)) + (g.B,))
-    perm = [axes.index(a) for a in ("s", "l", "c", "t", "h")] + [5]
-    return arr.transpose(perm)
-
-
-def _host_from_logical(Y, hh):
-    src_axes = ("s", "l", "c", "t", "h")
-    perm = [src_axes.index(a) for a in HOST_AXES[hh]] + [5]
-    return np.ascontiguousarray(Y.transpose(perm)).reshape(-1)
 
 
 # ----------------------------------------------------------------------- pins
@@ -227,23 +188,6 @@ def pin_trtllm_view(lib):
             got = raw[off:off + HS * eb]
             want = np.ascontiguousarray(six[nb, nl, kv, nh, bs]).view(np.uint8)
             assert np.array_equal(got, want), ("trtllm view", case, (nb, nl, kv, nh, bs))
-
-
-def _np_backup(pool, g, order, dev, host, S, hh, src, slots):
-    X = _logical_from_pool(pool, g, order, dev)
-    Y = _logical_from_host(host, g, S, hh).copy()
-    Y[np.asarray(slots)] = X[np.asarray(src)]
-    return _host_from_logical(Y, hh)
-
-
-def _np_restore(pool, g, order, dev, host, S, hh, slots, dst, layer):
-    X = _logical_from_pool(pool, g, order, dev).copy()
-    Y = _logical_from_host(host, g, S, hh)
-    if layer < 0:
-        X[np.asarray(dst)] = Y[np.asarray(slots)]
-    else:
-        X[np.asarray(dst), layer] = Y[np.asarray(slots), layer]
-    return _pool_from_logical(X, order, dev)
 
 
 def pin_numpy_restatement(lib, seed=7):
