@@ -9,6 +9,9 @@ method's arithmetic) feed both.
 
 The arithmetic lives in ``kv_oracle.c``; its header states the definition it
 restates and the pages it follows.  This module only marshals numpy buffers.
+``numpy_statement.py`` states the same definition a second time with numpy
+views and fancy indexing, sharing no code with the C file (the tests pin one
+against the other).
 """
 from __future__ import annotations
 
