@@ -40,7 +40,7 @@ struct RingPoolK {
 struct RingCtl {
     uint32_t gen;              // descriptors released to every CTA so far
     uint32_t stop;             // set by the leader once no more will be released
-    uint32_t arrived;          // CTA arrivals at descriptor ends, cumulative
+    uint32_t arrived;          // CTA arrivals at descriptor ends, cumulative mod 2^32
     uint32_t gave_up;          // a CTA's bounded wait ran out
     // the released descriptor
     uint32_t kind, n, pool;

@@ -228,10 +228,13 @@ __device__ __forceinline__ void complete_failed(const RingKDesc &k, uint64_t t, 
 }
 
 // Leader, thread 0: waits (bounded) until the movers' arrivals reach `want`.
+// Both count modulo 2^32 (movers x descriptors passes 2^32 after 2^32 / movers
+// descriptors); the count trails `want` by at most one descriptor's arrivals,
+// so the comparison is made on the signed difference.
 __device__ __forceinline__ int wait_arrivals(const RingKDesc &k, uint32_t want) {
     const unsigned long long deadline = now_ns() + kSlackNs;
     for (unsigned long long polls = 0;; ++polls) {
-        if (ld_acquire_gpu(&k.ctl->arrived) >= want) return 1;
+        if ((int32_t)(ld_acquire_gpu(&k.ctl->arrived) - want) >= 0) return 1;
         if (ld_acquire_gpu(&k.ctl->gave_up) != 0 || polls >= kSlackNs / 16ull ||
             ((polls & 63u) == 63u && now_ns() > deadline))
             return 0;
