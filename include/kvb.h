@@ -154,7 +154,11 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
  * peak); kv_restore_layers, made to run beside compute, runs 8 CTAs of 1024
  * threads (8 whole SMs); HBM-only moves run 4 CTAs of 256 threads per SM
  * (bulk-copy kernel: 3 per SM).  cta_threads = 256 or 1024 forces that CTA
- * size on every host-link move (64 CTAs of 256, 16 of 1024). */
+ * size on every host-link move (64 CTAs of 256, 16 of 1024).  Sizing the SM
+ * budget of moves that run beside compute: with cta_threads = 1024 each CTA
+ * holds one whole SM, and on GB300 one SM moves ~42-49 GB/s from the host
+ * tier and ~47 GB/s to it, so max_ctas = 6 reaches ~99% of the D2H link and
+ * ~96% of H2D, 8 reaches ~99% of both. */
 typedef struct {
     uint32_t mode;           /* kv_mode                                         */
     uint32_t max_ctas;       /* CTA cap of the transfer kernels, and the mover
