@@ -158,6 +158,7 @@ struct PoolObj {
     uint64_t instance_id, generation;
     bool imported;
     std::string ipc_key; // handle bytes of the mapping (imported pools)
+    std::vector<std::string> ipc_keys;   // imported split pools: each distinct mapping, once
     // split pools: one device buffer per (layer, component); the table of their
     // addresses (entry l * C + c) lives in device memory for the kernels
     unsigned long long *table_dev = nullptr;
@@ -1600,8 +1601,8 @@ kv_status kv_pool_export(kv_pool pool_h, kv_ipc_desc *out) {
     PoolObj *p = find_pool(pool_h);
     if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
     if (p->table_dev != nullptr)
-        return fail(KV_ERR_LAYOUT, "a split pool spans several allocations: one IPC "
-                    "descriptor cannot describe it");
+        return fail(KV_ERR_LAYOUT, "a split pool spans several allocations: export it with "
+                    "kv_pool_export_split");
     DeviceGuard guard(p->device);
     uintptr_t ab;
     size_t as;
@@ -1632,6 +1633,9 @@ kv_status kv_pool_export(kv_pool pool_h, kv_ipc_desc *out) {
 
 kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out) {
     if (desc == nullptr || out == nullptr) return fail(KV_ERR_INVALID_ARG, "NULL argument");
+    if (desc->magic == KVB_IPC_MAGIC_SPLIT)
+        return fail(KV_ERR_INVALID_ARG, "descriptor of a split pool: import it with "
+                    "kv_pool_import_split");
     if (desc->magic != KVB_IPC_MAGIC || desc->version != KVB_ABI_VERSION)
         return fail(KV_ERR_INVALID_ARG, "descriptor magic/version %08x/%u not recognised",
                     desc->magic, desc->version);
@@ -1709,6 +1713,189 @@ kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out) {
     return KV_OK;
 }
 
+kv_status kv_pool_export_split(kv_pool pool_h, kv_ipc_desc *out, kv_ipc_buffer *bufs,
+                               uint32_t nbufs) {
+    if (out == nullptr || bufs == nullptr) return fail(KV_ERR_INVALID_ARG, "NULL argument");
+    std::lock_guard<std::mutex> lk(g_mu);
+    PoolObj *p = find_pool(pool_h);
+    if (p == nullptr) return fail(KV_ERR_CLOSED, "pool handle is closed or unknown");
+    if (p->table_dev == nullptr)
+        return fail(KV_ERR_LAYOUT, "not a split pool: export it with kv_pool_export");
+    const uint64_t nb = p->g.L * p->g.C;
+    if (nbufs != nb)
+        return fail(KV_ERR_INVALID_ARG, "%u buffer entries for a pool of %llu buffers", nbufs,
+                    (unsigned long long)nb);
+    DeviceGuard guard(p->device);
+    std::vector<kv_ipc_buffer> tmp(nb);
+    std::unordered_map<uintptr_t, cudaIpcMemHandle_t> handles;   // one handle per allocation
+    for (uint64_t i = 0; i < nb; ++i) {
+        const uintptr_t ptr = (uintptr_t)p->table_host[i];
+        uintptr_t ab;
+        size_t as;
+        kv_status st = address_range((const void *)ptr, &ab, &as);
+        if (st != KV_OK) return st;
+        auto h = handles.find(ab);
+        if (h == handles.end()) {
+            cudaIpcMemHandle_t hd;
+            cudaError_t e = cudaIpcGetMemHandle(&hd, (void *)ab);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaIpcGetMemHandle(layer buffer allocation)");
+            h = handles.emplace(ab, hd).first;
+        }
+        static_assert(sizeof(h->second.reserved) == sizeof(tmp[i].handle), "IPC handle size");
+        std::memcpy(tmp[i].handle, h->second.reserved, sizeof tmp[i].handle);
+        tmp[i].alloc_offset = (uint64_t)(ptr - ab);
+    }
+    cudaDeviceProp prop;
+    cudaError_t e = cudaGetDeviceProperties(&prop, p->device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
+    kv_ipc_desc dsc;
+    std::memset(&dsc, 0, sizeof dsc);
+    dsc.magic = KVB_IPC_MAGIC_SPLIT;
+    dsc.version = KVB_ABI_VERSION;
+    std::memcpy(dsc.handle, tmp[0].handle, sizeof dsc.handle);
+    dsc.alloc_offset = tmp[0].alloc_offset;
+    dsc.nbytes = p->nbytes;
+    dsc.instance_id = p->instance_id;
+    dsc.generation = p->generation;
+    dsc.exporter_pid = (int64_t)getpid();
+    std::memcpy(dsc.device_uuid, prop.uuid.bytes, sizeof dsc.device_uuid);
+    dsc.layout = p->layout;
+    *out = dsc;
+    std::memcpy(bufs, tmp.data(), nb * sizeof(kv_ipc_buffer));
+    return KV_OK;
+}
+
+kv_status kv_pool_import_split(const kv_ipc_desc *desc, const kv_ipc_buffer *bufs, uint32_t nbufs,
+                               kv_pool *out) {
+    if (desc == nullptr || bufs == nullptr || out == nullptr)
+        return fail(KV_ERR_INVALID_ARG, "NULL argument");
+    if (desc->magic != KVB_IPC_MAGIC_SPLIT || desc->version != KVB_ABI_VERSION)
+        return fail(KV_ERR_INVALID_ARG, "not a split-pool descriptor (magic/version %08x/%u)",
+                    desc->magic, desc->version);
+    Geo g{};
+    kv_status st = check_layout(&desc->layout, &g);
+    if (st != KV_OK) return st;
+    if (g.order != KV_LAYER_FIRST)
+        return fail(KV_ERR_LAYOUT, "a split pool is layer-first: one buffer per layer and "
+                    "component");
+    const uint64_t nb = g.L * g.C;
+    if (nb > (1u << 20)) return fail(KV_ERR_LAYOUT, "too many layer buffers");
+    if (nbufs != nb)
+        return fail(KV_ERR_INVALID_ARG, "%u buffer entries for a pool of %llu buffers", nbufs,
+                    (unsigned long long)nb);
+    const uint64_t buf_bytes = g.P * g.cb;
+    if (desc->nbytes != buf_bytes * nb)
+        return fail(KV_ERR_LAYOUT, "descriptor nbytes %llu != %llu buffers of %llu bytes",
+                    (unsigned long long)desc->nbytes, (unsigned long long)nb,
+                    (unsigned long long)buf_bytes);
+    for (uint64_t i = 0; i < nb; ++i)
+        if (bufs[i].alloc_offset % 16 != 0)
+            return fail(KV_ERR_ALIGNMENT, "buffer %llu: alloc_offset %llu is not 16-byte aligned",
+                        (unsigned long long)i, (unsigned long long)bufs[i].alloc_offset);
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+    int device = -1;
+    for (int i = 0; i < ndev && device < 0; ++i) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, i) == cudaSuccess &&
+            std::memcmp(prop.uuid.bytes, desc->device_uuid, 16) == 0)
+            device = i;
+    }
+    if (device < 0) return fail(KV_ERR_INVALID_ARG, "no visible device has the descriptor's UUID");
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto fl = g_floor.find(desc->instance_id);
+    if (fl != g_floor.end() && desc->generation < fl->second)
+        return fail(KV_ERR_STALE, "descriptor generation %llu of instance %llu is retired",
+                    (unsigned long long)desc->generation, (unsigned long long)desc->instance_id);
+    DeviceGuard guard(device);
+    // each distinct allocation: its mapping (existing, or opened here) and size
+    struct Mapped {
+        void *base;
+        size_t size;
+        bool opened;
+    };
+    std::unordered_map<std::string, Mapped> mapped;
+    std::vector<std::string> keys;
+    auto undo = [&]() {
+        for (auto &m : mapped)
+            if (m.second.opened) cudaIpcCloseMemHandle(m.second.base);
+    };
+    std::vector<unsigned long long> table(nb);
+    for (uint64_t i = 0; i < nb; ++i) {
+        const std::string key((const char *)bufs[i].handle, sizeof bufs[i].handle);
+        auto m = mapped.find(key);
+        if (m == mapped.end()) {
+            Mapped mp{nullptr, 0, false};
+            auto it = g_maps.find(key);
+            if (it != g_maps.end()) {
+                mp.base = it->second.base;
+            } else {
+                cudaIpcMemHandle_t h;
+                std::memcpy(h.reserved, bufs[i].handle, sizeof bufs[i].handle);
+                if (fault_hit(FP_IPC_OPEN)) {
+                    undo();
+                    return fail(KV_ERR_CUDA, "cudaIpcOpenMemHandle: injected failure");
+                }
+                e = cudaIpcOpenMemHandle(&mp.base, h, cudaIpcMemLazyEnablePeerAccess);
+                if (e != cudaSuccess) {
+                    undo();
+                    return cuda_fail(e, "cudaIpcOpenMemHandle(layer buffer allocation)");
+                }
+                mp.opened = true;
+            }
+            uintptr_t ab = 0;
+            st = address_range(mp.base, &ab, &mp.size);
+            m = mapped.emplace(key, mp).first;   // recorded first, so undo() closes it
+            if (st != KV_OK) {
+                undo();
+                return st;
+            }
+            keys.push_back(key);
+        }
+        const uint64_t off = bufs[i].alloc_offset;
+        if (off > m->second.size || buf_bytes > m->second.size - off) {
+            undo();
+            return fail(KV_ERR_OUT_OF_RANGE, "buffer %llu (offset %llu + %llu bytes) overruns its "
+                        "imported allocation of %llu bytes", (unsigned long long)i,
+                        (unsigned long long)off, (unsigned long long)buf_bytes,
+                        (unsigned long long)m->second.size);
+        }
+        table[i] = (unsigned long long)((uintptr_t)m->second.base + off);
+    }
+    void *tdev = nullptr;
+    e = cudaMalloc(&tdev, nb * sizeof(unsigned long long));
+    if (e == cudaSuccess)
+        e = cudaMemcpy(tdev, table.data(), nb * sizeof(unsigned long long), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        if (tdev) cudaFree(tdev);
+        undo();
+        return cuda_fail(e, "copying the imported split pool's buffer table to the device");
+    }
+    PoolObj *p = new (std::nothrow) PoolObj{g, desc->layout, (char *)(uintptr_t)table[0],
+                                            desc->nbytes, device, desc->instance_id,
+                                            desc->generation, true, std::string()};
+    if (p == nullptr) {
+        cudaFree(tdev);
+        undo();
+        return fail(KV_ERR_NO_MEMORY, "out of host memory");
+    }
+    p->table_dev = (unsigned long long *)tdev;
+    p->table_host.swap(table);
+    p->ipc_keys = keys;
+    for (const std::string &key : keys) {
+        auto it = g_maps.find(key);
+        if (it != g_maps.end())
+            it->second.refs += 1;
+        else
+            g_maps[key] = Mapping{mapped[key].base, 1, device};
+    }
+    const uint64_t id = g_next_handle++;
+    g_pools[id] = p;
+    *out = (kv_pool)(uintptr_t)id;
+    return KV_OK;
+}
+
 kv_status kv_pool_close(kv_pool pool_h) {
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_pools.find(handle_id(pool_h));
@@ -1722,12 +1909,16 @@ kv_status kv_pool_close(kv_pool pool_h) {
             st = cuda_fail(cudaErrorUnknown, "cudaFree(split pool table)");
     }
     if (p->imported) {
-        auto m = g_maps.find(p->ipc_key);
-        if (m != g_maps.end() && --m->second.refs == 0) {
-            DeviceGuard guard(m->second.device);
-            cudaError_t e = cudaIpcCloseMemHandle(m->second.base);
-            g_maps.erase(m);
-            if (e != cudaSuccess) st = cuda_fail(e, "cudaIpcCloseMemHandle (mapping dropped)");
+        std::vector<std::string> keys = p->ipc_keys;
+        if (keys.empty()) keys.push_back(p->ipc_key);
+        for (const std::string &key : keys) {
+            auto m = g_maps.find(key);
+            if (m != g_maps.end() && --m->second.refs == 0) {
+                DeviceGuard guard(m->second.device);
+                cudaError_t e = cudaIpcCloseMemHandle(m->second.base);
+                g_maps.erase(m);
+                if (e != cudaSuccess) st = cuda_fail(e, "cudaIpcCloseMemHandle (mapping dropped)");
+            }
         }
     }
     delete p;

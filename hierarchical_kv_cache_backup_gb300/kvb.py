@@ -41,9 +41,11 @@ KV_MODE_ZERO_COPY, KV_MODE_STAGED, KV_MODE_COPY_ENGINE = 0, 1, 2
 KV_CFG_NO_BULK = 1
 KV_CFG_NO_PDL = 2
 KVB_IPC_MAGIC = 0x4B564231
+KVB_IPC_MAGIC_SPLIT = 0x4B564253
 
 # the symbols include/kvb.h declares
-EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_pool_import", "kv_pool_close",
+EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_pool_import",
+           "kv_pool_export_split", "kv_pool_import_split", "kv_pool_close",
            "kv_pool_retire", "kv_pool_info", "kv_host_register", "kv_host_close", "kv_backup",
            "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_restore_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
@@ -76,6 +78,10 @@ class kv_ipc_desc(ctypes.Structure):
                 ("device_uuid", ctypes.c_uint8 * 16), ("layout", kv_layout)]
 
 
+class kv_ipc_buffer(ctypes.Structure):
+    _fields_ = [("handle", ctypes.c_uint8 * 64), ("alloc_offset", ctypes.c_uint64)]
+
+
 KV_RING_MAX_IDS = 1024
 KV_RING_OP_BACKUP, KV_RING_OP_RESTORE = 0, 1
 
@@ -106,6 +112,8 @@ def _load():
         "kv_pool_register_split": (st, [P(kv_layout), P(vp), u64, u64, P(vp)]),
         "kv_pool_export": (st, [vp, P(kv_ipc_desc)]),
         "kv_pool_import": (st, [P(kv_ipc_desc), P(vp)]),
+        "kv_pool_export_split": (st, [vp, P(kv_ipc_desc), P(kv_ipc_buffer), u32]),
+        "kv_pool_import_split": (st, [P(kv_ipc_desc), P(kv_ipc_buffer), u32, P(vp)]),
         "kv_pool_close": (st, [vp]),
         "kv_pool_retire": (st, [u64, u64]),
         "kv_pool_info": (st, [vp, P(kv_layout), P(vp), P(u64)]),
@@ -230,6 +238,38 @@ def kv_pool_import(desc: kv_ipc_desc) -> int:
     out = ctypes.c_void_p()
     _check(_lib.kv_pool_import(ctypes.byref(desc), ctypes.byref(out)))
     return out.value
+
+
+def kv_pool_export_split(pool: int):
+    """A split pool as (kv_ipc_desc, array of L x C kv_ipc_buffer): the allocation handle and
+    offset of every layer buffer, for another process."""
+    lay, _, _ = kv_pool_info(pool)
+    nb = lay.num_layers * lay.num_comps
+    d, bufs = kv_ipc_desc(), (kv_ipc_buffer * nb)()
+    _check(_lib.kv_pool_export_split(pool, ctypes.byref(d), bufs, nb))
+    return d, bufs
+
+
+def kv_pool_import_split(desc: kv_ipc_desc, bufs) -> int:
+    """Maps a split pool exported by another process (each distinct allocation once,
+    refcounted); returns its handle."""
+    arr = (kv_ipc_buffer * len(bufs))(*bufs)
+    out = ctypes.c_void_p()
+    _check(_lib.kv_pool_import_split(ctypes.byref(desc), arr, len(bufs), ctypes.byref(out)))
+    return out.value
+
+
+def bufs_to_bytes(bufs) -> bytes:
+    """An array of kv_ipc_buffer as bytes (to send to another process)."""
+    return b"".join(ctypes.string_at(ctypes.addressof(b), ctypes.sizeof(b)) for b in bufs)
+
+
+def bufs_from_bytes(b: bytes):
+    """The kv_ipc_buffer entries bufs_to_bytes produced."""
+    n = ctypes.sizeof(kv_ipc_buffer)
+    if len(b) % n != 0:
+        raise ValueError(f"buffer entries are {n} bytes each, got {len(b)} bytes")
+    return [kv_ipc_buffer.from_buffer_copy(b[i:i + n]) for i in range(0, len(b), n)]
 
 
 def kv_pool_close(pool: int) -> None:

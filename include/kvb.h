@@ -127,6 +127,15 @@ typedef struct {
 } kv_ipc_desc;
 #define KVB_IPC_MAGIC 0x4B564231u /* "KVB1" */
 
+/* One buffer of a split pool over IPC: the handle of the allocation that holds
+ * it and the buffer's byte offset from that allocation's base.  Fixed-size
+ * POD.  A split pool's kv_ipc_desc carries KVB_IPC_MAGIC_SPLIT. */
+typedef struct {
+    uint8_t handle[64];        /* cudaIpcMemHandle_t of the allocation base    */
+    uint64_t alloc_offset;     /* buffer start minus allocation base, in bytes */
+} kv_ipc_buffer;
+#define KVB_IPC_MAGIC_SPLIT 0x4B564253u /* "KVBS" */
+
 /* Transfer modes.  ZERO_COPY: one kernel moves every byte between HBM and the
  * mapped pinned host tier over the host link.  STAGED: a kernel gathers /
  * scatters between the pool and a device staging buffer in host layout, and
@@ -190,7 +199,7 @@ KVB_API kv_status kv_pool_register(const kv_layout *layout, void *base, uint64_t
  * layout->order must be KV_LAYER_FIRST.  Each buffer: 16-B aligned, device
  * memory of one device, P x T x H x B bytes inside its allocation.  The
  * library keeps a device copy of the table (freed by kv_pool_close).  Split
- * pools cannot be exported over IPC (one descriptor names one allocation).
+ * pools travel over IPC with kv_pool_export_split / kv_pool_import_split.
  * Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, CUDA, NO_MEMORY. */
 KVB_API kv_status kv_pool_register_split(const kv_layout *layout, void *const *bases,
                                          uint64_t instance_id, uint64_t generation, kv_pool *out);
@@ -213,6 +222,29 @@ KVB_API kv_status kv_pool_export(kv_pool pool, kv_ipc_desc *out);
  * again).  Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, STALE, CUDA,
  * NO_MEMORY. */
 KVB_API kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out);
+
+/* Export of a split pool ([RFC] §Device IPC data path: REGISTER_KV_POOL
+ * carries the memory IPC handles of the scheduler's KV allocations, and the
+ * daemon imports those allocations once).  Writes the pool's descriptor to
+ * `out` (magic KVB_IPC_MAGIC_SPLIT; handle and alloc_offset of buffer 0;
+ * nbytes of all buffers; identity, device and layout as kv_pool_export) and
+ * to `bufs` (nbufs = L x C entries, entry l * C + c) the allocation handle and
+ * offset of every buffer; buffers that share an allocation carry the same
+ * handle.  Errors: INVALID_ARG (NULL, nbufs != L x C), CLOSED, LAYOUT (not a
+ * split pool: kv_pool_export), CUDA. */
+KVB_API kv_status kv_pool_export_split(kv_pool pool, kv_ipc_desc *out, kv_ipc_buffer *bufs,
+                                       uint32_t nbufs);
+
+/* Import of a split pool: maps every distinct allocation once per process (the
+ * registry kv_pool_import uses; the pool holds one reference per distinct
+ * allocation, dropped by kv_pool_close), checks each buffer's extent
+ * (alloc_offset + P x T x H x B) against its allocation, and builds the
+ * device table of buffer addresses.  Same identity checks as kv_pool_import
+ * (device UUID, retired generations: STALE); must run in a process other than
+ * the exporter.  On any error every mapping this call opened is closed again.
+ * Errors: INVALID_ARG, LAYOUT, ALIGNMENT, OUT_OF_RANGE, STALE, CUDA, NO_MEMORY. */
+KVB_API kv_status kv_pool_import_split(const kv_ipc_desc *desc, const kv_ipc_buffer *bufs,
+                                       uint32_t nbufs, kv_pool *out);
 
 /* Close ([RFC] DeviceMemoryIPC "close mapping"; [LMC] §重建生命周期与引用计数):
  * releases the handle; for an imported pool, drops one reference of its

@@ -192,6 +192,51 @@ def test_split_pool_checks_before_cuda():
         kvb.KV_ERR_INVALID_ARG
 
 
+def test_split_descriptor_checks_before_cuda():
+    """kv_pool_import_split refuses malformed split descriptors before any CUDA
+    call, kv_pool_import refuses a split descriptor, and the buffer entries
+    survive a bytes round trip."""
+    assert ctypes.sizeof(kvb.kv_ipc_buffer) == 72
+    L, C, P, T, H, B = 2, 2, 64, 16, 2, 128
+    d = kvb.kv_ipc_desc()
+    d.magic, d.version = kvb.KVB_IPC_MAGIC_SPLIT, 1
+    d.layout = lay(L=L, C=C, P=P, T=T, H=H, B=B)
+    d.nbytes = L * C * P * T * H * B
+    bufs = (kvb.kv_ipc_buffer * (L * C))()
+    for i, b in enumerate(bufs):
+        b.handle[0], b.alloc_offset = i, 4096 * i
+    again = kvb.bufs_from_bytes(kvb.bufs_to_bytes(bufs))
+    assert [b.alloc_offset for b in again] == [4096 * i for i in range(L * C)]
+    assert [b.handle[0] for b in again] == list(range(L * C))
+
+    def status(desc, entries):
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_pool_import_split(desc, entries)
+        return e.value.status
+
+    def copy(desc, **kw):
+        c = kvb.desc_from_bytes(kvb.desc_to_bytes(desc))
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c
+
+    assert status(copy(d, magic=kvb.KVB_IPC_MAGIC), bufs) == kvb.KV_ERR_INVALID_ARG
+    assert status(copy(d, layout=lay(L=L, C=C, P=P, T=T, H=H, B=B, order=1)), bufs) == \
+        kvb.KV_ERR_LAYOUT                                       # split pools are layer-first
+    assert status(d, list(bufs)[:3]) == kvb.KV_ERR_INVALID_ARG  # L x C entries
+    assert status(copy(d, nbytes=d.nbytes - 16), bufs) == kvb.KV_ERR_LAYOUT
+    odd = kvb.bufs_from_bytes(kvb.bufs_to_bytes(bufs))
+    odd[2].alloc_offset = 4100
+    assert status(d, odd) == kvb.KV_ERR_ALIGNMENT
+    with pytest.raises(kvb.KvError) as e:                       # the single-allocation import
+        kvb.kv_pool_import(d)
+    assert e.value.status == kvb.KV_ERR_INVALID_ARG and "split" in kvb.kv_last_error()
+    lib = kvb.library()
+    out = ctypes.c_void_p()
+    assert lib.kv_pool_import_split(ctypes.byref(d), None, L * C, ctypes.byref(out)) == \
+        kvb.KV_ERR_INVALID_ARG
+
+
 def test_fault_injection_points_without_gpu():
     with pytest.raises(kvb.KvError) as e:
         kvb.kv_fault_inject("no_such_point", 1)

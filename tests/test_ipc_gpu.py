@@ -194,3 +194,129 @@ def test_import_in_own_process_is_refused_cleanly():
         assert e.value.status == kvb.KV_ERR_INVALID_ARG
     finally:
         kvb.kv_pool_close(pool)
+
+
+def _child_drive_split(desc_bytes, bufs_bytes, geom_kw, ids, host_slots, host_seed, out_path, q):
+    """Importer of a split pool: maps every allocation once (imported twice to share
+    the mappings), backs pages up on one stream while restoring others on another,
+    then saves its host tier."""
+    try:
+        import sys
+        sys.path[:0] = [ROOT, os.path.join(ROOT, "tests")]
+        import torch as t
+        from hierarchical_kv_cache_backup_gb300 import kvb as k
+        from hierarchical_kv_cache_backup_gb300 import workloads as w
+
+        g = w.Geometry(**geom_kw)
+        desc = k.desc_from_bytes(desc_bytes)
+        bufs = k.bufs_from_bytes(bufs_bytes)
+        try:
+            k.kv_pool_import(desc)
+            raise AssertionError("a split descriptor was accepted by kv_pool_import")
+        except k.KvError as e:
+            assert e.status == k.KV_ERR_INVALID_ARG
+        pool = k.kv_pool_import_split(desc, bufs)
+        pool2 = k.kv_pool_import_split(desc, bufs)      # shares every mapping
+        lay, _, nbytes = k.kv_pool_info(pool)
+        host = t.empty(host_slots * g.page_bytes, dtype=t.uint8, pin_memory=True)
+        w.fill_random_(host, host_seed)
+        tier = k.kv_host_register(host.data_ptr(), host.numel(), host_slots, g.host_heads, lay)
+        sa, sb = t.cuda.Stream(), t.cuda.Stream()
+        fa = k.kv_backup(pool, tier, ids["backup_src"], ids["backup_slots"], sa.cuda_stream)
+        fb = k.kv_restore(pool2, tier, ids["restore_slots"], ids["restore_dst"], -1,
+                          sb.cuda_stream)
+        k.kv_fence_wait(fa, 30_000_000_000)
+        k.kv_fence_wait(fb, 30_000_000_000)
+        k.kv_pool_close(pool2)
+        # the first handle still maps every buffer after the second is closed: one layer
+        f = k.kv_restore(pool, tier, ids["restore_slots"][:2], ids["backup_src"][:2], g.L - 1)
+        k.kv_fence_wait(f, 30_000_000_000)
+        # an entry whose offset overruns its allocation is refused, the live pool unharmed
+        far = k.bufs_from_bytes(bufs_bytes)
+        far[1].alloc_offset = 1 << 40
+        try:
+            k.kv_pool_import_split(desc, far)
+            raise AssertionError("an overrunning buffer entry was accepted")
+        except k.KvError as e:
+            assert e.status == k.KV_ERR_OUT_OF_RANGE
+        k.kv_pool_close(pool)
+        k.kv_host_close(tier)
+        np.save(out_path, host.numpy())
+        q.put(("ok", nbytes, len(bufs)))
+    except Exception as e:  # reported to the parent
+        q.put(("error", repr(e), 0))
+
+
+def test_split_pool_import_in_second_process():
+    """A layer-first pool held as one buffer per (layer, K/V) -- four of them slices
+    of one allocation at odd offsets, the rest tensors of their own -- exported
+    with one handle per allocation and driven by a second process; the pool's
+    buffers and the importer's host tier against the oracle, which sees the
+    buffers as the contiguous pool they form."""
+    g = wl.Geometry(L=4, C=2, P=48, T=16, H=8, B=256, order=wl.LAYER_FIRST, dev_heads=wl.NHD,
+                    host_heads=wl.NHD)
+    nb = g.L * g.C
+    buf_bytes = g.P * g.T * g.H * g.B
+    shared = torch.full((4 * buf_bytes + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    views = [shared[48 + k * (buf_bytes + 16):48 + k * (buf_bytes + 16) + buf_bytes]
+             for k in range(4)]
+    own = [torch.empty(buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(nb - 4)]
+    buffers = views + own
+    for k, b in enumerate(buffers):
+        wl.fill_random_(b, 6100 + k)
+    lay = kvb.make_layout(g.L, g.C, g.P, g.T, g.H, g.B, g.order, g.dev_heads, g.elem_bytes)
+    pool = kvb.kv_pool_register_split(lay, [b.data_ptr() for b in buffers], instance_id=12,
+                                      generation=3)
+    try:
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_pool_export(pool)
+        assert e.value.status == kvb.KV_ERR_LAYOUT
+        desc, bufs = kvb.kv_pool_export_split(pool)
+        assert desc.magic == kvb.KVB_IPC_MAGIC_SPLIT and desc.nbytes == nb * buf_bytes
+        handles = [bytes(b.handle) for b in bufs]
+        assert len(set(handles[:4])) == 1                # slices of one allocation share a handle
+        assert [b.alloc_offset % 16 for b in bufs] == [0] * nb
+        assert bufs[1].alloc_offset - bufs[0].alloc_offset == buf_bytes + 16
+        n, S = 12, 24
+        r = np.random.default_rng(6200)
+        perm = r.permutation(g.P).astype(np.int32)
+        ids = {"backup_src": perm[:n], "backup_slots": np.arange(n, dtype=np.int32),
+               "restore_slots": np.arange(n, 2 * n, dtype=np.int32), "restore_dst": perm[n:2 * n]}
+        torch.cuda.synchronize()
+        contiguous = np.concatenate([b.cpu().numpy() for b in buffers])
+        host_seed = 6300
+        host0 = torch.empty(S * g.page_bytes, dtype=torch.uint8)
+        wl.fill_random_(host0, host_seed)
+        want_pool, want_host = contiguous.copy(), host0.numpy().copy()
+        og = oracle_geom(g)
+        oracle.backup(og, want_pool, want_host, ids["backup_src"], ids["backup_slots"])
+        oracle.restore(og, want_pool, want_host, ids["restore_slots"], ids["restore_dst"])
+        oracle.restore(og, want_pool, want_host, ids["restore_slots"][:2], ids["backup_src"][:2],
+                       layer=g.L - 1)
+        ctx = mp.get_context("spawn")
+        q = ctx.Queue()
+        with tempfile.TemporaryDirectory() as td:
+            out = os.path.join(td, "host.npy")
+            geom_kw = dict(L=g.L, C=g.C, P=g.P, T=g.T, H=g.H, B=g.B, order=g.order,
+                           dev_heads=g.dev_heads, host_heads=g.host_heads)
+            p = ctx.Process(target=_child_drive_split,
+                            args=(kvb.desc_to_bytes(desc), kvb.bufs_to_bytes(bufs), geom_kw, ids,
+                                  S, host_seed, out, q))
+            p.start()
+            status = q.get(timeout=600)
+            p.join(timeout=120)
+            assert status[0] == "ok", status
+            assert status[1:] == (nb * buf_bytes, nb)
+            got_host = np.load(out)
+        assert np.array_equal(got_host, want_host), "importer's host tier differs from the oracle"
+        torch.cuda.synchronize()
+        for k, b in enumerate(buffers):
+            assert np.array_equal(b.cpu().numpy(), want_pool[k * buf_bytes:(k + 1) * buf_bytes]), \
+                f"layer buffer {k} differs from the oracle"
+        # bytes of the shared allocation around the four slices are untouched
+        outside = np.ones(shared.numel(), dtype=bool)
+        for k in range(4):
+            outside[48 + k * (buf_bytes + 16):48 + k * (buf_bytes + 16) + buf_bytes] = False
+        assert (shared.cpu().numpy()[outside] == 0xA5).all()
+    finally:
+        kvb.kv_pool_close(pool)
