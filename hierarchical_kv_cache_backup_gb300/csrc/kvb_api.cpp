@@ -1422,6 +1422,17 @@ int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_hand
     return staged_copies(*host, (char *)staging, slots, n, g.pb, 0, true, stream);
 }
 
+int fence_gate_word(kv_fence f, const unsigned long long **word, unsigned long long *tag) {
+    const int d = (int)(f >> 56);
+    const uint64_t seq = f & kSeqMask;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (seq == 0 || d >= kMaxDevices || !g_dev[d].init || seq >= g_next_seq)
+        return fail(KV_ERR_INVALID_ARG, "invalid fence %llu", (unsigned long long)f);
+    *word = g_dev[d].status_dev + (seq % kRing);
+    *tag = seq;
+    return KV_OK;
+}
+
 }  // namespace kvb
 
 // =================================================================== C ABI

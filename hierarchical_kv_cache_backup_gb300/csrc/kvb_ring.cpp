@@ -11,7 +11,7 @@
 // the shared page the submitter polls.
 //
 // Layout of the shared segment (page-aligned regions):
-//   [0, 4096)            RingHeader
+//   [0, 4096)            RingHeader (with the ready words of gated descriptors)
 //   [comp_off, +C)       CompRec[slots]   (registered with CUDA by the server)
 //   [entry_off, +E)      kv_ring_op[slots]
 // Ticket t (1, 2, ...) uses slot (t - 1) % slots.  tail = last ticket published
@@ -41,7 +41,7 @@
 namespace {
 
 constexpr uint32_t kRingMagic = 0x4B565252u;   // "KVRR"
-constexpr uint32_t kRingVersion = 1u;
+constexpr uint32_t kRingVersion = 2u;   // 2: ready words, gated descriptors
 constexpr uint32_t kMaxSlots = 4096;
 constexpr size_t kPage = 4096;
 
@@ -52,6 +52,7 @@ struct RingHeader {
     alignas(64) uint64_t tail;        // last published ticket
     alignas(64) uint64_t head;        // last taken ticket
     alignas(64) int64_t server_pid;   // last server that took a descriptor
+    alignas(64) uint64_t ready[KV_RING_READY_WORDS];   // ready fences of gated descriptors
 };
 static_assert(sizeof(RingHeader) <= kPage, "ring header fits one page");
 
@@ -173,6 +174,12 @@ kv_status register_segment(RingObj *o) {
 }
 
 uint32_t slot_of(const RingObj *o, uint64_t t) { return (uint32_t)((t - 1) % o->h->slots); }
+
+// A gated descriptor names a ready word that does not exist or a wait above 60 s.
+bool bad_gate(const kv_ring_op &op) {
+    return op.ready_value != 0 &&
+           (op.ready_index >= KV_RING_READY_WORDS || op.ready_timeout_ms > 60000u);
+}
 
 // CPU completion of ticket t with status s (error record first, then done).
 void complete_cpu(RingObj *o, uint64_t t, kv_status s) {
@@ -300,6 +307,9 @@ kv_status kv_ring_submit(kv_ring r, const kv_ring_op *op, uint64_t timeout_ns, u
     if (op == nullptr || ticket == nullptr) return err(KV_ERR_INVALID_ARG, "NULL argument");
     if (op->kind > KV_RING_OP_RESTORE) return err(KV_ERR_INVALID_ARG, "unknown operation kind");
     if (op->n > KV_RING_MAX_IDS) return err(KV_ERR_INVALID_ARG, "n exceeds KV_RING_MAX_IDS");
+    if (bad_gate(*op))
+        return err(KV_ERR_INVALID_ARG, "gated descriptor: ready_index must be below "
+                   "KV_RING_READY_WORDS and ready_timeout_ms at most 60000");
     std::lock_guard<std::mutex> lk(o->mu);
     RingHeader *h = o->h;
     const uint64_t t = ld(&h->tail) + 1;
@@ -357,7 +367,8 @@ kv_status kv_ring_pop(kv_ring r, uint64_t timeout_ns, kv_ring_op *op, uint64_t *
     std::memcpy(op, &e, offsetof(kv_ring_op, a));
     // The entry comes from another process's memory: a descriptor that
     // kv_ring_submit would have refused is taken and failed here, not served.
-    const bool malformed = op->n > KV_RING_MAX_IDS || op->kind > KV_RING_OP_RESTORE;
+    const bool malformed = op->n > KV_RING_MAX_IDS || op->kind > KV_RING_OP_RESTORE ||
+                           bad_gate(*op);
     const uint32_t n = malformed ? 0 : op->n;
     std::memcpy(op->a, e.a, n * sizeof(int32_t));
     std::memcpy(op->b, e.b, n * sizeof(int32_t));
@@ -367,8 +378,8 @@ kv_status kv_ring_pop(kv_ring r, uint64_t timeout_ns, kv_ring_op *op, uint64_t *
     if (malformed) {
         op->n = 0;
         complete_cpu(o, t, KV_ERR_INVALID_ARG);
-        return err(KV_ERR_INVALID_ARG, "descriptor with an unknown kind or n above "
-                   "KV_RING_MAX_IDS: taken and completed with INVALID_ARG");
+        return err(KV_ERR_INVALID_ARG, "descriptor with an unknown kind, n above "
+                   "KV_RING_MAX_IDS or a bad gate: taken and completed with INVALID_ARG");
     }
     return KV_OK;
 }
@@ -382,6 +393,33 @@ kv_status kv_ring_complete(kv_ring r, uint64_t ticket, kv_status op_status) {
     return KV_OK;
 }
 
+kv_status kv_ring_ready_set(kv_ring r, uint32_t index, uint64_t value) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (index >= KV_RING_READY_WORDS)
+        return err(KV_ERR_INVALID_ARG, "ready index must be below KV_RING_READY_WORDS");
+    st(&o->h->ready[index], value);
+    return KV_OK;
+}
+
+kv_status kv_ring_ready_stream_set(kv_ring r, uint32_t index, uint64_t value, void *stream) {
+    RingObj *o = find(r);
+    if (o == nullptr) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
+    if (index >= KV_RING_READY_WORDS)
+        return err(KV_ERR_INVALID_ARG, "ready index must be below KV_RING_READY_WORDS");
+    std::lock_guard<std::mutex> lk(o->mu);
+    kv_status rs = register_segment(o);
+    if (rs != KV_OK) return rs;
+    unsigned long long *word =
+        (unsigned long long *)(o->seg_dev + offsetof(RingHeader, ready)) + index;
+    cudaError_t e = kvb::launch_mark(word, value, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return err(KV_ERR_CUDA, "launch of the ready-word store failed");
+    }
+    return KV_OK;
+}
+
 kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_host host,
                         void *stream, uint32_t max_ops, uint64_t idle_timeout_ns,
                         uint32_t *served) {
@@ -390,7 +428,11 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
     if (served == nullptr || (npools > 0 && pools == nullptr))
         return err(KV_ERR_INVALID_ARG, "NULL argument");
     *served = 0;
-    kv_status rs = register_segment(o);
+    kv_status rs;
+    {
+        std::lock_guard<std::mutex> lk(o->mu);
+        rs = register_segment(o);
+    }
     if (rs != KV_OK) return rs;
     static thread_local kv_ring_op op;
     for (uint32_t k = 0; k < max_ops; ++k) {
@@ -408,11 +450,22 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
             continue;
         }
         kv_fence f = 0;
+        const bool gated = op.ready_value != 0;
+        const uint64_t *ready = (const uint64_t *)(o->seg_dev + offsetof(RingHeader, ready)) +
+                                op.ready_index;
+        const uint64_t ready_ns =
+            (uint64_t)(op.ready_timeout_ms ? op.ready_timeout_ms : 10000u) * 1000000ull;
         if (op.kind == KV_RING_OP_BACKUP)
-            s = op.layer == -1 ? kv_backup(pools[op.pool_index], host, op.a, op.b, op.n, stream, &f)
-                               : KV_ERR_INVALID_ARG;
+            s = op.layer != -1 ? KV_ERR_INVALID_ARG
+                : gated ? kv_backup_when_ready(pools[op.pool_index], host, op.a, op.b, op.n, ready,
+                                               op.ready_value, ready_ns, stream, &f)
+                        : kv_backup(pools[op.pool_index], host, op.a, op.b, op.n, stream, &f);
         else
-            s = kv_restore(pools[op.pool_index], host, op.a, op.b, op.n, op.layer, stream, &f);
+            s = gated ? kv_restore_when_ready(pools[op.pool_index], host, op.a, op.b, op.n,
+                                              op.layer, ready, op.ready_value, ready_ns, stream,
+                                              &f)
+                      : kv_restore(pools[op.pool_index], host, op.a, op.b, op.n, op.layer, stream,
+                                   &f);
         if (s != KV_OK) {
             complete_cpu(o, t, s);
             continue;
@@ -422,8 +475,18 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
         int prev = -1;
         if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
         if (prev != device) cudaSetDevice(device);
-        cudaError_t e = kvb::launch_mark((unsigned long long *)&o->comp_dev[slot_of(o, t)].done,
-                                         t, (cudaStream_t)stream);
+        CompRec *cd = &o->comp_dev[slot_of(o, t)];
+        cudaError_t e = cudaSuccess;
+        if (gated) {   // the ticket reports a gate that gave up (ABORTED)
+            const unsigned long long *status = nullptr;
+            unsigned long long tag = 0;
+            kvb::fence_gate_word(f, &status, &tag);
+            e = kvb::launch_ring_mark((unsigned long long *)&cd->done,
+                                      (unsigned long long *)&cd->err_ticket, &cd->err, t, status,
+                                      tag, (cudaStream_t)stream);
+        } else {
+            e = kvb::launch_mark((unsigned long long *)&cd->done, t, (cudaStream_t)stream);
+        }
         if (prev >= 0 && prev != device) cudaSetDevice(prev);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
@@ -521,6 +584,7 @@ kv_status kv_ring_serve_device(kv_ring r, const kv_pool *pools, uint32_t npools,
     if (st != KV_OK) return st;
     kvb::RingKDesc k{};
     k.tail = (const unsigned long long *)(o->seg_dev + offsetof(RingHeader, tail));
+    k.ready = (const unsigned long long *)(o->seg_dev + offsetof(RingHeader, ready));
     k.head = (unsigned long long *)(o->seg_dev + offsetof(RingHeader, head));
     k.server_pid = (long long *)(o->seg_dev + offsetof(RingHeader, server_pid));
     k.ops = (const kv_ring_op *)(o->seg_dev + o->h->entry_off);

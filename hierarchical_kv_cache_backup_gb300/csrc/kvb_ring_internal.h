@@ -52,6 +52,7 @@ struct RingCtl {
 struct RingKDesc {
     // the shared segment, device views
     const unsigned long long *tail;   // last published ticket
+    const unsigned long long *ready;  // KV_RING_READY_WORDS ready words of gated descriptors
     unsigned long long *head;         // last taken ticket
     long long *server_pid;
     const kv_ring_op *ops;            // entries
@@ -100,5 +101,19 @@ int ring_server_view(const kv_pool *pools, uint32_t npools, kv_host host, RingPo
 // that might wait for the device runs while the server is resident.
 int ring_launch_server(int device, const RingKDesc &k, int ctas, cudaStream_t stream,
                        kv_fence *fence);
+// For a fence issued by a gated operation (kv_backup_when_ready /
+// kv_restore_when_ready): the device address of its gate-status word and the
+// tag the gate stores there when it gives up.  Returns a kv_status.
+int fence_gate_word(kv_fence f, const unsigned long long **word, unsigned long long *tag);
+
+// ---- host server support (kvb_ring.cpp) -----------------------------------
+// Completes ring ticket `ticket` on `stream` after the work before it: when
+// `status` is set and holds `tag` (the gate of the ticket's operation gave
+// up), first stores ABORTED into `err` and the ticket into `err_ticket`; then
+// stores the ticket into `done` (system scope, release).
+cudaError_t launch_ring_mark(unsigned long long *done, unsigned long long *err_ticket,
+                             int32_t *err, unsigned long long ticket,
+                             const unsigned long long *status, unsigned long long tag,
+                             cudaStream_t stream);
 
 }  // namespace kvb

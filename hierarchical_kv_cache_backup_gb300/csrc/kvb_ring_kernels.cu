@@ -71,6 +71,11 @@ __device__ __forceinline__ uint32_t ld_relaxed_sys_u32(const uint32_t *p) {
     asm volatile("ld.relaxed.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ unsigned long long ld_relaxed_sys_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t *p) {
     int32_t v;
     asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -339,7 +344,8 @@ __device__ int32_t check_descriptor(const RingKDesc &k, uint32_t kind, uint32_t 
 __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __grid_constant__ RingKDesc k) {
     __shared__ int32_t s_a[kMaxIds], s_b[kMaxIds];
     __shared__ unsigned long long s_key[kMaxIds];   // leader: (b[i] << 32) | i, sorted
-    __shared__ uint32_t s_hdr[4];                   // kind, n, pool, layer of the descriptor
+    __shared__ uint32_t s_hdr[6];   // kind, n, pool, layer, ready index, ready timeout (ms)
+    __shared__ unsigned long long s_ready;          // ready value (0: not gated)
     __shared__ uint32_t s_first_bad, s_first_dup, s_any_bad_a;
     __shared__ int s_flag, s_done;   // descriptor wait / arrival wait results
     RingCtl *ctl = k.ctl;
@@ -427,6 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
             s_hdr[1] = (uint32_t)ld_relaxed_sys((const int32_t *)&e.n);
             s_hdr[2] = (uint32_t)ld_relaxed_sys((const int32_t *)&e.pool_index);
             s_hdr[3] = (uint32_t)ld_relaxed_sys(&e.layer);
+            s_hdr[4] = (uint32_t)ld_relaxed_sys((const int32_t *)&e.ready_index);
+            s_hdr[5] = (uint32_t)ld_relaxed_sys((const int32_t *)&e.ready_timeout_ms);
+            s_ready = ld_relaxed_sys_u64((const unsigned long long *)&e.ready_value);
             s_first_bad = s_first_dup = 0xffffffffu;
             s_any_bad_a = 0u;
         }
@@ -434,8 +443,16 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
         ++taken;
         const uint32_t kind = s_hdr[0], n = s_hdr[1], pool = s_hdr[2];
         const int32_t layer = (int32_t)s_hdr[3];
-        const int32_t status = check_descriptor(k, kind, n, pool, layer, a_r, b_r, s_a, s_b, s_key,
-                                                &s_first_bad, &s_first_dup, &s_any_bad_a);
+        const uint32_t ready_index = s_hdr[4], ready_ms = s_hdr[5];
+        const unsigned long long ready_value = s_ready;
+        // a gate naming no ready word, or a wait above 60 s, is refused like a
+        // malformed descriptor (the host server's pop does the same)
+        const bool bad_gate =
+            ready_value != 0 && (ready_index >= KV_RING_READY_WORDS || ready_ms > 60000u);
+        const int32_t status =
+            bad_gate ? (int32_t)KV_ERR_INVALID_ARG
+                     : check_descriptor(k, kind, n, pool, layer, a_r, b_r, s_a, s_b, s_key,
+                                        &s_first_bad, &s_first_dup, &s_any_bad_a);
         if (status != KV_OK) {   // rejected: completed at once, nothing moves
             if (tid == 0) {
                 st_relaxed_sys64(k.head, t);
@@ -443,6 +460,36 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
             }
             __syncthreads();
             continue;
+        }
+        // gated: wait (bounded) for its ready word; on time-out -- or a stop
+        // request meanwhile -- it moves nothing and completes with ABORTED
+        if (ready_value != 0) {
+            if (tid == 0) {
+                const unsigned long long limit_ns =
+                    (unsigned long long)(ready_ms ? ready_ms : 10000u) * 1000000ull;
+                const unsigned long long deadline = now_ns() + limit_ns;
+                const unsigned long long max_polls = limit_ns / 16ull + 4096ull;
+                int open = 0;
+                for (unsigned long long polls = 0;; ++polls) {
+                    if (ld_acquire_sys(k.ready + ready_index) >= ready_value) {
+                        open = 1;
+                        break;
+                    }
+                    if (ld_relaxed_sys_u32(k.result + 2) != 0) break;
+                    if (polls >= max_polls || ((polls & 63u) == 63u && now_ns() > deadline)) break;
+                    if (polls >= 4096) __nanosleep(256);
+                }
+                s_flag = open;
+            }
+            __syncthreads();
+            if (!s_flag) {
+                if (tid == 0) {
+                    st_relaxed_sys64(k.head, t);
+                    complete_failed(k, t, KV_ERR_ABORTED);
+                }
+                __syncthreads();
+                continue;
+            }
         }
         // accepted: it runs after the one released before it has ended
         if (tid == 0) {
@@ -494,9 +541,35 @@ __global__ void __launch_bounds__(kThreads, 1) kv_ring_server_kernel(const __gri
 
 }  // namespace
 
+namespace {
+
+__global__ void kv_ring_mark_kernel(unsigned long long *done, unsigned long long *err_ticket,
+                                    int32_t *err, unsigned long long ticket,
+                                    const unsigned long long *status, unsigned long long tag) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    if (status != nullptr && ld_relaxed_sys_u64(status) == tag) {
+        asm volatile("st.relaxed.sys.global.s32 [%0], %1;" ::"l"(err), "r"((int32_t)KV_ERR_ABORTED)
+                     : "memory");
+        st_relaxed_sys64(err_ticket, ticket);
+    }
+    __threadfence_system();
+    st_release_sys(done, ticket);
+}
+
+}  // namespace
+
 cudaError_t preload_ring_kernels() {
     cudaFuncAttributes a;
-    return cudaFuncGetAttributes(&a, (const void *)kv_ring_server_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&a, (const void *)kv_ring_server_kernel);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, (const void *)kv_ring_mark_kernel);
+    return e;
+}
+
+cudaError_t launch_ring_mark(unsigned long long *done, unsigned long long *err_ticket, int32_t *err,
+                             unsigned long long ticket, const unsigned long long *status,
+                             unsigned long long tag, cudaStream_t stream) {
+    kv_ring_mark_kernel<<<1, 32, 0, stream>>>(done, err_ticket, err, ticket, status, tag);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_ring_server(const RingKDesc &k, int ctas, cudaStream_t stream) {

@@ -53,7 +53,7 @@ EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_p
            "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
            "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
            "kv_ring_pop", "kv_ring_complete", "kv_ring_serve_device", "kv_ring_device_result",
-           "kv_ring_device_stop",
+           "kv_ring_device_stop", "kv_ring_ready_set", "kv_ring_ready_stream_set",
            "kv_fault_inject", "kv_l3_open", "kv_l3_close",
            "kv_l3_put", "kv_l3_get")
 
@@ -84,12 +84,15 @@ class kv_ipc_buffer(ctypes.Structure):
 
 KV_RING_MAX_IDS = 1024
 KV_RING_OP_BACKUP, KV_RING_OP_RESTORE = 0, 1
+KV_RING_READY_WORDS = 64
 
 
 class kv_ring_op(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_uint32), ("pool_index", ctypes.c_uint32),
                 ("n", ctypes.c_uint32), ("layer", ctypes.c_int32),
                 ("operation_id", ctypes.c_uint64),
+                ("ready_index", ctypes.c_uint32), ("ready_timeout_ms", ctypes.c_uint32),
+                ("ready_value", ctypes.c_uint64),
                 ("a", ctypes.c_int32 * KV_RING_MAX_IDS), ("b", ctypes.c_int32 * KV_RING_MAX_IDS)]
 
 
@@ -148,6 +151,8 @@ def _load():
         "kv_ring_serve_device": (st, [vp, P(vp), u32, vp, vp, u32, u64, P(u64)]),
         "kv_ring_device_result": (st, [vp, P(u32), P(ctypes.c_int)]),
         "kv_ring_device_stop": (st, [vp]),
+        "kv_ring_ready_set": (st, [vp, u32, u64]),
+        "kv_ring_ready_stream_set": (st, [vp, u32, u64, vp]),
         "kv_fault_inject": (st, [ctypes.c_char_p, u32]),
         "kv_l3_open": (st, [ctypes.c_int, u64, u64, u64, u32, P(vp)]),
         "kv_l3_close": (st, [vp]),
@@ -487,9 +492,11 @@ def kv_abi_version() -> int:
 # ----------------------------------------------------------- descriptor ring
 
 def make_ring_op(kind: int, a, b, pool_index: int = 0, layer: int = -1,
-                 operation_id: int = 0) -> kv_ring_op:
+                 operation_id: int = 0, ready_index: int = 0, ready_value: int = 0,
+                 ready_timeout_ms: int = 0) -> kv_ring_op:
     """A descriptor for the shared-memory ring: kind 0 BACKUP (a = pages, b = slots) or 1
-    RESTORE (a = slots, b = pages)."""
+    RESTORE (a = slots, b = pages).  ready_value != 0 gates it on ready word ready_index
+    reaching that value (waited for on the GPU for at most ready_timeout_ms, 0 = 10 s)."""
     a_, _ = _ids(a)
     b_, _ = _ids(b)
     if a_.size != b_.size or a_.size > KV_RING_MAX_IDS:
@@ -497,6 +504,8 @@ def make_ring_op(kind: int, a, b, pool_index: int = 0, layer: int = -1,
     op = kv_ring_op()
     op.kind, op.pool_index, op.n, op.layer, op.operation_id = kind, pool_index, a_.size, layer, \
         operation_id
+    op.ready_index, op.ready_value, op.ready_timeout_ms = ready_index, ready_value, \
+        ready_timeout_ms
     ctypes.memmove(op.a, a_.ctypes.data, a_.nbytes) if a_.size else None
     ctypes.memmove(op.b, b_.ctypes.data, b_.nbytes) if b_.size else None
     return op
@@ -569,6 +578,17 @@ def kv_ring_serve_device(ring: int, pools, host: int, stream=None, max_ops: int 
     _check(_lib.kv_ring_serve_device(ring, arr, len(pools), host, stream, max_ops,
                                      idle_timeout_ns, ctypes.byref(f)))
     return f.value
+
+
+def kv_ring_ready_set(ring: int, index: int, value: int) -> None:
+    """Sets ready word `index` of the ring to `value` from the CPU (either process)."""
+    _check(_lib.kv_ring_ready_set(ring, index, value))
+
+
+def kv_ring_ready_stream_set(ring: int, index: int, value: int, stream=None) -> None:
+    """Sets ready word `index` to `value` from the GPU once the work before it on `stream`
+    has finished."""
+    _check(_lib.kv_ring_ready_stream_set(ring, index, value, stream))
 
 
 def kv_ring_device_stop(ring: int) -> None:

@@ -419,13 +419,25 @@ typedef struct kv_ring_s *kv_ring;
 #define KV_RING_OP_BACKUP 0u
 #define KV_RING_OP_RESTORE 1u
 
-/* One BACKUP / RESTORE descriptor ([RFC] §Device IPC data path).  POD. */
+#define KV_RING_READY_WORDS 64
+
+/* One BACKUP / RESTORE descriptor ([RFC] §Device IPC data path).  POD.
+ * Ready fence ([RFC] BACKUP(..., ready_fence)): with ready_value != 0 the
+ * operation starts only once the ring's ready word ready_index (one of
+ * KV_RING_READY_WORDS 64-bit words in the shared segment, set with
+ * kv_ring_ready_set or kv_ring_ready_stream_set) holds a value >= ready_value.
+ * The server waits for it on the GPU, at most ready_timeout_ms (1..60000;
+ * 0 = 10000); on time-out the operation moves no byte and its ticket completes
+ * with ABORTED (fail closed).  ready_value = 0: no gate. */
 typedef struct {
     uint32_t kind;           /* KV_RING_OP_BACKUP or KV_RING_OP_RESTORE              */
     uint32_t pool_index;     /* index into the server's pool table                 */
     uint32_t n;              /* ids in a[] and b[] (<= KV_RING_MAX_IDS)            */
     int32_t layer;           /* restore: -1 = all layers, else one; backup: -1     */
     uint64_t operation_id;   /* the submitter's operation_id, returned by pop      */
+    uint32_t ready_index;    /* ready word gating the operation (< KV_RING_READY_WORDS) */
+    uint32_t ready_timeout_ms;    /* bound on the wait for it; 0 = 10 s            */
+    uint64_t ready_value;    /* start once the word >= this; 0 = not gated        */
     int32_t a[KV_RING_MAX_IDS];   /* backup: source pages; restore: host slots     */
     int32_t b[KV_RING_MAX_IDS];   /* backup: host slots; restore: destination pages */
 } kv_ring_op;
@@ -446,7 +458,8 @@ KVB_API kv_status kv_ring_close(kv_ring ring);
 
 /* Submitter: copies `op` into the next slot and publishes it; waits up to
  * timeout_ns for a free slot (TIMEOUT: ring full -- the server is behind or
- * gone).  Returns the ticket.  Errors: INVALID_ARG (kind, n), TIMEOUT. */
+ * gone).  Returns the ticket.  Errors: INVALID_ARG (kind, n, ready_index or
+ * ready_timeout_ms of a gated op), TIMEOUT. */
 KVB_API kv_status kv_ring_submit(kv_ring ring, const kv_ring_op *op, uint64_t timeout_ns,
                                  uint64_t *ticket);
 /* Submitter: waits up to timeout_ns for `ticket` to complete and returns the
@@ -456,12 +469,32 @@ KVB_API kv_status kv_ring_submit(kv_ring ring, const kv_ring_op *op, uint64_t ti
 KVB_API kv_status kv_ring_wait(kv_ring ring, uint64_t ticket, uint64_t timeout_ns,
                                kv_status *op_status);
 
+/* Sets ready word `index` (< KV_RING_READY_WORDS) of the ring to `value` from
+ * the CPU (a release store into the shared segment); either process may call
+ * it.  Words start at 0 and are the caller's to sequence: a gate opens once
+ * its word is >= its ready_value.  Errors: CLOSED, INVALID_ARG (index). */
+KVB_API kv_status kv_ring_ready_set(kv_ring ring, uint32_t index, uint64_t value);
+/* Sets ready word `index` to `value` from the GPU, once the work enqueued
+ * before it on `stream` has finished (a stream memory write): a scheduler's
+ * forward stream releases the data plane's gated backup with no CPU wait in
+ * either process.  The first call registers the shared segment with CUDA in
+ * this process; make it (or kv_ring_ready_set) before gated operations of this
+ * process wait.  Likewise launch once, beforehand, any kernel of this process
+ * that precedes the word on `stream`: under lazy module loading a kernel's
+ * first launch waits for the device to go idle, and a gate waiting in the
+ * same process keeps it busy until its bound.  Errors: CLOSED, INVALID_ARG
+ * (index), CUDA. */
+KVB_API kv_status kv_ring_ready_stream_set(kv_ring ring, uint32_t index, uint64_t value,
+                                           void *stream);
+
 /* Server: takes up to max_ops descriptors, waiting up to idle_timeout_ns for
  * the first, and enqueues each on `stream` as kv_backup / kv_restore on
- * pools[op.pool_index] and `host`; the GPU completes each ticket in shared
- * memory after its bytes.  A descriptor the engine rejects is completed at
- * once with that error.  *served = descriptors taken.  Errors: INVALID_ARG,
- * CUDA (registering the completion page). */
+ * pools[op.pool_index] and `host` (a gated one as kv_backup_when_ready /
+ * kv_restore_when_ready on its ready word); the GPU completes each ticket in
+ * shared memory after its bytes (ABORTED for a gate that timed out).  A
+ * descriptor the engine rejects is completed at once with that error.
+ * *served = descriptors taken.  Errors: INVALID_ARG, CUDA (registering the
+ * completion page). */
 KVB_API kv_status kv_ring_serve(kv_ring ring, const kv_pool *pools, uint32_t npools, kv_host host,
                                 void *stream, uint32_t max_ops, uint64_t idle_timeout_ns,
                                 uint32_t *served);
@@ -486,8 +519,10 @@ KVB_API kv_status kv_ring_complete(kv_ring ring, uint64_t ticket, kv_status op_s
  * (the same status for every rejected descriptor: INVALID_ARG for a kind, n,
  * pool index or backup layer it refuses, then OUT_OF_RANGE / DUPLICATE for
  * layers and ids in the host engine's order), moves the accepted ones
- * zero-copy in ticket order, and completes every ticket from the GPU.  No host
- * thread and no launch per descriptor.  The server ends after max_ops
+ * zero-copy in ticket order -- a gated one once its ready word allows, or
+ * completed with ABORTED after its ready_timeout_ms -- and completes every
+ * ticket from the GPU.  No host thread and no launch per descriptor.  The
+ * server ends after max_ops
  * descriptors, or once idle_timeout_ns (<= 60 s) pass without a new one;
  * every other wait inside it is bounded too.  Returns at once; *fence
  * completes when the kernel has ended (then kv_ring_device_result).  The

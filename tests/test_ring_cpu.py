@@ -221,3 +221,54 @@ def test_attach_refuses_a_header_whose_regions_overrun_the_segment():
     finally:
         m.close()
         kvb.kv_ring_close(sub)
+
+
+def test_gated_descriptors_and_ready_words_without_gpu():
+    """Gated descriptors: the gate fields travel with the descriptor; a gate that
+    names no ready word or waits above 60 s is refused by submit and, written
+    into the segment directly, taken and failed by pop; ready words set through
+    one handle are seen through the other (shared memory)."""
+    import ctypes
+    import struct
+    name = ring_name()
+    sub = kvb.kv_ring_create(name, 4)
+    srv = kvb.kv_ring_attach(name)
+    m = _shm_view(name)
+    try:
+        assert ctypes.sizeof(kvb.kv_ring_op) == 24 + 16 + 8 * kvb.KV_RING_MAX_IDS
+        op = kvb.make_ring_op(0, [1, 2], [3, 4], ready_index=5, ready_value=9,
+                              ready_timeout_ms=250)
+        t = kvb.kv_ring_submit(sub, op)
+        t2, got = kvb.kv_ring_pop(srv)
+        assert (t2, got.ready_index, got.ready_value, got.ready_timeout_ms) == (t, 5, 9, 250)
+        kvb.kv_ring_complete(srv, t2, kvb.KV_OK)
+        for bad in (dict(ready_index=kvb.KV_RING_READY_WORDS, ready_value=1),
+                    dict(ready_index=0, ready_value=1, ready_timeout_ms=60001)):
+            with pytest.raises(kvb.KvError) as e:
+                kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [1], [2], **bad))
+            assert e.value.status == kvb.KV_ERR_INVALID_ARG
+        # not gated (ready_value 0): any index is ignored
+        t = kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [1], [2], ready_index=999))
+        t2, got = kvb.kv_ring_pop(srv)
+        kvb.kv_ring_complete(srv, t2, kvb.KV_OK)
+        # a bad gate written into the shared segment directly: taken, failed
+        slots, entry_bytes, _, entry_off = struct.unpack_from("<IIQQ", m, 8)
+        t = kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [1], [2], ready_index=1, ready_value=1))
+        struct.pack_into("<I", m, entry_off + ((t - 1) % slots) * entry_bytes + 24, 4096)
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_ring_pop(srv)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+        assert kvb.kv_ring_wait(sub, t) == kvb.KV_ERR_INVALID_ARG
+        # ready words: set through one handle, read in the shared header
+        kvb.kv_ring_ready_set(sub, 3, 41)
+        kvb.kv_ring_ready_set(srv, 63, 7)
+        ready_off = 256   # after the fixed fields, tail, head and server_pid (64 B each)
+        assert struct.unpack_from("<Q", m, ready_off + 8 * 3)[0] == 41
+        assert struct.unpack_from("<Q", m, ready_off + 8 * 63)[0] == 7
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_ring_ready_set(sub, kvb.KV_RING_READY_WORDS, 1)
+        assert e.value.status == kvb.KV_ERR_INVALID_ARG
+    finally:
+        m.close()
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)

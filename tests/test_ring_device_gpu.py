@@ -456,3 +456,82 @@ def test_device_server_one_layer_restores_of_a_prefix():
     want = replay(g, 0, snap, ops, statuses)
     assert np.array_equal(after[0], want[0]), "pool allocation differs from the oracle"
     assert np.array_equal(after[1], want[1]), "host tier differs from the oracle"
+
+
+@pytest.mark.parametrize("server", ["host", "device"])
+def test_gated_descriptors_wait_for_their_ready_words(server):
+    """Descriptors with a ready fence, served by a host thread and by the
+    resident server: a backup that waits until the submitter sets its ready word
+    from the CPU (the restore behind it waits in ticket order), one whose word
+    is never set (ABORTED after its 200 ms bound, nothing moved, the ring goes
+    on), and a restore released from the submitter's GPU stream after other
+    work on it.  Bytes against the oracle's replay of the moved descriptors."""
+    import threading
+    g = wl.TINY.geom.with_(P=48)
+    S = 16
+    r = np.random.default_rng(5100 + (server == "device"))
+    pages = r.permutation(g.P)
+    ops = [(0, pages[0:4], np.arange(0, 4), -1, 0, dict(ready_index=2, ready_value=5,
+                                                        ready_timeout_ms=5000)),
+           (1, np.arange(0, 4), pages[4:8], -1, 0, {}),
+           (0, pages[8:12], np.arange(4, 8), -1, 0, dict(ready_index=7, ready_value=1,
+                                                         ready_timeout_ms=200)),
+           (0, pages[12:16], np.arange(8, 12), -1, 0, {}),
+           (1, np.arange(8, 12), pages[16:20], 1, 0, dict(ready_index=9, ready_value=3,
+                                                           ready_timeout_ms=5000))]
+    rig = Rig(g, S, seed=5200)
+    sub, srv = ring_pair(8)
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    # load the stand-in forward's kernel before any gate waits: with lazy module
+    # loading a kernel's first launch waits for the device to go idle, which a
+    # gate spinning for this very stream's word would hold off until its bound
+    torch.cuda._sleep(1000)
+    torch.cuda.synchronize()
+    th, fence = None, None
+    try:
+        snap = rig.snapshot()
+        if server == "device":
+            fence = kvb.kv_ring_serve_device(srv, [rig.pool], rig.hostt, stream.cuda_stream,
+                                             len(ops), 5_000_000_000)
+        else:
+            def serve():
+                left = len(ops)
+                for _ in range(10):   # bounded: each call waits at most 5 s for a descriptor
+                    if left == 0:
+                        break
+                    left -= kvb.kv_ring_serve(srv, [rig.pool], rig.hostt, stream.cuda_stream,
+                                              left, 5_000_000_000)
+            th = threading.Thread(target=serve, daemon=True)
+            th.start()
+        tickets = [kvb.kv_ring_submit(sub, kvb.make_ring_op(k, a, b, pool_index=pi, layer=ly,
+                                                            operation_id=i, **gate), WAIT)
+                   for i, (k, a, b, ly, pi, gate) in enumerate(ops)]
+        time.sleep(0.05)
+        with pytest.raises(kvb.KvError) as e:            # its ready word is still 0
+            kvb.kv_ring_wait(sub, tickets[0], 20_000_000)
+        assert e.value.status == kvb.KV_ERR_TIMEOUT
+        kvb.kv_ring_ready_set(sub, 2, 5)
+        assert kvb.kv_ring_wait(sub, tickets[0], WAIT) == kvb.KV_OK
+        assert kvb.kv_ring_wait(sub, tickets[1], WAIT) == kvb.KV_OK
+        assert kvb.kv_ring_wait(sub, tickets[2], WAIT) == kvb.KV_ERR_ABORTED
+        assert kvb.kv_ring_wait(sub, tickets[3], WAIT) == kvb.KV_OK
+        with torch.cuda.stream(side):                    # the submitter's "forward", then the word
+            torch.cuda._sleep(2_000_000)
+            kvb.kv_ring_ready_stream_set(sub, 9, 3, side.cuda_stream)
+        assert kvb.kv_ring_wait(sub, tickets[4], WAIT) == kvb.KV_OK
+        if fence is not None:
+            kvb.kv_fence_wait(fence, WAIT)
+            assert kvb.kv_ring_device_result(srv) == (len(ops), kvb.KV_OK)
+        if th is not None:
+            th.join(30)
+        stream.synchronize()
+        side.synchronize()
+        after = rig.snapshot()
+        statuses = [kvb.KV_OK, kvb.KV_OK, kvb.KV_ERR_ABORTED, kvb.KV_OK, kvb.KV_OK]
+        want = replay(g, 0, snap, [op[:5] for op in ops], statuses)
+        assert np.array_equal(after[0], want[0]), "pool allocation differs from the oracle"
+        assert np.array_equal(after[1], want[1]), "host tier differs from the oracle"
+    finally:
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        rig.close()
