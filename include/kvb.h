@@ -478,12 +478,11 @@ KVB_API kv_status kv_ring_ready_set(kv_ring ring, uint32_t index, uint64_t value
  * before it on `stream` has finished (a stream memory write): a scheduler's
  * forward stream releases the data plane's gated backup with no CPU wait in
  * either process.  The first call registers the shared segment with CUDA in
- * this process; make it (or kv_ring_ready_set) before gated operations of this
- * process wait.  Likewise launch once, beforehand, any kernel of this process
- * that precedes the word on `stream`: under lazy module loading a kernel's
- * first launch waits for the device to go idle, and a gate waiting in the
- * same process keeps it busy until its bound.  Errors: CLOSED, INVALID_ARG
- * (index), CUDA. */
+ * this process.  Launch once, beforehand, any kernel of this process that
+ * precedes the word on `stream`: under lazy module loading a kernel's first
+ * launch waits for the device to go idle, and a gate (or a resident server)
+ * waiting in the same process keeps it busy until its bound.  Errors: CLOSED,
+ * INVALID_ARG (index), CUDA. */
 KVB_API kv_status kv_ring_ready_stream_set(kv_ring ring, uint32_t index, uint64_t value,
                                            void *stream);
 
