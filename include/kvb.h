@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define KVB_ABI_VERSION 1u
+#define KVB_ABI_VERSION 2u   /* 2: gated ring descriptors (kv_ring_op grew), split-pool IPC */
 
 #if defined(__GNUC__)
 #define KVB_API __attribute__((visibility("default")))

@@ -33,7 +33,7 @@ def test_struct_sizes_match_header():
     assert ctypes.sizeof(kvb.kv_layout) == 40
     assert ctypes.sizeof(kvb.kv_ipc_desc) == 168
     assert ctypes.sizeof(kvb.kv_config) == 24   # mode, max_ctas, staging, flags, cta_threads
-    assert kvb.kv_abi_version() == 1
+    assert kvb.kv_abi_version() == 2
 
 
 def lay(**kw):
@@ -162,7 +162,8 @@ def test_register_rejects_before_touching_cuda():
 
 def test_descriptor_bytes_roundtrip():
     d = kvb.kv_ipc_desc()
-    d.magic, d.version, d.alloc_offset, d.generation = kvb.KVB_IPC_MAGIC, 1, 2 * 1024 * 1024 + 48, 7
+    d.magic, d.version, d.alloc_offset, d.generation = kvb.KVB_IPC_MAGIC, kvb.kv_abi_version(), \
+        2 * 1024 * 1024 + 48, 7
     d.layout = lay(P=2048, L=40, T=32, H=8, B=256, order=1, heads=1)
     b = kvb.desc_to_bytes(d)
     assert len(b) == 168
@@ -199,7 +200,7 @@ def test_split_descriptor_checks_before_cuda():
     assert ctypes.sizeof(kvb.kv_ipc_buffer) == 72
     L, C, P, T, H, B = 2, 2, 64, 16, 2, 128
     d = kvb.kv_ipc_desc()
-    d.magic, d.version = kvb.KVB_IPC_MAGIC_SPLIT, 1
+    d.magic, d.version = kvb.KVB_IPC_MAGIC_SPLIT, kvb.kv_abi_version()
     d.layout = lay(L=L, C=C, P=P, T=T, H=H, B=B)
     d.nbytes = L * C * P * T * H * B
     bufs = (kvb.kv_ipc_buffer * (L * C))()
