@@ -218,6 +218,23 @@ struct DevState {
     cudaEvent_t gids_copied = nullptr;       // the pinned -> device copy is done
     cudaEvent_t gids_free = nullptr;         // the kernel reading the device ids is done
     bool gids_used = false;
+    // KV_CFG_OVERLAP_RESTORES: per stream, the run of zero-copy restores of one
+    // pool issued there since the last op that waited for its predecessor; any
+    // other op of this library on the stream erases it.  Each overlapped kernel
+    // may start while its predecessors still run (each lets the next launch
+    // early), so a new restore may overlap only if it writes nothing that any
+    // restore of the run whose fence is not yet complete writes.
+    struct ChainOp {
+        int k;                      // fence slot and sequence number
+        uint64_t seq;
+        int32_t layer;              // -1 = every layer
+        std::vector<int32_t> dst;   // pages it writes, sorted
+    };
+    struct Chain {
+        uint64_t pool;              // pool handle id
+        std::vector<ChainOp> ops;   // in call order; the last is the stream's last op
+    };
+    std::unordered_map<void *, Chain> chains;
 };
 
 std::mutex g_mu;
@@ -230,6 +247,7 @@ uint64_t g_next_seq = 1;
 DevState g_dev[kMaxDevices];
 kv_config g_cfg = {KV_MODE_ZERO_COPY, 0, 0, 0, 0};
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_overlapped{0};   // restores issued overlapped
 
 constexpr uint64_t kDefaultStaging = 256ull << 20;
 constexpr uint64_t kMaxReadyTimeoutNs = 60ull * 1000 * 1000 * 1000;   // gate waits at most 60 s
@@ -538,6 +556,54 @@ kv_status check_op(const Geo &g, uint64_t num_slots, int kind, const int32_t *a,
     kv_status st = check_ids("host_slots", a, n, num_slots, false);
     if (st != KV_OK) return st;
     return check_ids("dst_pages", b, n, g.P, true);
+}
+
+// -------------------------------------------------- overlapped restores
+
+// Any library work on `stream` other than a zero-copy restore ends the run of
+// restores there that a later one may overlap.  That work waits for the
+// stream's previous kernel, whose completion implies every earlier restore of
+// the run is in place (each published its fence only after its predecessor's).
+void forget_stream(DevState &ds, void *stream) {
+    if (!ds.chains.empty()) ds.chains.erase(stream);
+}
+
+// True when two sorted, duplicate-free page lists have no page in common.
+bool sorted_disjoint(const std::vector<int32_t> &x, const std::vector<int32_t> &y) {
+    size_t i = 0, j = 0;
+    while (i < x.size() && j < y.size()) {
+        if (x[i] == y[j]) return false;
+        if (x[i] < y[j]) ++i; else ++j;
+    }
+    return true;
+}
+
+constexpr size_t kMaxChain = 256;   // restores of one run checked against a new one
+
+// Whether a restore of (pool, layer, sorted pages) on `stream` may overlap the
+// run there; sets *pred to the run's last op (the fence it chains on).  Drops
+// restores of the run whose fence the host already sees complete: their bytes
+// are in place.
+bool may_overlap(DevState &ds, void *stream, uint64_t pool, int32_t layer,
+                 const std::vector<int32_t> &pages, const DevState::ChainOp **pred) {
+    auto it = ds.chains.find(stream);
+    if (it == ds.chains.end() || it->second.pool != pool || it->second.ops.empty()) return false;
+    std::vector<DevState::ChainOp> &ops = it->second.ops;
+    size_t keep = 0;
+    for (size_t i = 0; i < ops.size(); ++i) {
+        const bool last = i + 1 == ops.size();
+        if (!last && load_acquire(&ds.words[ops[i].k]) >= ops[i].seq) continue;
+        if (keep != i) ops[keep] = std::move(ops[i]);
+        ++keep;
+    }
+    ops.resize(keep);
+    if (ops.size() >= kMaxChain) return false;
+    for (const DevState::ChainOp &o : ops) {
+        const bool other_layer = layer >= 0 && o.layer >= 0 && layer != o.layer;
+        if (!other_layer && !sorted_disjoint(o.dst, pages)) return false;
+    }
+    *pred = &ops.back();
+    return true;
 }
 
 // ---------------------------------------------------------- launch planning
@@ -1054,6 +1120,34 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     };
     bool fused = false;
 
+    // Overlapped restores (KV_CFG_OVERLAP_RESTORES): a zero-copy restore may
+    // start moving while the previous kernel on its stream still runs when that
+    // kernel is the last restore this library issued there, of the same pool,
+    // and the two write disjoint bytes (other layers, or no page in common).
+    // Restores only read the host tier, so nothing else can conflict.
+    const bool overlap_cfg = (g_cfg.flags & KV_CFG_OVERLAP_RESTORES) != 0 &&
+                             (g_cfg.flags & KV_CFG_NO_PDL) == 0;
+    const bool restore_kind = !backup && ready == nullptr && n > 0 &&
+                              g_cfg.mode == KV_MODE_ZERO_COPY;
+    bool chain = false, overlapped = false;
+    int chain_k = 0;
+    uint64_t chain_seq = 0;
+    static thread_local std::vector<int32_t> sorted_dst;
+    if (overlap_cfg && restore_kind) {
+        sorted_dst.assign(b, b + n);
+        std::sort(sorted_dst.begin(), sorted_dst.end());
+        const DevState::ChainOp *pred = nullptr;
+        if (may_overlap(ds, stream_v, handle_id(pool_h), layer, sorted_dst, &pred)) {
+            chain = true;
+            chain_k = pred->k;
+            chain_seq = pred->seq;
+        }
+    }
+    // the stream's run, kept aside: re-recorded below once this op is committed
+    DevState::Chain run;
+    if (chain) run = std::move(ds.chains[stream_v]);
+    forget_stream(ds, stream_v);
+
     if (n > 0 && (g_cfg.mode == KV_MODE_ZERO_COPY || ready != nullptr)) {
         const Side ps = pool_side(*pool), hs = host_side(*host);
         Plan p;
@@ -1068,6 +1162,16 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         }
         p.threads = link_threads(p.d.transpose != 0);
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
+        if (overlap_cfg && restore_kind) {
+            p.d.early_trigger = 1u;
+            // one launch only: the op's fence and its overlap sit in the same kernel
+            if (chain && n <= p.max_items) {
+                p.d.overlap = 1u;
+                p.d.chain_word = ds.words_dev + chain_k;
+                p.d.chain_seq = chain_seq;
+                overlapped = true;
+            }
+        }
         st = run_moves(p, a, b, n, default_ctas(ds, true, PK_REG, p.threads), stream, false, &ds,
                        &fs);
         if (st != KV_OK) return bail(st);
@@ -1190,7 +1294,18 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
         ds.staging_used[half] = true;
     }
-    return bail(commit_fence(d, fs, !fused, stream, fence));
+    st = commit_fence(d, fs, !fused, stream, fence);
+    if (st != KV_OK) return bail(st);
+    if (overlapped) g_overlapped.fetch_add(1, std::memory_order_relaxed);
+    if (overlap_cfg && restore_kind && fused) {
+        // an op that did not overlap waited for all before it: it starts a new run
+        if (!overlapped) run.ops.clear();
+        run.pool = handle_id(pool_h);
+        run.ops.push_back(DevState::ChainOp{fs.k, fs.seq, layer, sorted_dst});
+        if (ds.chains.size() >= 4096) ds.chains.clear();   // streams come and go
+        ds.chains[stream_v] = std::move(run);
+    }
+    return KV_OK;
 }
 
 // Device gather (kind 0) / scatter (kind 1) between the pool and a caller's
@@ -1230,6 +1345,7 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
     if (st != KV_OK) return st;
     DevState &ds = g_dev[d];
     cudaStream_t stream = (cudaStream_t)stream_v;
+    forget_stream(ds, stream_v);
     if (n > 0) {
         cudaPointerAttributes attr;
         cudaError_t e = cudaPointerGetAttributes(&attr, buf);
@@ -1347,6 +1463,7 @@ int ring_launch_server(int device, const RingKDesc &k, int ctas, cudaStream_t st
     DeviceGuard guard(device);
     kv_status st = init_device(device);
     if (st != KV_OK) return st;
+    forget_stream(g_dev[device], (void *)stream);
     // the fence's slot (and its event) before the launch, its marker after
     FenceSlot fs;
     st = reserve_fence(device, &fs);
@@ -1400,6 +1517,7 @@ int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_hand
             return fail(KV_ERR_DUPLICATE, "host slot %d appears twice: one call may write a slot "
                         "only once", sorted[i]);
     if (n == 0) return KV_OK;
+    if (g_dev[pool->device].init) forget_stream(g_dev[pool->device], (void *)stream);
     int sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, pool->device);
     const Side ps = pool_side(*pool);
@@ -1456,6 +1574,8 @@ const char *kv_last_error(void) { return t_err.c_str(); }
 
 uint64_t kv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+uint64_t kv_overlap_count(void) { return g_overlapped.load(std::memory_order_relaxed); }
+
 kv_status kv_layout_page_bytes(const kv_layout *layout, uint64_t *out) {
     if (out == nullptr) return fail(KV_ERR_INVALID_ARG, "output pointer is NULL");
     Geo g{};
@@ -1478,7 +1598,7 @@ kv_status kv_config_set(const kv_config *cfg) {
     if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
     if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
         return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
-    if ((cfg->flags & ~(uint32_t)(KV_CFG_NO_BULK | KV_CFG_NO_PDL)) != 0)
+    if ((cfg->flags & ~(uint32_t)(KV_CFG_NO_BULK | KV_CFG_NO_PDL | KV_CFG_OVERLAP_RESTORES)) != 0)
         return fail(KV_ERR_INVALID_ARG, "unknown config flags %#x", cfg->flags);
     if (cfg->cta_threads != 0 && cfg->cta_threads != (uint32_t)kMoveThreads &&
         cfg->cta_threads != (uint32_t)kWideThreads)
@@ -1679,6 +1799,9 @@ kv_status kv_pool_import(const kv_ipc_desc *desc, kv_pool *out) {
     auto it = g_maps.find(key);
     void *base = nullptr;
     if (it != g_maps.end()) {
+        if (it->second.device != device)   // addresses of another device's context
+            return fail(KV_ERR_INVALID_ARG, "the allocation is already mapped on device %d, not "
+                        "on the descriptor's device %d", it->second.device, device);
         base = it->second.base;
     } else {
         DeviceGuard guard(device);
@@ -1840,6 +1963,12 @@ kv_status kv_pool_import_split(const kv_ipc_desc *desc, const kv_ipc_buffer *buf
             Mapped mp{nullptr, 0, false};
             auto it = g_maps.find(key);
             if (it != g_maps.end()) {
+                if (it->second.device != device) {   // addresses of another device's context
+                    undo();
+                    return fail(KV_ERR_INVALID_ARG, "buffer %llu's allocation is already mapped "
+                                "on device %d, not on the descriptor's device %d",
+                                (unsigned long long)i, it->second.device, device);
+                }
                 mp.base = it->second.base;
             } else {
                 cudaIpcMemHandle_t h;
@@ -2084,6 +2213,7 @@ kv_status kv_restore_layers(kv_pool pool_h, kv_host host_h, const int32_t *host_
     if (st != KV_OK) return st;
     DevState &ds = g_dev[d];
     cudaStream_t stream = (cudaStream_t)stream_v;
+    forget_stream(ds, stream_v);
     uint64_t seq0 = 0;
     st = reserve_fence_range(d, num_layers, &seq0);
     if (st != KV_OK) return st;
@@ -2178,7 +2308,13 @@ kv_status kv_fence_query(kv_fence f) {
     if (aborted)
         return fail(KV_ERR_ABORTED, "fence %llu: the ready fence was not reached in time; the "
                     "operation moved nothing", (unsigned long long)f);
-    if (g_dev[d].err != nullptr && __atomic_load_n(g_dev[d].err, __ATOMIC_ACQUIRE) != 0)
+    const uint32_t kerr = g_dev[d].err != nullptr ? __atomic_load_n(g_dev[d].err, __ATOMIC_ACQUIRE)
+                                                  : 0u;
+    if (kerr == 3u)
+        return fail(KV_ERR_TIMEOUT, "an overlapped restore gave up waiting (2 s of GPU time) for "
+                    "the previous restore's fence and published its own anyway: fences may have "
+                    "completed out of call order");
+    if (kerr != 0u)
         return fail(KV_ERR_OUT_OF_RANGE, "a transfer kernel met an out-of-range id and skipped it");
     return done ? KV_OK : KV_ERR_TIMEOUT;
 }

@@ -68,7 +68,8 @@ struct MoveDesc {
     uint32_t transpose;  // 1 when the two sides' head orders differ (H, T > 1)
     uint32_t iter_dst;   // transpose only: 1 = walk destination order
     FastDiv div_segs, div_lc, div_c, div_b16, div_T, div_H;
-    uint32_t *err;       // device-visible word set to 1 if a kernel meets a bad id
+    uint32_t *err;       // device-visible sticky word: 1 a kernel met a bad id, 2 a bulk
+                         // copy's wait gave up, 3 a chained fence's wait gave up
     // Completion, fused: when fence_word is set, the last CTA to finish stores
     // fence_seq there (system scope, release) once every CTA's bytes are
     // visible; fence_count is a zeroed device counter that CTA resets.
@@ -96,6 +97,19 @@ struct MoveDesc {
     // previous kernel on its stream finishes; it waits (griddepcontrol.wait)
     // for that kernel's completion before touching memory.
     uint32_t pdl;
+    // Overlapped restores (KV_CFG_OVERLAP_RESTORES).  early_trigger: each warp
+    // lets the next kernel on the stream launch when it takes its last segment
+    // rather than after it, so a successor that starts moving at once finds the
+    // link still busy with this kernel's last bytes.  overlap: the host proved
+    // that this restore and the previous kernel on the stream (a restore of
+    // the same pool) write disjoint bytes and neither writes what the other
+    // reads, so this kernel skips griddepcontrol.wait; its last CTA publishes
+    // the fence only once the previous op's fence word (chain_word) holds
+    // chain_seq or more, so fences still complete in call order.
+    uint32_t early_trigger;
+    uint32_t overlap;
+    const unsigned long long *chain_word;
+    unsigned long long chain_seq;
     // Ids in device memory (item i: gid_a[i], gid_b[i]) instead of the launch's
     // parameter block, for one move kernel over more items than a parameter
     // block holds (progressive restores of more than kMaxItems pages).

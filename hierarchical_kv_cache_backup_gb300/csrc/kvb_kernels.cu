@@ -85,10 +85,40 @@ __device__ __forceinline__ uint64_t chunk_base(const Side &s, uint32_t id, uint6
     return s.base + id * s.s_id + l * s.s_l + c * s.s_c;
 }
 
+// GPU time in nanoseconds (the global timer), for bounded waits.
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Overlapped restores: the last CTA waits until the previous op's fence word
+// holds chain_seq or more before it publishes its own, so fences complete in
+// call order.  The previous kernel let this one launch only once each of its
+// CTAs was running its last segments, so it is resident and finishes without
+// waiting for anything here: the wait ends.  It is bounded all the same
+// (2 s of GPU time, and a poll cap in case the timer stalls); on giving up it
+// sets the sticky error word (3), which the host reports with the fence.
+__device__ __forceinline__ void chain_wait(const MoveDesc &d) {
+    const unsigned long long t0 = global_ns();
+    unsigned int sleep_ns = 32;
+    for (uint32_t polls = 0; polls < (1u << 24); ++polls) {
+        unsigned long long v;
+        asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(d.chain_word)
+                     : "memory");
+        if (v >= d.chain_seq) return;
+        if (global_ns() - t0 > 2000000000ull) break;
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 1024) sleep_ns <<= 1;
+    }
+    if (d.err != nullptr) *(volatile uint32_t *)d.err = 3u;
+}
+
 // Completion of a grid, fused into its last CTA: every thread makes its own
 // stores visible system-wide, the CTA counts itself done, and the CTA that
 // finishes last publishes the sequence number for the host (and resets the
-// counter for the fence slot's next use).
+// counter for the fence slot's next use); an overlapped restore first waits
+// for its predecessor's fence (chain_wait).
 __device__ __forceinline__ void complete_grid(const MoveDesc &d) {
     __threadfence_system();
     __syncthreads();
@@ -100,6 +130,7 @@ __device__ __forceinline__ void complete_grid(const MoveDesc &d) {
                      : "memory");
         if (done == gridDim.x - 1) {
             *d.fence_count = 0u;
+            if (d.chain_word != nullptr) chain_wait(d);
             __threadfence_system();
             asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.fence_word),
                          "l"(d.fence_seq)
@@ -168,9 +199,11 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
     const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
     const uint32_t lc_per_item = d.nl * d.C;
 
-    if (d.pdl) {
+    if (d.pdl && !d.overlap) {
         // Wait for the previous kernel on this stream (and its memory) before
         // any access here; a no-op when it was not launched as a dependent.
+        // An overlapped restore skips it: the host proved the two kernels'
+        // bytes disjoint, and its fence is chained on the previous op's.
         asm volatile("griddepcontrol.wait;" ::: "memory");
     }
     uint32_t cur_layer = 0xffffffffu, cur_count = 0;   // progressive: this warp's tally
@@ -197,6 +230,10 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
         w = __shfl_sync(0xffffffffu, t, 0);
     }
     for (; w < d.total_segs;) {
+        if (d.early_trigger && w + nwarps >= d.total_segs) {
+            // this warp's last segment (grid stride): the next kernel may launch
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        }
         uint32_t seg, item, lr, c;
         if (d.layer_major) {   // layer, then item, component, segment
             lr = fdiv(w, d.div_pls);
@@ -304,12 +341,6 @@ __global__ void __launch_bounds__(kThreads, kThreads == kWideThreads ? 1 : 4)
 }
 
 // ----------------------------------------------------------- bulk (TMA) path
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
 
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

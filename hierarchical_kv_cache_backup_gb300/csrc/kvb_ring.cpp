@@ -37,6 +37,7 @@
 #include <sys/stat.h>
 #include <unistd.h>
 #include <unordered_map>
+#include <vector>
 
 namespace {
 
@@ -82,6 +83,15 @@ struct RingObj {
     uint32_t *srv_result = nullptr;       // mapped pinned: served, status
     uint32_t *srv_result_dev = nullptr;
     kv_fence srv_fence = 0;               // completes when the last resident server ended
+    // Stores into the segment queued on streams (ready words set from a stream,
+    // completion marks of the host server): per (stream, device), an event
+    // recorded after the last one; close waits for them before unmapping.
+    struct PendingStore {
+        void *stream;
+        int device;
+        cudaEvent_t ev;
+    };
+    std::vector<PendingStore> stores;
 };
 
 std::mutex g_rings_mu;
@@ -171,6 +181,54 @@ kv_status register_segment(RingObj *o) {
     o->comp_dev = (CompRec *)(o->seg_dev + o->h->comp_off);
     o->registered = true;
     return KV_OK;
+}
+
+// After a store into the segment was launched on `stream` (current device):
+// records that stream's event, so close can tell when the store has run.
+// Caller holds o->mu.
+kv_status note_store(RingObj *o, void *stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return err(KV_ERR_CUDA, "cudaGetDevice failed");
+    }
+    RingObj::PendingStore *ps = nullptr;
+    for (auto &x : o->stores)
+        if (x.stream == stream && x.device == dev) ps = &x;
+    if (ps == nullptr) {
+        cudaEvent_t ev = nullptr;
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return err(KV_ERR_CUDA, "cudaEventCreate for a ring store failed");
+        }
+        o->stores.push_back(RingObj::PendingStore{stream, dev, ev});
+        ps = &o->stores.back();
+    }
+    if (cudaEventRecord(ps->ev, (cudaStream_t)stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return err(KV_ERR_CUDA, "cudaEventRecord after a ring store failed");
+    }
+    return KV_OK;
+}
+
+// Whether every store queued into the segment has run, polling for at most
+// timeout_ns.
+bool stores_done(RingObj *o, double timeout_ns) {
+    const double deadline = now_ns() + timeout_ns;
+    for (auto &x : o->stores) {
+        for (;;) {
+            const cudaError_t e = cudaEventQuery(x.ev);
+            if (e == cudaSuccess) break;
+            if (e != cudaErrorNotReady) {   // a broken context: nothing will run any more
+                (void)cudaGetLastError();
+                break;
+            }
+            if (now_ns() >= deadline) return false;
+            timespec ts{0, 50000};
+            nanosleep(&ts, nullptr);
+        }
+    }
+    return true;
 }
 
 uint32_t slot_of(const RingObj *o, uint64_t t) { return (uint32_t)((t - 1) % o->h->slots); }
@@ -266,13 +324,26 @@ kv_status kv_ring_attach(const char *name, kv_ring *out) {
 
 kv_status kv_ring_close(kv_ring r) {
     RingObj *o;
+    const uint64_t id = (uint64_t)(uintptr_t)r;
     {
         std::lock_guard<std::mutex> lk(g_rings_mu);
-        auto it = g_rings.find((uint64_t)(uintptr_t)r);
+        auto it = g_rings.find(id);
         if (it == g_rings.end()) return err(KV_ERR_CLOSED, "ring handle is closed or unknown");
         o = it->second;
         g_rings.erase(it);
     }
+    // A store into the segment still queued on a stream would land in unmapped
+    // memory after munmap: wait (bounded) for each, else keep the ring open.
+    if (!stores_done(o, 2e9)) {
+        std::lock_guard<std::mutex> lk(g_rings_mu);
+        g_rings[id] = o;
+        return err(KV_ERR_TIMEOUT, "a store into the ring's segment queued on a stream "
+                   "(kv_ring_ready_stream_set, or a completion of kv_ring_serve) has not run "
+                   "within 2 s: the ring stays open; close it again once that stream's work "
+                   "has finished");
+    }
+    for (auto &x : o->stores) cudaEventDestroy(x.ev);
+    o->stores.clear();
     kv_status s = KV_OK;
     if (o->srv_fence != 0 && kv_fence_query(o->srv_fence) == KV_ERR_TIMEOUT) {
         // a resident server still reads the segment: ask it to stop, and never
@@ -417,7 +488,7 @@ kv_status kv_ring_ready_stream_set(kv_ring r, uint32_t index, uint64_t value, vo
         (void)cudaGetLastError();
         return err(KV_ERR_CUDA, "launch of the ready-word store failed");
     }
-    return KV_OK;
+    return note_store(o, stream);
 }
 
 kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_host host,
@@ -477,21 +548,36 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
         if (prev != device) cudaSetDevice(device);
         CompRec *cd = &o->comp_dev[slot_of(o, t)];
         cudaError_t e = cudaSuccess;
+        kv_status fail_st = KV_OK;   // completed from the CPU with this status instead
         if (gated) {   // the ticket reports a gate that gave up (ABORTED)
             const unsigned long long *status = nullptr;
             unsigned long long tag = 0;
-            kvb::fence_gate_word(f, &status, &tag);
-            e = kvb::launch_ring_mark((unsigned long long *)&cd->done,
-                                      (unsigned long long *)&cd->err_ticket, &cd->err, t, status,
-                                      tag, (cudaStream_t)stream);
+            const int gs = kvb::fence_gate_word(f, &status, &tag);
+            if (gs != KV_OK)
+                fail_st = (kv_status)gs;   // never report a gated op OK without its gate's word
+            else
+                e = kvb::launch_ring_mark((unsigned long long *)&cd->done,
+                                          (unsigned long long *)&cd->err_ticket, &cd->err, t,
+                                          status, tag, (cudaStream_t)stream);
         } else {
             e = kvb::launch_mark((unsigned long long *)&cd->done, t, (cudaStream_t)stream);
         }
-        if (prev >= 0 && prev != device) cudaSetDevice(prev);
         if (e != cudaSuccess) {
             (void)cudaGetLastError();
+            fail_st = KV_ERR_CUDA;
+        } else if (fail_st == KV_OK) {
+            std::lock_guard<std::mutex> lk(o->mu);
+            fail_st = note_store(o, stream);
+            if (fail_st != KV_OK) {
+                // the mark is queued but close could not see it: let it run first
+                cudaStreamSynchronize((cudaStream_t)stream);
+                fail_st = KV_OK;
+            }
+        }
+        if (prev >= 0 && prev != device) cudaSetDevice(prev);
+        if (fail_st != KV_OK) {
             kv_fence_wait(f, 60ull * 1000 * 1000 * 1000);   // the bytes land; report the failure
-            complete_cpu(o, t, KV_ERR_CUDA);
+            complete_cpu(o, t, fail_st);
         }
     }
     return KV_OK;

@@ -40,6 +40,7 @@ KV_NHD, KV_HND = 0, 1
 KV_MODE_ZERO_COPY, KV_MODE_STAGED, KV_MODE_COPY_ENGINE = 0, 1, 2
 KV_CFG_NO_BULK = 1
 KV_CFG_NO_PDL = 2
+KV_CFG_OVERLAP_RESTORES = 4
 KVB_IPC_MAGIC = 0x4B564231
 KVB_IPC_MAGIC_SPLIT = 0x4B564253
 
@@ -50,7 +51,7 @@ EXPORTS = ("kv_pool_register", "kv_pool_register_split", "kv_pool_export", "kv_p
            "kv_restore", "kv_restore_layers", "kv_backup_when_ready", "kv_restore_when_ready", "kv_device_gather", "kv_device_scatter", "kv_backup_staged_noalloc",
            "kv_op_validate", "kv_fence_query", "kv_fence_wait",
            "kv_fence_stream_wait", "kv_config_get", "kv_config_set", "kv_layout_page_bytes",
-           "kv_launch_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
+           "kv_launch_count", "kv_overlap_count", "kv_last_error", "kv_abi_version", "kv_ring_create",
            "kv_ring_attach", "kv_ring_close", "kv_ring_submit", "kv_ring_wait", "kv_ring_serve",
            "kv_ring_pop", "kv_ring_complete", "kv_ring_serve_device", "kv_ring_device_result",
            "kv_ring_device_stop", "kv_ring_ready_set", "kv_ring_ready_stream_set",
@@ -138,6 +139,7 @@ def _load():
         "kv_config_set": (st, [P(kv_config)]),
         "kv_layout_page_bytes": (st, [P(kv_layout), P(u64)]),
         "kv_launch_count": (u64, []),
+        "kv_overlap_count": (u64, []),
         "kv_last_error": (ctypes.c_char_p, []),
         "kv_abi_version": (u32, []),
         "kv_ring_create": (st, [ctypes.c_char_p, u32, P(vp)]),
@@ -477,6 +479,11 @@ def kv_layout_page_bytes(layout: kv_layout) -> int:
 def kv_launch_count() -> int:
     """Kernels the library has launched so far (all devices)."""
     return _lib.kv_launch_count()
+
+
+def kv_overlap_count() -> int:
+    """Restores issued overlapped with the previous one on their stream so far."""
+    return _lib.kv_overlap_count()
 
 
 def kv_last_error() -> str:

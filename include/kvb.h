@@ -155,6 +155,26 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
 #define KV_CFG_NO_PDL 2u    /* zero-copy moves and device gathers / scatters launch plainly:
                                no programmatic dependent launch overlapping a kernel's
                                launch with the previous kernel's end */
+/* KV_CFG_OVERLAP_RESTORES (opt-in; needs programmatic dependent launch, so it
+ * has no effect together with KV_CFG_NO_PDL).  A zero-copy kv_restore may start
+ * moving bytes while the previous kernel on its stream is still finishing,
+ * instead of after it, when the library can prove the two independent: that
+ * kernel is the last kv_restore issued on the same stream through this
+ * library, of the same pool handle, with no other call of this library on that
+ * stream in between, and the two write disjoint bytes -- different layers
+ * (both one-layer restores), or no destination page in common.  A restore
+ * only reads the host tier, so nothing else of the two can conflict.  This is
+ * the layer-by-layer restore of the PP prefetch PR (§PP Prefetch Ticket Path,
+ * "Layer-wise H2D + forward"): consecutive one-layer restores keep the host
+ * link busy across the boundary between calls instead of draining it.  The
+ * overlapping restore must fit one launch (n <= 2,048 pages).  Fences still
+ * complete in call order: the later restore publishes its fence only after the
+ * earlier one's (a wait on the GPU, bounded at 2 s; if it ever gave up, every
+ * later fence query reports KV_ERR_TIMEOUT).  Contract: the library cannot see
+ * work that the caller itself puts on the stream between two restores; under
+ * this flag such work must not write the host slots or pages the later restore
+ * reads or writes, nor read the pages it writes. */
+#define KV_CFG_OVERLAP_RESTORES 4u
 
 /* Defaults: host-link moves (zero-copy backup / restore) run 16 CTAs of 1024
  * threads when pool and tier share a head order and 64 CTAs of 256 when the
@@ -450,10 +470,16 @@ KVB_API kv_status kv_ring_create(const char *name, uint32_t slots, kv_ring *out)
 /* Attaches to an existing ring.  Errors: INVALID_ARG (no such ring, wrong
  * magic or version, or a header whose regions do not fit the segment). */
 KVB_API kv_status kv_ring_attach(const char *name, kv_ring *out);
-/* Detaches (and unlinks, for the creator; unregisters the segment from CUDA,
- * for a server).  A resident server still running on this handle is asked to
- * stop and waited for (bounded); if it has not ended, TIMEOUT and the memory
- * stays mapped.  Errors: CLOSED, TIMEOUT. */
+/* Detaches (and unlinks, for the creator).  Any process that registered the
+ * segment with CUDA -- a server, or a submitter that called
+ * kv_ring_ready_stream_set -- unregisters it here, so every store into the
+ * segment that this process queued on a stream (ready words set from a
+ * stream, the host server's completion marks) must run first: close waits up
+ * to 2 s for them, and if one has not run it returns TIMEOUT and the ring
+ * stays open (the handle stays valid: close it again once that stream's work
+ * has finished).  A resident server still running on this handle is asked to
+ * stop and waited for (bounded); if it has not ended, TIMEOUT, the handle is
+ * closed and the memory stays mapped.  Errors: CLOSED, TIMEOUT. */
 KVB_API kv_status kv_ring_close(kv_ring ring);
 
 /* Submitter: copies `op` into the next slot and publishes it; waits up to
@@ -500,9 +526,11 @@ KVB_API kv_status kv_ring_serve(kv_ring ring, const kv_pool *pools, uint32_t npo
 /* Server without a GPU (tests, or a server that moves bytes some other way):
  * takes the next descriptor (waiting up to timeout_ns; TIMEOUT if none) ...
  * A descriptor that kv_ring_submit would refuse (unknown kind, n above
- * KV_RING_MAX_IDS: written into the shared segment some other way) is taken,
- * completed with INVALID_ARG and reported as INVALID_ARG with *ticket set and
- * op->n = 0; kv_ring_serve counts it as served and moves on. */
+ * KV_RING_MAX_IDS, or a bad gate: ready_index >= KV_RING_READY_WORDS or
+ * ready_timeout_ms above 60000 on a gated op -- written into the shared
+ * segment some other way) is taken, completed with INVALID_ARG and reported as
+ * INVALID_ARG with *ticket set and op->n = 0; kv_ring_serve counts it as
+ * served and moves on. */
 KVB_API kv_status kv_ring_pop(kv_ring ring, uint64_t timeout_ns, kv_ring_op *op,
                               uint64_t *ticket);
 /* ... and completes a ticket from the CPU with the given status. */
@@ -626,6 +654,10 @@ KVB_API kv_status kv_config_set(const kv_config *cfg);
 KVB_API kv_status kv_layout_page_bytes(const kv_layout *layout, uint64_t *out);
 /* Number of kernels this library has launched in this process. */
 KVB_API uint64_t kv_launch_count(void);
+/* Number of restores this process issued overlapped with the previous one on
+ * their stream (KV_CFG_OVERLAP_RESTORES): a way to check that the flag applies
+ * to a caller's pattern of calls. */
+KVB_API uint64_t kv_overlap_count(void);
 /* Message of the last failing call on this thread ("" if none). */
 KVB_API const char *kv_last_error(void);
 KVB_API uint32_t kv_abi_version(void);
