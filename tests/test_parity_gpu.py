@@ -292,20 +292,20 @@ def test_retired_generation_is_refused():
 
 
 def test_fence_stream_wait_orders_compute_after_restore():
-    """A compute stream that waits on a layer's fence sees that layer restored."""
+    """A compute stream that waits on a layer's fence sees that layer restored: a
+    copy of the whole allocation taken on the compute stream equals the oracle's
+    pool after the restore."""
     g = wl.MLA_FP8.geom.with_(P=8, L=4)
     rig = Rig(g, 2, seed=6)
     try:
+        want = rig.expect_restore(rig.snapshot(), [0, 1], [5, 2], layer=3)
         copy_s, comp_s = torch.cuda.Stream(), torch.cuda.Stream()
         f = kvb.kv_restore(rig.pool, rig.hostt, [0, 1], [5, 2], 3, copy_s.cuda_stream)
         kvb.kv_fence_stream_wait(f, comp_s.cuda_stream)
-        lb = g.layer_page_bytes
         with torch.cuda.stream(comp_s):
-            # layer-first pool: page p of layer l starts at (l*C*P + p) * T*H*B
-            got = rig.alloc[(3 * 8 + 5) * lb:(3 * 8 + 6) * lb].clone()
+            got = rig.alloc.clone()
         comp_s.synchronize()
-        want = rig.host[0 * g.page_bytes + 3 * lb:0 * g.page_bytes + 4 * lb]
-        assert torch.equal(got.cpu(), want)
+        assert np.array_equal(got.cpu().numpy(), want[0])
     finally:
         rig.close()
 
