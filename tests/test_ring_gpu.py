@@ -124,3 +124,51 @@ def test_scheduler_and_data_plane_over_the_ring(wname, server):
             p.join(60)
         kvb.kv_ring_close(ring)
         kvb.kv_pool_close(pool)
+
+
+
+def test_close_waits_for_a_store_queued_on_a_stream():
+    """kv_ring_close unregisters and unmaps the shared segment, so a ready-word
+    store still queued on a stream must run first: closing right after one that
+    waits behind ~4 s of GPU work returns TIMEOUT and keeps the ring open (the
+    segment stays mapped, so the store lands in it); once the stream is done,
+    closing the same handle succeeds, and a descriptor gated on that word is
+    served at once, its bytes equal to the oracle's BACKUP."""
+    import time
+
+    name = f"/kvbtest_close_{os.getpid()}_{uuid.uuid4().hex[:8]}"
+    sub = kvb.kv_ring_create(name, 4)
+    srv = kvb.kv_ring_attach(name)
+    s = torch.cuda.Stream()
+    rig = Rig(wl.TINY.geom, wl.TINY.host_slots, seed=3)
+    try:
+        kvb.kv_ring_ready_stream_set(srv, 3, 1, s.cuda_stream)   # loads the store's kernel
+        s.synchronize()
+        kvb.kv_ring_close(srv)                                    # nothing pending: closes
+        srv = kvb.kv_ring_attach(name)
+        with torch.cuda.stream(s):
+            torch.cuda._sleep(8_000_000_000)                      # bounded GPU spin, ~4 s
+        kvb.kv_ring_ready_stream_set(srv, 3, 7, s.cuda_stream)
+        t0 = time.monotonic()
+        with pytest.raises(kvb.KvError) as e:
+            kvb.kv_ring_close(srv)
+        assert e.value.status == kvb.KV_ERR_TIMEOUT
+        assert time.monotonic() - t0 >= 1.5
+        assert "stays open" in kvb.kv_last_error()
+        s.synchronize()                                           # the store has run
+        kvb.kv_ring_close(srv)                                    # the same handle closes now
+        srv = kvb.kv_ring_attach(name)
+        want = rig.expect_backup(rig.snapshot(), [1, 2], [0, 1])
+        tk = kvb.kv_ring_submit(sub, kvb.make_ring_op(0, [1, 2], [0, 1], ready_index=3,
+                                                      ready_value=7, ready_timeout_ms=3000))
+        served = kvb.kv_ring_serve(srv, [rig.pool], rig.hostt, s.cuda_stream, 1, 1_000_000_000)
+        assert served == 1
+        assert kvb.kv_ring_wait(sub, tk, 10_000_000_000) == kvb.KV_OK   # not ABORTED
+        s.synchronize()
+        rig.assert_equal(want)
+    finally:
+        rig.close()
+        if srv is not None:
+            s.synchronize()
+            kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
