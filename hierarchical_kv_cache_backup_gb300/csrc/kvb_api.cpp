@@ -731,6 +731,14 @@ constexpr int kLinkWideCtas = 16;   // CTAs of kWideThreads (cta_threads = 1024)
 // CTAs (8 SMs) still reach 98% of the H2D peak and cut the time of a 61-layer
 // restore pipelined with a per-layer GEMM from 4.26 ms (16 CTAs) to 3.54 ms.
 constexpr int kOverlapWideCtas = 8;
+// Overlapped restores (KV_CFG_OVERLAP_RESTORES) keep the link busy across
+// calls, so fewer SMs carry it: 61 one-layer restores on GB300 (MLA pool;
+// TRT-LLM HND pool) reach 98.8% / 98.7% of the H2D peak with 6 wide CTAs
+// alone, and pipelined with a GEMM per layer take 3.69 / 2.47 ms, as fast as
+// non-overlapped calls (3.70 / 2.44); 8 CTAs: 99.3% alone but 3.76 / 2.57 ms
+// pipelined; 16: 4.03 / 2.56 ms; 4: 88.8% alone.  Head-order changes use
+// 1,024-thread CTAs here too (32 x 256: 2.66 ms pipelined).
+constexpr int kOverlapRestoreCtas = 6;
 
 int link_threads(bool transpose) {
     if (g_cfg.cta_threads) return (int)g_cfg.cta_threads;
@@ -1161,6 +1169,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             p.d.skip_tag = fs.seq;
         }
         p.threads = link_threads(p.d.transpose != 0);
+        if (overlap_cfg && restore_kind && g_cfg.cta_threads == 0) p.threads = kWideThreads;
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
         if (overlap_cfg && restore_kind) {
             p.d.early_trigger = 1u;
@@ -1172,8 +1181,11 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                 overlapped = true;
             }
         }
-        st = run_moves(p, a, b, n, default_ctas(ds, true, PK_REG, p.threads), stream, false, &ds,
-                       &fs);
+        int ctas = default_ctas(ds, true, PK_REG, p.threads);
+        if (overlap_cfg && restore_kind && g_cfg.max_ctas == 0)
+            ctas = p.threads == kWideThreads ? std::min(kOverlapRestoreCtas, ds.sms)
+                                             : std::min(4 * kOverlapRestoreCtas, 4 * ds.sms);
+        st = run_moves(p, a, b, n, ctas, stream, false, &ds, &fs);
         if (st != KV_OK) return bail(st);
         fused = true;
     } else if (ready != nullptr) {   // an empty gated op: its fence follows the gate

@@ -170,7 +170,10 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
  * overlapping restore must fit one launch (n <= 2,048 pages).  Fences still
  * complete in call order: the later restore publishes its fence only after the
  * earlier one's (a wait on the GPU, bounded at 2 s; if it ever gave up, every
- * later fence query reports KV_ERR_TIMEOUT).  Contract: the library cannot see
+ * later fence query reports KV_ERR_TIMEOUT).  Under this flag zero-copy
+ * restores run, unless max_ctas / cta_threads say otherwise, on 6 CTAs of
+ * 1,024 threads (6 whole SMs): overlapped, that reaches ~99% of the H2D link
+ * and leaves the rest of the GPU to the forward pass.  Contract: the library cannot see
  * work that the caller itself puts on the stream between two restores; under
  * this flag such work must not write the host slots or pages the later restore
  * reads or writes, nor read the pages it writes. */
