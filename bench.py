@@ -444,6 +444,7 @@ class Ctx:
         self.peaks, self.peak_src = measured_peaks()
         self.clk = None
         self.link = None
+        self.probe_bufs = None   # set by measure_link: 1 GiB each way for bidir_nearby
 
     def set_config(self, overlap=None, mode=None, max_ctas=None, cta_threads=None):
         a, kvb = self.args, self.kvb
@@ -520,9 +521,39 @@ def measure_link(ctx, probe_alloc=None):
         ev2.record(s_b)
         s_a.wait_event(ev2)
     link["bidir"] = best_of(bidir, probe_n)
-    del pin, pin2, dbuf, dbuf2
-    torch.cuda.empty_cache()
+    # kept for bidir_nearby(): 1 GiB each way
+    ctx.probe_bufs = (pin[:probe_n // 2], dbuf[:probe_n // 2], pin2, dbuf2)
     return link
+
+
+def bidir_nearby(ctx):
+    """The bidirectional pinned-memcpy rate (1 GiB each way, best of 3) measured
+    right beside a concurrent measurement: the host link's capacity at that
+    moment.  Other tenants of the same host can take some of it, and concurrent
+    figures taken seconds apart then differ for that reason alone."""
+    torch = ctx.torch
+    pin, dbuf, pin2, dbuf2 = ctx.probe_bufs
+    s_a, s_b = ctx.s_a, ctx.s_b
+    ts = []
+    for i in range(4):
+        torch.cuda.synchronize()
+        e0, e1 = ctx.event(), ctx.event()
+        e0.record(s_a)
+        ev = torch.cuda.Event()
+        ev.record(s_a)
+        s_b.wait_event(ev)
+        with torch.cuda.stream(s_a):
+            pin.copy_(dbuf, non_blocking=True)
+        with torch.cuda.stream(s_b):
+            dbuf2.copy_(pin2, non_blocking=True)
+        ev2 = torch.cuda.Event()
+        ev2.record(s_b)
+        s_a.wait_event(ev2)
+        e1.record(s_a)
+        e1.synchronize()
+        if i >= 1:
+            ts.append(e0.elapsed_time(e1) / 1000)
+    return round((pin.numel() + pin2.numel()) / min(ts) / GB, 2)
 
 
 class Setup:
@@ -1078,7 +1109,9 @@ def trtllm_record(ctx):
     steps, warmup = max(5, min(args.steps, 20)), max(3, args.warmup)
     try:
         step, bytes_b, bytes_r = step_fn(ctx, su)
+        near0 = bidir_nearby(ctx)
         elapsed, evs, launches, win = timed_steps(ctx, step, steps, warmup)
+        near1 = bidir_nearby(ctx)
         b_ms = [e[0].elapsed_time(e[1]) for e in evs]
         r_ms = [e[3].elapsed_time(e[4]) for e in evs]
         step_bytes = bytes_b + bytes_r
@@ -1102,7 +1135,9 @@ def trtllm_record(ctx):
                         "unit": "GB/s", "frac": round(value / link["bidir"], 4), "traffic": None,
                         "algorithmic_bytes_per_launch": step_bytes,
                         "peak_source": "pinned cudaMemcpyAsync D2H || H2D (two streams, 1 GiB "
-                                       "each way) measured in this run, best of 10"},
+                                       "each way) measured in this run, best of 10",
+                        "bidir_memcpy_nearby_gbs": [near0, near1],
+                        "frac_of_nearby": round(value / max(near0, near1), 4)},
            "per_direction": {
                "note": "each direction while the other runs; secondary to the bidirectional "
                        "roofline",
@@ -1201,17 +1236,18 @@ def sweep_record(ctx):
     and copy-engine modes."""
     kvb, link = ctx.kvb, ctx.link
     modes = (("zero_copy", kvb.KV_MODE_ZERO_COPY), ("copy_engine", kvb.KV_MODE_COPY_ENGINE))
+    near0 = bidir_nearby(ctx)
     with Window() as win:
         recs = sweep_points(ctx, SUMMARY_SIZES, SUMMARY_BATCHES, modes, reps=5, warmup=2,
                             pages=4096)
+    near1 = bidir_nearby(ctx)
     ctx.set_config()
     peak = {"d2h": link["d2h"], "h2d": link["h2d"], "both": link["bidir"]}
-    points = []
-    for x in recs:
-        points.append({"page_bytes": x["page_bytes"], "batch": x["batch"], "ids": x["ids"],
-                       "mode": x["mode"], "direction": x["direction"], "gbs": round(x["gbs"], 2),
-                       "pct_of_peak": round(100 * x["gbs"] / peak[x["direction"]], 1),
-                       "us": round(1e6 * x["seconds"], 1)})
+    points = {"fields": ["page_bytes", "batch", "ids", "mode", "direction", "gbs",
+                         "pct_of_peak", "us"],
+              "rows": [[x["page_bytes"], x["batch"], x["ids"], x["mode"], x["direction"],
+                        round(x["gbs"], 2), round(100 * x["gbs"] / peak[x["direction"]], 1),
+                        round(1e6 * x["seconds"], 1)] for x in recs]}
     big = {d: next(x for x in recs if x["page_bytes"] == max(SUMMARY_SIZES) and
                    x["batch"] == max(SUMMARY_BATCHES) and x["ids"] == "random" and
                    x["mode"] == "zero_copy" and x["direction"] == d)
@@ -1244,6 +1280,8 @@ def sweep_record(ctx):
                          "unit": "GB/s", "frac": round(a / link["bidir"], 4), "traffic": None,
                          "algorithmic_bytes_per_launch": 2 * max(SUMMARY_BATCHES) *
                          max(SUMMARY_SIZES),
+                         "bidir_memcpy_nearby_gbs": [near0, near1],
+                         "frac_of_nearby": round(a / max(near0, near1), 4),
                          "one_way": {d: {"gbs": round(big[d]["gbs"], 2),
                                          "frac": round(big[d]["gbs"] / peak[d], 4)}
                                      for d in ("d2h", "h2d")}},
@@ -1543,8 +1581,12 @@ def small_ops(ctx, su):
                               old_cfg.flags, old_cfg.cta_threads)
         return [round(w.n * g.page_bytes / x / GB, 2) for x in times[1:]]
 
+    near = [bidir_nearby(ctx)]
     two32 = two_rings(0)
+    near.append(bidir_nearby(ctx))
     two64 = two_rings(64)
+    near.append(bidir_nearby(ctx))
+    ring_tp["bidir_memcpy_nearby_gbs"] = near
     ring_tp["device_served_two_rings_gbs"] = statistics.median(two32)
     ring_tp["device_served_two_rings_gbs_steps"] = two32
     ring_tp["device_served_two_rings_64_movers_gbs"] = statistics.median(two64)
@@ -1560,6 +1602,41 @@ def small_ops(ctx, su):
     kvb.kv_host_close(ttier)
     del talloc, thost
     return latency
+
+
+def records_summary(line):
+    """The line's main figures in a few hundred bytes, last on the line (a
+    reader that keeps only the line's tail still sees every record)."""
+    out = {"headline": {"gbs": line["value"], "roofline_frac": line["roofline"]["frac"],
+                        "e2e_gbs": line["e2e"]["value"]}}
+    if line.get("roofline_hbm"):
+        out["headline"]["hbm_gather_frac"] = line["roofline_hbm"]["frac"]
+    m = line.get("mla_fp8")
+    if m:
+        out["mla_fp8"] = {
+            "one_layer_calls_gbs": m["value"], "frac": m["roofline"]["frac"],
+            "overlapped_calls_gbs": m["overlapped_calls"]["gbs"],
+            "overlapped_frac": m["overlapped_calls"]["roofline"]["frac"],
+            "progressive_gbs": m["progressive_call"]["gbs"],
+            "progressive_frac": m["progressive_call"]["roofline"]["frac"],
+            "exposed_ms_beside_gemms": m["overlap_with_compute"]["exposed_transfer_ms"],
+            "cpu_gbs": m.get("cpu_baseline", {}).get("value")}
+    t = line.get("trtllm_ipc")
+    if t:
+        out["trtllm_ipc"] = {"gbs": t["value"], "frac_of_bidir": t["roofline"]["frac"],
+                             "d2h_gbs": t["per_direction"]["d2h"]["gbs"],
+                             "h2d_gbs": t["per_direction"]["h2d"]["gbs"],
+                             "hbm_gather_frac": t["roofline_hbm"]["frac"],
+                             "cpu_gbs": t.get("cpu_baseline", {}).get("value")}
+    w = line.get("sweep")
+    if w:
+        out["sweep"] = {"both_1MiB_x1024_random_gbs": w["value"],
+                        "frac_of_bidir": w["roofline"]["frac"],
+                        "one_way_frac": {d: v["frac"] for d, v in w["roofline"]["one_way"].items()},
+                        "cpu_gbs": w.get("cpu_baseline", {}).get("value")}
+    if line.get("cpu_baseline"):
+        out["cpu_baseline_gbs"] = line["cpu_baseline"]["value"]
+    return out
 
 
 def run_ours(args):
@@ -1607,6 +1684,7 @@ def run_ours(args):
                                                     "sample": sample2}
     else:
         line["cpu_baseline"] = None
+    line["records_summary"] = records_summary(line)
     if ctx.rank == 0:
         print(json.dumps(line), flush=True)
     if ctx.dist is not None:
