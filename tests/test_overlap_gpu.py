@@ -260,3 +260,43 @@ def test_compute_stream_waits_see_each_overlapped_layer(overlap):
         rig.assert_equal(want)
     finally:
         rig.close()
+
+
+def test_overlap_after_a_multi_launch_restore_and_a_gated_one(overlap):
+    """A restore above one launch's 2,048 pages is never overlapped itself but
+    starts a run the next restore may overlap; a gated restore in between ends
+    the run.  Whole buffers against the oracle in call order."""
+    g = wl.Geometry(L=3, C=2, P=5000, T=2, H=1, B=16, elem_bytes=1)
+    rig = Rig(g, 4500, seed=21)
+    r = np.random.default_rng(22)
+    s = torch.cuda.Stream()
+    ready = torch.zeros(1, dtype=torch.int64, device="cuda")
+    try:
+        want = rig.snapshot()
+        want = (want[0].copy(), want[1])
+        big_sl = r.permutation(4500)[:2100].astype(np.int32)
+        big_dst = r.permutation(5000)[:2100].astype(np.int32)
+        small_sl = r.permutation(4500)[:300].astype(np.int32)
+        small_dst = np.setdiff1d(np.arange(5000), big_dst)[r.permutation(5000 - 2100)[:300]]
+        small_dst = small_dst.astype(np.int32)
+        c0 = kvb.kv_overlap_count()
+        kvb.kv_restore(rig.pool, rig.hostt, big_sl, big_dst, 0, s.cuda_stream)     # 2 launches
+        kvb.kv_restore(rig.pool, rig.hostt, small_sl, small_dst, 0, s.cuda_stream)  # disjoint
+        assert kvb.kv_overlap_count() - c0 == 1
+        kvb.kv_restore(rig.pool, rig.hostt, small_sl, small_dst, 1, s.cuda_stream)  # layer 1
+        assert kvb.kv_overlap_count() - c0 == 2
+        ready.fill_(5)
+        torch.cuda.synchronize()
+        kvb.kv_restore_when_ready(rig.pool, rig.hostt, small_sl, small_dst, ready.data_ptr(),
+                                  5, 1_000_000_000, 2, s.cuda_stream)               # gated
+        f = kvb.kv_restore(rig.pool, rig.hostt, big_sl[:100], big_dst[:100], 1, s.cuda_stream)
+        assert kvb.kv_overlap_count() - c0 == 2                                     # after a gate
+        kvb.kv_fence_wait(f, 30_000_000_000)
+        og = oracle_geom(g)
+        for sl, dd, layer in ((big_sl, big_dst, 0), (small_sl, small_dst, 0),
+                              (small_sl, small_dst, 1), (small_sl, small_dst, 2),
+                              (big_sl[:100], big_dst[:100], 1)):
+            oracle.restore(og, want[0], want[1], sl, dd, layer=layer)
+        rig.assert_equal(want)
+    finally:
+        rig.close()

@@ -108,3 +108,33 @@ def test_split_pool_checks_on_device():
     lay2, ptr, nbytes = kvb.kv_pool_info(p)
     assert ptr == ptrs[0] and nbytes == g.pool_bytes
     kvb.kv_pool_close(p)
+
+
+@pytest.mark.parametrize("heads", [(wl.NHD, wl.NHD), (wl.HND, wl.NHD)], ids=["NHD", "HND-to-NHD"])
+def test_split_pool_overlapped_one_layer_restores(heads):
+    """Every layer restored one per call with KV_CFG_OVERLAP_RESTORES on a split
+    pool (each layer in its own buffers): all but the first overlapped, the
+    layer buffers equal the oracle's pool."""
+    g = wl.LLAMA8B.geom.with_(P=48, L=7, dev_heads=heads[0], host_heads=heads[1])
+    og = oracle_geom(g)
+    r = np.random.default_rng(6)
+    old = kvb.kv_config_get()
+    kvb.kv_config_set(kvb.KV_MODE_ZERO_COPY, 0, 0, kvb.KV_CFG_OVERLAP_RESTORES)
+    rig = SplitRig(g, 16, seed=60)
+    s = torch.cuda.Stream()
+    try:
+        want = rig.contiguous()
+        host_np = rig.host.numpy().copy()
+        slots = r.permutation(16).astype(np.int32)
+        dst = r.permutation(g.P)[:16].astype(np.int32)
+        c0 = kvb.kv_overlap_count()
+        fences = [kvb.kv_restore(rig.pool, rig.tier, slots, dst, l, s.cuda_stream)
+                  for l in range(g.L)]
+        assert kvb.kv_overlap_count() - c0 == g.L - 1
+        kvb.kv_fence_wait(fences[-1], 30_000_000_000)
+        for l in range(g.L):
+            oracle.restore(og, want, host_np, slots, dst, layer=l)
+        rig.assert_pool(want)
+    finally:
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+        rig.close()
