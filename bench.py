@@ -1238,10 +1238,11 @@ def sweep_points(ctx, sizes, batches, modes, reps, warmup, pages):
 
 def sweep_record(ctx):
     """A summary of the bandwidth sweep: page bytes {4 KiB, 64 KiB, 1 MiB} x
-    batch {1, 32, 1024} x {sequential, random} ids x {D2H, H2D, both}, zero-copy
-    and copy-engine modes."""
+    batch {1, 32, 1024} x {sequential, random} ids x {D2H, H2D, both}, in
+    zero-copy, STAGED and copy-engine mode."""
     kvb, link = ctx.kvb, ctx.link
-    modes = (("zero_copy", kvb.KV_MODE_ZERO_COPY), ("copy_engine", kvb.KV_MODE_COPY_ENGINE))
+    modes = (("zero_copy", kvb.KV_MODE_ZERO_COPY), ("staged", kvb.KV_MODE_STAGED),
+             ("copy_engine", kvb.KV_MODE_COPY_ENGINE))
     near0 = bidir_nearby(ctx)
     with Window() as win:
         recs = sweep_points(ctx, SUMMARY_SIZES, SUMMARY_BATCHES, modes, reps=5, warmup=2,
@@ -1262,22 +1263,19 @@ def sweep_record(ctx):
     wins = {}
     for d in ("d2h", "h2d", "both"):
         for ids in ("seq", "random"):
-            z = c = 0
+            count = {m: 0 for m, _ in modes}
             for pb in SUMMARY_SIZES:
                 for n in SUMMARY_BATCHES:
                     pt = {x["mode"]: x["gbs"] for x in recs if x["page_bytes"] == pb and
                           x["batch"] == n and x["ids"] == ids and x["direction"] == d}
-                    if pt["zero_copy"] >= pt["copy_engine"]:
-                        z += 1
-                    else:
-                        c += 1
-            wins[f"{d}_{ids}"] = {"zero_copy": z, "copy_engine": c}
+                    count[max(pt, key=pt.get)] += 1
+            wins[f"{d}_{ids}"] = count
     return {"workload": "one opaque run per page (L = C = T = H = 1, B = page bytes), 4,096-page "
                         "pool, random uint8 payload; ops of `batch` pages into slots 0..batch-1 "
                         "(backup) and from slots batch..2*batch-1 (restore)",
             "grid": {"page_bytes": SUMMARY_SIZES, "batch": SUMMARY_BATCHES,
                      "ids": ["seq", "random"], "direction": ["d2h", "h2d", "both"],
-                     "mode": ["zero_copy", "copy_engine"]},
+                     "mode": [m for m, _ in modes]},
             "value": round(a, 2), "unit": "GB/s",
             "roofline": {"bound": "host_link_bidirectional",
                          "kernel": "kv_move_kernel x 2 at once (1,024 random pages of 1 MiB each "

@@ -300,3 +300,40 @@ def test_overlap_after_a_multi_launch_restore_and_a_gated_one(overlap):
         rig.assert_equal(want)
     finally:
         rig.close()
+
+
+def test_ring_host_server_with_overlapped_restores(overlap):
+    """The host ring server issues each descriptor as kv_restore and a completion
+    mark on its stream; with the flag on, one-layer restore descriptors of every
+    layer still complete in ticket order, and the pool equals the oracle's."""
+    import os
+    import uuid
+
+    g = GEOMS["mla"]
+    n = 20
+    r = np.random.default_rng(31)
+    rig = Rig(g, n, seed=32)
+    name = f"/kvbtest_ovl_{os.getpid()}_{uuid.uuid4().hex[:8]}"
+    sub = kvb.kv_ring_create(name, 64)
+    srv = kvb.kv_ring_attach(name)
+    s = torch.cuda.Stream()
+    try:
+        want = rig.snapshot()
+        want = (want[0].copy(), want[1])
+        slots = r.permutation(n).astype(np.int32)
+        dst = wl.distinct_pages(r, g.P, n)
+        layers = [int(x) for x in r.permutation(g.L)]
+        tks = [kvb.kv_ring_submit(sub, kvb.make_ring_op(1, slots, dst, layer=l)) for l in layers]
+        served = 0
+        while served < len(tks):
+            served += kvb.kv_ring_serve(srv, [rig.pool], rig.hostt, s.cuda_stream, 64,
+                                        1_000_000_000)
+        for tk in tks:
+            assert kvb.kv_ring_wait(sub, tk, 30_000_000_000) == kvb.KV_OK
+        s.synchronize()
+        rig.assert_equal(expect_layers(rig, want, slots, dst, layers))
+    finally:
+        s.synchronize()
+        kvb.kv_ring_close(srv)
+        kvb.kv_ring_close(sub)
+        rig.close()
