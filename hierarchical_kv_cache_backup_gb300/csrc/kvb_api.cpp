@@ -1135,8 +1135,12 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     // Restores only read the host tier, so nothing else can conflict.
     const bool overlap_cfg = (g_cfg.flags & KV_CFG_OVERLAP_RESTORES) != 0 &&
                              (g_cfg.flags & KV_CFG_NO_PDL) == 0;
+    // Not on the legacy default stream nor the special handles (0, 1, 2): the
+    // legacy stream also waits on every blocking stream, so work the library
+    // cannot see may sit between two of its restores there.
+    const bool plain_stream = (uintptr_t)stream_v > 2u;
     const bool restore_kind = !backup && ready == nullptr && n > 0 &&
-                              g_cfg.mode == KV_MODE_ZERO_COPY;
+                              g_cfg.mode == KV_MODE_ZERO_COPY && plain_stream;
     bool chain = false, overlapped = false;
     int chain_k = 0;
     uint64_t chain_seq = 0;

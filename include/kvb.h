@@ -159,9 +159,10 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
  * has no effect together with KV_CFG_NO_PDL).  A zero-copy kv_restore may start
  * moving bytes while the previous kernel on its stream is still finishing,
  * instead of after it, when the library can prove the two independent: that
- * kernel is the last kv_restore issued on the same stream through this
- * library, of the same pool handle, with no other call of this library on that
- * stream in between, and the two write disjoint bytes -- different layers
+ * kernel is the last kv_restore issued on the same stream (a created stream:
+ * never the legacy default stream, cudaStreamLegacy or cudaStreamPerThread)
+ * through this library, of the same pool handle, with no other call of this
+ * library on that stream in between, and the two write disjoint bytes -- different layers
  * (both one-layer restores), or no destination page in common.  A restore
  * only reads the host tier, so nothing else of the two can conflict.  This is
  * the layer-by-layer restore of the PP prefetch PR (§PP Prefetch Ticket Path,

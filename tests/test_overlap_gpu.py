@@ -213,13 +213,16 @@ def test_other_pool_or_stream_does_not_chain(overlap):
         kvb.kv_restore(rig2.pool, rig2.hostt, sl, dst, 1, s1.cuda_stream)   # other pool
         kvb.kv_restore(rig.pool, rig.hostt, sl, dst, 2, s2.cuda_stream)     # other stream
         assert kvb.kv_overlap_count() == c0
+        kvb.kv_restore(rig.pool, rig.hostt, sl, dst, 5, None)               # legacy stream
+        kvb.kv_restore(rig.pool, rig.hostt, sl, dst, 6, None)
+        assert kvb.kv_overlap_count() == c0
         overlap(flags=kvb.KV_CFG_OVERLAP_RESTORES | kvb.KV_CFG_NO_PDL)
         kvb.kv_restore(rig.pool, rig.hostt, sl, dst, 3, s2.cuda_stream)
         overlap(flags=0)
         kvb.kv_restore(rig.pool, rig.hostt, sl, dst, 4, s2.cuda_stream)
         assert kvb.kv_overlap_count() == c0
         torch.cuda.synchronize()
-        expect_layers(rig, want1, sl, dst, [0, 2, 3, 4])
+        expect_layers(rig, want1, sl, dst, [0, 2, 5, 6, 3, 4])
         expect_layers(rig2, want2, sl, dst, [1])
         rig.assert_equal(want1)
         rig2.assert_equal(want2)
