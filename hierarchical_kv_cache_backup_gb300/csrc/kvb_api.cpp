@@ -62,11 +62,14 @@ kv_status cuda_fail(cudaError_t e, const char *what) {
 // §Targeted fault-injection validation: injected allocation failures must fall
 // back and leave the service running).  The next `count` passes through a
 // point fail as if the CUDA call there had failed ("launch_nth": only the
-// count-th pass from now fails); nothing touches the GPU.
+// count-th pass from now fails); nothing touches the GPU.  "chain_stall" is
+// the one drill that reaches a kernel: the next overlapped restore chains its
+// fence on a sequence number its predecessor never stores, so its bounded
+// wait runs out (2 s) and the kernel reports it through the error word.
 enum FaultPoint { FP_STAGING_ALLOC, FP_FENCE_RESERVE, FP_LAUNCH, FP_IPC_OPEN, FP_HOST_REGISTER,
-                  FP_LAUNCH_NTH, FP_COUNT };
+                  FP_LAUNCH_NTH, FP_CHAIN_STALL, FP_COUNT };
 const char *const kFaultNames[FP_COUNT] = {"staging_alloc", "fence_reserve", "launch", "ipc_open",
-                                           "host_register", "launch_nth"};
+                                           "host_register", "launch_nth", "chain_stall"};
 std::atomic<uint32_t> g_fault[FP_COUNT];
 std::once_flag g_fault_env_once;
 
@@ -1181,7 +1184,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             if (chain && n <= p.max_items) {
                 p.d.overlap = 1u;
                 p.d.chain_word = ds.words_dev + chain_k;
-                p.d.chain_seq = chain_seq;
+                p.d.chain_seq = fault_hit(FP_CHAIN_STALL) ? ~0ull : chain_seq;
                 overlapped = true;
             }
         }

@@ -673,9 +673,15 @@ KVB_API uint32_t kv_abi_version(void);
  * "launch" (CUDA, at an op's first kernel launch), "ipc_open" (CUDA),
  * "host_register" (CUDA), "launch_nth" (CUDA: only the count-th move-kernel
  * launch from now fails, possibly in the middle of an op -- what the op had
- * enqueued before it still runs, and later ops wait for it); count 0 disarms.  The environment variable
- * KVB_FAULT="point:count[,point:count]" arms points at first use.  Nothing
- * here touches the GPU.  Errors: INVALID_ARG for an unknown point. */
+ * enqueued before it still runs, and later ops wait for it); count 0 disarms.
+ * One drill reaches a kernel without faulting it: "chain_stall" makes the next
+ * overlapped restore (KV_CFG_OVERLAP_RESTORES) chain its fence on a sequence
+ * number that never arrives, so its bounded GPU wait runs out after 2 s, its
+ * bytes still land, and from then on every fence query of this process on
+ * that device reports TIMEOUT (the kernel error word is sticky: drill it in a
+ * process of its own).  The environment variable
+ * KVB_FAULT="point:count[,point:count]" arms points at first use.  Errors:
+ * INVALID_ARG for an unknown point. */
 KVB_API kv_status kv_fault_inject(const char *point, uint32_t count);
 
 #ifdef __cplusplus

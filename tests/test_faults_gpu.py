@@ -218,3 +218,51 @@ def test_gated_op_failing_after_its_gate_does_not_poison_the_next_op(rig):
     kvb.kv_fence_wait(f, 20_000_000_000)
     assert kvb.kv_fence_query(f) == kvb.KV_OK
     rig.assert_equal(want)
+
+
+_CHAIN_STALL_CHILD = r'''
+import sys, numpy as np, torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + "/tests"]
+import oracle
+from gpu_rig import Rig, oracle_geom
+from hierarchical_kv_cache_backup_gb300 import kvb
+from hierarchical_kv_cache_backup_gb300 import workloads as wl
+g = wl.MLA_FP8.geom.with_(P=64, L=4)
+rig = Rig(g, 8, seed=71)
+want = rig.snapshot()
+want = (want[0].copy(), want[1])
+s = torch.cuda.Stream()
+kvb.kv_config_set(kvb.KV_MODE_ZERO_COPY, 0, 0, kvb.KV_CFG_OVERLAP_RESTORES)
+slots, dst = np.arange(8, dtype=np.int32), np.arange(10, 18, dtype=np.int32)
+f0 = kvb.kv_restore(rig.pool, rig.hostt, slots, dst, 0, s.cuda_stream)
+kvb.kv_fault_inject("chain_stall", 1)
+f1 = kvb.kv_restore(rig.pool, rig.hostt, slots, dst, 1, s.cuda_stream)   # overlapped, stalls
+assert kvb.kv_overlap_count() == 1
+s.synchronize()                                     # the wait ran out and the kernel ended
+try:
+    kvb.kv_fence_wait(f1, 30_000_000_000)
+    print("NO-ERROR")
+except kvb.KvError as e:
+    print("STATUS", e.status == kvb.KV_ERR_TIMEOUT, "out of call order" in kvb.kv_last_error())
+for layer in (0, 1):
+    oracle.restore(oracle_geom(g), want[0], want[1], slots, dst, layer=layer)
+rig.assert_equal(want)                              # the bytes landed all the same
+print("BYTES-OK")
+'''
+
+
+def test_chained_fence_wait_runs_out_and_reports_timeout():
+    """An overlapped restore whose chained fence wait cannot be satisfied (the
+    "chain_stall" drill: a sequence number its predecessor never stores) gives
+    up after its 2 s bound, publishes its fence, and every fence query then
+    reports KV_ERR_TIMEOUT; its bytes are the oracle's.  Run in a child process:
+    the kernel error word it sets is sticky for the process."""
+    import subprocess
+    import sys
+    root = __import__("os").path.dirname(__import__("os").path.dirname(
+        __import__("os").path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _CHAIN_STALL_CHILD, root], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "STATUS True True" in r.stdout, r.stdout + r.stderr
+    assert "BYTES-OK" in r.stdout
