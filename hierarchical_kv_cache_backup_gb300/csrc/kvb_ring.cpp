@@ -211,22 +211,43 @@ kv_status note_store(RingObj *o, void *stream) {
     return KV_OK;
 }
 
+// Runs f() with `device` current, then restores the caller's device.
+template <class F>
+void on_device(int device, F f) {
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != device) cudaSetDevice(device);
+    f();
+    if (prev >= 0 && prev != device) cudaSetDevice(prev);
+}
+
 // Whether every store queued into the segment has run, polling for at most
-// timeout_ns.
+// timeout_ns (each event queried with its own device current).
 bool stores_done(RingObj *o, double timeout_ns) {
     const double deadline = now_ns() + timeout_ns;
     for (auto &x : o->stores) {
-        for (;;) {
-            const cudaError_t e = cudaEventQuery(x.ev);
-            if (e == cudaSuccess) break;
-            if (e != cudaErrorNotReady) {   // a broken context: nothing will run any more
-                (void)cudaGetLastError();
-                break;
+        bool done = false, expired = false;
+        on_device(x.device, [&] {
+            for (;;) {
+                const cudaError_t e = cudaEventQuery(x.ev);
+                if (e == cudaSuccess) {
+                    done = true;
+                    return;
+                }
+                if (e != cudaErrorNotReady) {   // a broken context: nothing will run any more
+                    (void)cudaGetLastError();
+                    done = true;
+                    return;
+                }
+                if (now_ns() >= deadline) {
+                    expired = true;
+                    return;
+                }
+                timespec ts{0, 50000};
+                nanosleep(&ts, nullptr);
             }
-            if (now_ns() >= deadline) return false;
-            timespec ts{0, 50000};
-            nanosleep(&ts, nullptr);
-        }
+        });
+        if (expired && !done) return false;
     }
     return true;
 }
@@ -342,7 +363,7 @@ kv_status kv_ring_close(kv_ring r) {
                    "within 2 s: the ring stays open; close it again once that stream's work "
                    "has finished");
     }
-    for (auto &x : o->stores) cudaEventDestroy(x.ev);
+    for (auto &x : o->stores) on_device(x.device, [&] { cudaEventDestroy(x.ev); });
     o->stores.clear();
     kv_status s = KV_OK;
     if (o->srv_fence != 0 && kv_fence_query(o->srv_fence) == KV_ERR_TIMEOUT) {
