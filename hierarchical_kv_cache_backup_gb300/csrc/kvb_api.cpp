@@ -824,6 +824,7 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
     // (310 vs 325 GB/s for 4,096 x 1 MiB both ways), and one op gains nothing
     // from overlapping its own slices' launches.
     const uint32_t pdl0 = p.d.pdl;
+    unsigned long long *const ext_word = p.d.ext_word;   // the last slice's, with the fence
     for (uint32_t i0 = 0; i0 < n; i0 += p.max_items) {
         const uint32_t m = std::min(p.max_items, n - i0);
         const bool last = i0 + m >= n;
@@ -832,9 +833,11 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
             p.d.fence_word = ds->words_dev + fence->k;
             p.d.fence_seq = fence->seq;
             p.d.fence_count = ds->counters + fence->k;
+            p.d.ext_word = ext_word;
         } else {
             p.d.fence_word = nullptr;
             p.d.fence_count = nullptr;
+            p.d.ext_word = nullptr;
         }
         std::memcpy(ids.a, a + i0, m * sizeof(int32_t));
         if (b_is_index)
@@ -860,6 +863,7 @@ kv_status run_moves(Plan &p, const int32_t *a, const int32_t *b, uint32_t n, int
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
     p.d.pdl = pdl0;
+    p.d.ext_word = ext_word;
     return KV_OK;
 }
 
@@ -1080,10 +1084,15 @@ kv_status ce_copies(const PoolObj &pool, const HostObj &host, bool backup, const
 // `ready` (device-visible, or NULL): BACKUP's ready_fence -- the move starts
 // only once *ready >= ready_value, waited for on the GPU for at most
 // ready_timeout_ns; on time-out nothing moves and the fence reports ABORTED.
+// `ext_word` (device-visible, or NULL): a second completion word the move
+// kernel stores `ext_value` to right after the fence; *ext_fused says whether
+// it could (a zero-copy op with pages to move).
 kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, const int32_t *b,
                 uint32_t n, int32_t layer, void *stream_v, kv_fence *fence,
                 const unsigned long long *ready = nullptr, uint64_t ready_value = 0,
-                uint64_t ready_timeout_ns = 0) {
+                uint64_t ready_timeout_ns = 0, unsigned long long *ext_word = nullptr,
+                uint64_t ext_value = 0, int *ext_fused = nullptr) {
+    if (ext_fused != nullptr) *ext_fused = 0;
     if (fence == nullptr) return fail(KV_ERR_INVALID_ARG, "fence output pointer is NULL");
     if (pool_h == nullptr || host_h == nullptr)
         return fail(KV_ERR_INVALID_ARG, "pool or host handle is NULL");
@@ -1188,6 +1197,8 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
                 overlapped = true;
             }
         }
+        p.d.ext_word = ext_word;
+        p.d.ext_value = ext_value;
         int ctas = default_ctas(ds, true, PK_REG, p.threads);
         if (overlap_cfg && restore_kind && g_cfg.max_ctas == 0)
             ctas = p.threads == kWideThreads ? std::min(kOverlapRestoreCtas, ds.sms)
@@ -1315,6 +1326,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     }
     st = commit_fence(d, fs, !fused, stream, fence);
     if (st != KV_OK) return bail(st);
+    if (ext_fused != nullptr) *ext_fused = fused && ext_word != nullptr ? 1 : 0;
     if (overlapped) g_overlapped.fetch_add(1, std::memory_order_relaxed);
     if (overlap_cfg && restore_kind && fused) {
         // an op that did not overlap waited for all before it: it starts a new run
@@ -1408,6 +1420,15 @@ kv_status issue_device(kv_pool pool_h, void *buf, uint64_t buf_bytes, uint32_t b
 namespace kvb {
 
 int set_last_error(int status, const char *msg) { return fail((kv_status)status, "%s", msg); }
+
+int ring_issue(const void *pool_handle, const void *host_handle, int kind, const int32_t *a,
+               const int32_t *b, uint32_t n, int32_t layer, void *stream,
+               unsigned long long *done_word, unsigned long long ticket, uint64_t *fence,
+               int *fused) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return issue((kv_pool)pool_handle, (kv_host)host_handle, kind, a, b, n, layer, stream,
+                 (kv_fence *)fence, nullptr, 0, 0, done_word, ticket, fused);
+}
 
 int pool_device_of(const void *pool_handle, int *device) {
     std::lock_guard<std::mutex> lk(g_mu);

@@ -114,6 +114,10 @@ struct MoveDesc {
     // parameter block, for one move kernel over more items than a parameter
     // block holds (progressive restores of more than kMaxItems pages).
     const int32_t *gid_a, *gid_b;
+    // A second completion word (a ring descriptor's completion record): the
+    // CTA that publishes the fence then stores ext_value to ext_word too.
+    unsigned long long *ext_word;
+    unsigned long long ext_value;
 };
 
 // Ids of one launch, inside the kernel's parameter block.  Launches use the
@@ -159,6 +163,15 @@ int pool_device_of(const void *pool_handle, int *device);
 // `staging_bytes` and enqueues it on `stream`: the gather kernel (pool ->
 // staging, host layout) and copy-engine copies (staging -> host tier).  Uses
 // no heap, no CUDA allocation and no library fence; returns a kv_status.
+// Issues a ring descriptor's backup (kind 0) or restore (kind 1) like
+// kv_backup / kv_restore, and asks for `done_word` (device view of the ticket's
+// completion record) to be set to `ticket` by the move kernel itself once the
+// bytes are in place.  *fused = 1 when that was possible (a zero-copy op with
+// pages to move); otherwise the caller completes the ticket itself.
+int ring_issue(const void *pool_handle, const void *host_handle, int kind, const int32_t *a,
+               const int32_t *b, uint32_t n, int32_t layer, void *stream,
+               unsigned long long *done_word, unsigned long long ticket, uint64_t *fence,
+               int *fused);
 int enqueue_staged_backup_noalloc(const void *pool_handle, const void *host_handle,
                                   const int32_t *src_pages, const int32_t *host_slots, uint32_t n,
                                   void *staging, uint64_t staging_bytes, cudaStream_t stream);

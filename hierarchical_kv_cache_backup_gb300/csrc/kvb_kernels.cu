@@ -118,7 +118,8 @@ __device__ __forceinline__ void chain_wait(const MoveDesc &d) {
 // stores visible system-wide, the CTA counts itself done, and the CTA that
 // finishes last publishes the sequence number for the host (and resets the
 // counter for the fence slot's next use); an overlapped restore first waits
-// for its predecessor's fence (chain_wait).
+// for its predecessor's fence (chain_wait).  A ring descriptor's completion
+// record (ext_word), when given, is stored right after the fence.
 __device__ __forceinline__ void complete_grid(const MoveDesc &d) {
     __threadfence_system();
     __syncthreads();
@@ -135,6 +136,10 @@ __device__ __forceinline__ void complete_grid(const MoveDesc &d) {
             asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.fence_word),
                          "l"(d.fence_seq)
                          : "memory");
+            if (d.ext_word != nullptr)
+                asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.ext_word),
+                             "l"(d.ext_value)
+                             : "memory");
         }
     }
 }

@@ -547,17 +547,26 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
                                 op.ready_index;
         const uint64_t ready_ns =
             (uint64_t)(op.ready_timeout_ms ? op.ready_timeout_ms : 10000u) * 1000000ull;
+        CompRec *cd = &o->comp_dev[slot_of(o, t)];
+        // An ungated op's move kernel completes the ticket itself, right after its
+        // fence (no marker kernel between consecutive ops on the stream, so
+        // restores overlapped under KV_CFG_OVERLAP_RESTORES stay overlapped).
+        int fused = 0;
         if (op.kind == KV_RING_OP_BACKUP)
             s = op.layer != -1 ? KV_ERR_INVALID_ARG
                 : gated ? kv_backup_when_ready(pools[op.pool_index], host, op.a, op.b, op.n, ready,
                                                op.ready_value, ready_ns, stream, &f)
-                        : kv_backup(pools[op.pool_index], host, op.a, op.b, op.n, stream, &f);
+                        : (kv_status)kvb::ring_issue(pools[op.pool_index], host, 0, op.a, op.b,
+                                                     op.n, -1, stream,
+                                                     (unsigned long long *)&cd->done, t, &f,
+                                                     &fused);
         else
             s = gated ? kv_restore_when_ready(pools[op.pool_index], host, op.a, op.b, op.n,
                                               op.layer, ready, op.ready_value, ready_ns, stream,
                                               &f)
-                      : kv_restore(pools[op.pool_index], host, op.a, op.b, op.n, op.layer, stream,
-                                   &f);
+                      : (kv_status)kvb::ring_issue(pools[op.pool_index], host, 1, op.a, op.b,
+                                                   op.n, op.layer, stream,
+                                                   (unsigned long long *)&cd->done, t, &f, &fused);
         if (s != KV_OK) {
             complete_cpu(o, t, s);
             continue;
@@ -567,7 +576,6 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
         int prev = -1;
         if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
         if (prev != device) cudaSetDevice(device);
-        CompRec *cd = &o->comp_dev[slot_of(o, t)];
         cudaError_t e = cudaSuccess;
         kv_status fail_st = KV_OK;   // completed from the CPU with this status instead
         if (gated) {   // the ticket reports a gate that gave up (ABORTED)
@@ -580,7 +588,7 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
                 e = kvb::launch_ring_mark((unsigned long long *)&cd->done,
                                           (unsigned long long *)&cd->err_ticket, &cd->err, t,
                                           status, tag, (cudaStream_t)stream);
-        } else {
+        } else if (!fused) {
             e = kvb::launch_mark((unsigned long long *)&cd->done, t, (cudaStream_t)stream);
         }
         if (e != cudaSuccess) {
@@ -590,7 +598,7 @@ kv_status kv_ring_serve(kv_ring r, const kv_pool *pools, uint32_t npools, kv_hos
             std::lock_guard<std::mutex> lk(o->mu);
             fail_st = note_store(o, stream);
             if (fail_st != KV_OK) {
-                // the mark is queued but close could not see it: let it run first
+                // the store is queued but close could not see it: let it run first
                 cudaStreamSynchronize((cudaStream_t)stream);
                 fail_st = KV_OK;
             }
