@@ -1089,10 +1089,16 @@ def mla_ring_layers(ctx, su):
 
 
 def mla_record(ctx):
-    """The MLA fp8 workload as a record of its own (17.2 GiB pool)."""
+    """The MLA fp8 workload as a record of its own (17.2 GiB pool), with the 61
+    one-layer restores also sent as ring descriptors (overlapped restores on)."""
     su = Setup(ctx, wl.MLA_FP8)
     try:
         rec = mla_layerwise(ctx, su)
+        ctx.set_config(overlap=True)
+        ring = mla_ring_layers(ctx, su)
+        ring["config"] = "kv_config.flags = KV_CFG_OVERLAP_RESTORES"
+        rec["ring_one_layer_descriptors"] = ring
+        ctx.set_config()
     finally:
         su.close()
     g, w = wl.MLA_FP8.geom, wl.MLA_FP8
@@ -1624,6 +1630,8 @@ def records_summary(line):
             "progressive_gbs": m["progressive_call"]["gbs"],
             "progressive_frac": m["progressive_call"]["roofline"]["frac"],
             "exposed_ms_beside_gemms": m["overlap_with_compute"]["exposed_transfer_ms"],
+            "ring_host_served_gbs": m.get("ring_one_layer_descriptors", {}).get(
+                "host_served_gbs"),
             "cpu_gbs": m.get("cpu_baseline", {}).get("value")}
     t = line.get("trtllm_ipc")
     if t:
