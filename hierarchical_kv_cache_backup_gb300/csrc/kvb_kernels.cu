@@ -28,8 +28,11 @@
 //                   order by 256 threads.
 //   kv_gate_kernel  bounded wait for a ready fence before a gated backup.
 //   kv_mark_kernel  stores a fence word after copy-engine work.
-// The move kernels complete their op's fence from their last CTA; all waits
-// inside kernels are bounded and nothing traps.
+// The move kernels complete their op's fence from their last CTA (and, for a
+// ring descriptor, its completion record right after); an overlapped restore
+// (KV_CFG_OVERLAP_RESTORES) skips griddepcontrol.wait and publishes its fence
+// only after its predecessor's.  All waits inside kernels are bounded and
+// nothing traps.
 #include "kvb_internal.h"
 
 namespace kvb {
