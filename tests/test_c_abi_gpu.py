@@ -1,8 +1,9 @@
 """The C ABI end to end from a C program on the GPU: the program allocates
 with the CUDA runtime, registers a page-first HND pool at a byte offset and a
-mapped pinned NHD host tier, backs pages up and restores one layer into other
-pages through kvb.h, and compares every byte of the host tier and of the pool
-allocation with the oracle's C functions (linked into the test program only;
+mapped pinned NHD host tier, backs pages up, restores one layer into other
+pages and then every layer one per call with overlapped restores through
+kvb.h, and compares every byte of the host tier and of the pool allocation
+with the oracle's C functions (linked into the test program only;
 the library never links the oracle)."""
 import os
 import shutil
@@ -80,6 +81,31 @@ int main(void) {
     kvo_restore(&g, img, (int64_t)off, want_host, slots, dst, n, 2);
     CK(cudaMemcpy(got, alloc_d, off + pool_bytes, cudaMemcpyDeviceToHost));
     if (memcmp(got, img, off + pool_bytes) != 0) { printf("pool differs\n"); return 6; }
+
+    /* every layer restored one per call on a created stream, overlapped */
+    {
+        kv_config cfg;
+        cudaStream_t st;
+        int32_t dst2[8] = {20, 21, 22, 23, 24, 25, 26, 27};
+        kv_fence fl[4];
+        uint64_t c0 = kv_overlap_count();
+        KV(kv_config_get(&cfg));
+        cfg.flags |= KV_CFG_OVERLAP_RESTORES;
+        KV(kv_config_set(&cfg));
+        CK(cudaStreamCreate(&st));
+        for (uint32_t l = 0; l < L; ++l) KV(kv_restore(pool, tier, slots, dst2, n, (int32_t)l, st, &fl[l]));
+        if (kv_overlap_count() - c0 != L - 1) { printf("overlap count %llu\n", (unsigned long long)(kv_overlap_count() - c0)); return 7; }
+        KV(kv_fence_wait(fl[L - 1], 20000000000ull));
+        for (uint32_t l = 0; l < L; ++l) {
+            KV(kv_fence_query(fl[l]));
+            kvo_restore(&g, img, (int64_t)off, want_host, slots, dst2, n, (int32_t)l);
+        }
+        CK(cudaMemcpy(got, alloc_d, off + pool_bytes, cudaMemcpyDeviceToHost));
+        if (memcmp(got, img, off + pool_bytes) != 0) { printf("pool differs (overlapped)\n"); return 8; }
+        cfg.flags &= ~KV_CFG_OVERLAP_RESTORES;
+        KV(kv_config_set(&cfg));
+        CK(cudaStreamDestroy(st));
+    }
 
     KV(kv_pool_close(pool));
     KV(kv_host_close(tier));
