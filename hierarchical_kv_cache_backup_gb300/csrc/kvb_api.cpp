@@ -221,17 +221,20 @@ struct DevState {
     cudaEvent_t gids_copied = nullptr;       // the pinned -> device copy is done
     cudaEvent_t gids_free = nullptr;         // the kernel reading the device ids is done
     bool gids_used = false;
-    // KV_CFG_OVERLAP_RESTORES: per stream, the run of zero-copy restores of one
-    // pool issued there since the last op that waited for its predecessor; any
-    // other op of this library on the stream erases it.  Each overlapped kernel
-    // may start while its predecessors still run (each lets the next launch
-    // early), so a new restore may overlap only if it writes nothing that any
-    // restore of the run whose fence is not yet complete writes.
+    // KV_CFG_OVERLAP_RESTORES / _BACKUPS: per stream, the run of zero-copy
+    // restores and backups of one pool issued there since the last op that
+    // waited for its predecessor; any other op of this library on the stream
+    // erases it.  Each overlapped kernel may start while its predecessors still
+    // run (each lets the next launch early), so a new op may overlap only if no
+    // byte it touches is written by an op of the run whose fence is not yet
+    // complete, and it writes no byte such an op reads (ops_conflict).
     struct ChainOp {
         int k;                      // fence slot and sequence number
         uint64_t seq;
+        int kind;                   // 0 backup (reads pages, writes slots), 1 restore
         int32_t layer;              // -1 = every layer
-        std::vector<int32_t> dst;   // pages it writes, sorted
+        std::vector<int32_t> pages; // pool pages it reads (backup) or writes (restore), sorted
+        std::vector<int32_t> slots; // host slots it writes (backup) or reads (restore), sorted
     };
     struct Chain {
         uint64_t pool;              // pool handle id
@@ -250,7 +253,7 @@ uint64_t g_next_seq = 1;
 DevState g_dev[kMaxDevices];
 kv_config g_cfg = {KV_MODE_ZERO_COPY, 0, 0, 0, 0};
 std::atomic<uint64_t> g_launches{0};
-std::atomic<uint64_t> g_overlapped{0};   // restores issued overlapped
+std::atomic<uint64_t> g_overlapped{0};   // ops issued overlapped
 
 constexpr uint64_t kDefaultStaging = 256ull << 20;
 constexpr uint64_t kMaxReadyTimeoutNs = 60ull * 1000 * 1000 * 1000;   // gate waits at most 60 s
@@ -561,7 +564,7 @@ kv_status check_op(const Geo &g, uint64_t num_slots, int kind, const int32_t *a,
     return check_ids("dst_pages", b, n, g.P, true);
 }
 
-// -------------------------------------------------- overlapped restores
+// ------------------------------------------------------ overlapped ops
 
 // Any library work on `stream` other than a zero-copy restore ends the run of
 // restores there that a later one may overlap.  That work waits for the
@@ -581,29 +584,44 @@ bool sorted_disjoint(const std::vector<int32_t> &x, const std::vector<int32_t> &
     return true;
 }
 
-constexpr size_t kMaxChain = 256;   // restores of one run checked against a new one
+constexpr size_t kMaxChain = 256;   // ops of one run checked against a new one
 
-// Whether a restore of (pool, layer, sorted pages) on `stream` may overlap the
-// run there; sets *pred to the run's last op (the fence it chains on).  Drops
-// restores of the run whose fence the host already sees complete: their bytes
-// are in place.
-bool may_overlap(DevState &ds, void *stream, uint64_t pool, int32_t layer,
-                 const std::vector<int32_t> &pages, const DevState::ChainOp **pred) {
+// Whether ops x and y touch a common byte that one of them writes.  A backup
+// reads the pool pages and writes the host slots it names (every layer); a
+// restore reads the slots and writes the pages (one layer, or every layer).
+// Two one-layer ops on different layers touch no common byte.
+bool ops_conflict(const DevState::ChainOp &x, const DevState::ChainOp &y) {
+    if (x.layer >= 0 && y.layer >= 0 && x.layer != y.layer) return false;
+    const bool pool_written = x.kind == 1 || y.kind == 1;    // restores write the pool
+    const bool host_written = x.kind == 0 || y.kind == 0;    // backups write the host tier
+    if (pool_written && !sorted_disjoint(x.pages, y.pages)) return true;
+    if (host_written && !sorted_disjoint(x.slots, y.slots)) return true;
+    return false;
+}
+
+// Whether op `y` of `pool` on `stream` may overlap the run there; sets *pred to
+// the run's last op (the fence it chains on).  Drops ops of the run whose fence
+// the host already sees complete: their bytes are in place.
+bool may_overlap(DevState &ds, void *stream, uint64_t pool, const DevState::ChainOp &y,
+                 const DevState::ChainOp **pred) {
     auto it = ds.chains.find(stream);
     if (it == ds.chains.end() || it->second.pool != pool || it->second.ops.empty()) return false;
     std::vector<DevState::ChainOp> &ops = it->second.ops;
     size_t keep = 0;
+    bool last_done = false;   // the last op stays as the chain's anchor even when done
     for (size_t i = 0; i < ops.size(); ++i) {
         const bool last = i + 1 == ops.size();
-        if (!last && load_acquire(&ds.words[ops[i].k]) >= ops[i].seq) continue;
+        const bool done = load_acquire(&ds.words[ops[i].k]) >= ops[i].seq;
+        if (done && !last) continue;
+        if (last) last_done = done;
         if (keep != i) ops[keep] = std::move(ops[i]);
         ++keep;
     }
     ops.resize(keep);
     if (ops.size() >= kMaxChain) return false;
-    for (const DevState::ChainOp &o : ops) {
-        const bool other_layer = layer >= 0 && o.layer >= 0 && layer != o.layer;
-        if (!other_layer && !sorted_disjoint(o.dst, pages)) return false;
+    for (size_t i = 0; i < ops.size(); ++i) {
+        if (i + 1 == ops.size() && last_done) break;   // its bytes are in place
+        if (ops_conflict(ops[i], y)) return false;
     }
     *pred = &ops.back();
     return true;
@@ -1140,28 +1158,36 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     };
     bool fused = false;
 
-    // Overlapped restores (KV_CFG_OVERLAP_RESTORES): a zero-copy restore may
-    // start moving while the previous kernel on its stream still runs when that
-    // kernel is the last restore this library issued there, of the same pool,
-    // and the two write disjoint bytes (other layers, or no page in common).
-    // Restores only read the host tier, so nothing else can conflict.
-    const bool overlap_cfg = (g_cfg.flags & KV_CFG_OVERLAP_RESTORES) != 0 &&
+    // Overlapped ops (KV_CFG_OVERLAP_RESTORES, KV_CFG_OVERLAP_BACKUPS): a
+    // zero-copy op may start moving while the previous kernel on its stream
+    // still runs when that kernel is the last op this library issued there, of
+    // the same pool, and the new op conflicts with no unfinished op of the run
+    // (ops_conflict: no common byte that one of them writes).
+    const uint32_t kind_flag = backup ? KV_CFG_OVERLAP_BACKUPS : KV_CFG_OVERLAP_RESTORES;
+    const bool overlap_cfg = (g_cfg.flags & kind_flag) != 0 &&
                              (g_cfg.flags & KV_CFG_NO_PDL) == 0;
     // Not on the legacy default stream nor the special handles (0, 1, 2): the
     // legacy stream also waits on every blocking stream, so work the library
-    // cannot see may sit between two of its restores there.
+    // cannot see may sit between two of its ops there.
     const bool plain_stream = (uintptr_t)stream_v > 2u;
-    const bool restore_kind = !backup && ready == nullptr && n > 0 &&
-                              g_cfg.mode == KV_MODE_ZERO_COPY && plain_stream;
+    const bool run_kind = ready == nullptr && n > 0 && g_cfg.mode == KV_MODE_ZERO_COPY &&
+                          plain_stream;   // an op that may take part in a run
     bool chain = false, overlapped = false;
     int chain_k = 0;
     uint64_t chain_seq = 0;
-    static thread_local std::vector<int32_t> sorted_dst;
-    if (overlap_cfg && restore_kind) {
-        sorted_dst.assign(b, b + n);
-        std::sort(sorted_dst.begin(), sorted_dst.end());
+    static thread_local DevState::ChainOp me;
+    if (overlap_cfg && run_kind) {
+        const int32_t *pages = backup ? a : b, *slots = backup ? b : a;
+        me.kind = backup ? 0 : 1;
+        me.layer = layer;
+        me.pages.assign(pages, pages + n);
+        me.slots.assign(slots, slots + n);
+        std::sort(me.pages.begin(), me.pages.end());
+        std::sort(me.slots.begin(), me.slots.end());
+        // a backup's source pages may repeat (duplicate sources are allowed)
+        me.pages.erase(std::unique(me.pages.begin(), me.pages.end()), me.pages.end());
         const DevState::ChainOp *pred = nullptr;
-        if (may_overlap(ds, stream_v, handle_id(pool_h), layer, sorted_dst, &pred)) {
+        if (may_overlap(ds, stream_v, handle_id(pool_h), me, &pred)) {
             chain = true;
             chain_k = pred->k;
             chain_seq = pred->seq;
@@ -1185,9 +1211,9 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
             p.d.skip_tag = fs.seq;
         }
         p.threads = link_threads(p.d.transpose != 0);
-        if (overlap_cfg && restore_kind && g_cfg.cta_threads == 0) p.threads = kWideThreads;
+        if (overlap_cfg && run_kind && g_cfg.cta_threads == 0) p.threads = kWideThreads;
         p.d.pdl = (g_cfg.flags & KV_CFG_NO_PDL) ? 0u : 1u;
-        if (overlap_cfg && restore_kind) {
+        if (overlap_cfg && run_kind) {
             p.d.early_trigger = 1u;
             // one launch only: the op's fence and its overlap sit in the same kernel
             if (chain && n <= p.max_items) {
@@ -1200,7 +1226,7 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
         p.d.ext_word = ext_word;
         p.d.ext_value = ext_value;
         int ctas = default_ctas(ds, true, PK_REG, p.threads);
-        if (overlap_cfg && restore_kind && g_cfg.max_ctas == 0)
+        if (overlap_cfg && run_kind && g_cfg.max_ctas == 0)
             ctas = p.threads == kWideThreads ? std::min(kOverlapRestoreCtas, ds.sms)
                                              : std::min(4 * kOverlapRestoreCtas, 4 * ds.sms);
         st = run_moves(p, a, b, n, ctas, stream, false, &ds, &fs);
@@ -1328,11 +1354,13 @@ kv_status issue(kv_pool pool_h, kv_host host_h, int kind, const int32_t *a, cons
     if (st != KV_OK) return bail(st);
     if (ext_fused != nullptr) *ext_fused = fused && ext_word != nullptr ? 1 : 0;
     if (overlapped) g_overlapped.fetch_add(1, std::memory_order_relaxed);
-    if (overlap_cfg && restore_kind && fused) {
+    if (overlap_cfg && run_kind && fused) {
         // an op that did not overlap waited for all before it: it starts a new run
         if (!overlapped) run.ops.clear();
         run.pool = handle_id(pool_h);
-        run.ops.push_back(DevState::ChainOp{fs.k, fs.seq, layer, sorted_dst});
+        me.k = fs.k;
+        me.seq = fs.seq;
+        run.ops.push_back(me);
         if (ds.chains.size() >= 4096) ds.chains.clear();   // streams come and go
         ds.chains[stream_v] = std::move(run);
     }
@@ -1638,7 +1666,8 @@ kv_status kv_config_set(const kv_config *cfg) {
     if (cfg->max_ctas > 65535) return fail(KV_ERR_INVALID_ARG, "max_ctas %u > 65535", cfg->max_ctas);
     if (cfg->staging_bytes != 0 && (cfg->staging_bytes < (2ull << 20) || cfg->staging_bytes % 512))
         return fail(KV_ERR_INVALID_ARG, "staging_bytes must be 0 or a multiple of 512 >= 2 MiB");
-    if ((cfg->flags & ~(uint32_t)(KV_CFG_NO_BULK | KV_CFG_NO_PDL | KV_CFG_OVERLAP_RESTORES)) != 0)
+    if ((cfg->flags & ~(uint32_t)(KV_CFG_NO_BULK | KV_CFG_NO_PDL | KV_CFG_OVERLAP_RESTORES |
+                                  KV_CFG_OVERLAP_BACKUPS)) != 0)
         return fail(KV_ERR_INVALID_ARG, "unknown config flags %#x", cfg->flags);
     if (cfg->cta_threads != 0 && cfg->cta_threads != (uint32_t)kMoveThreads &&
         cfg->cta_threads != (uint32_t)kWideThreads)

@@ -41,6 +41,7 @@ KV_MODE_ZERO_COPY, KV_MODE_STAGED, KV_MODE_COPY_ENGINE = 0, 1, 2
 KV_CFG_NO_BULK = 1
 KV_CFG_NO_PDL = 2
 KV_CFG_OVERLAP_RESTORES = 4
+KV_CFG_OVERLAP_BACKUPS = 8
 KVB_IPC_MAGIC = 0x4B564231
 KVB_IPC_MAGIC_SPLIT = 0x4B564253
 
@@ -482,7 +483,7 @@ def kv_launch_count() -> int:
 
 
 def kv_overlap_count() -> int:
-    """Restores issued overlapped with the previous one on their stream so far."""
+    """Ops issued overlapped with the previous one on their stream so far."""
     return _lib.kv_overlap_count()
 
 

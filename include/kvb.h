@@ -179,6 +179,17 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
  * this flag such work must not write the host slots or pages the later restore
  * reads or writes, nor read the pages it writes. */
 #define KV_CFG_OVERLAP_RESTORES 4u
+/* KV_CFG_OVERLAP_BACKUPS (opt-in, same mechanism and contract): zero-copy
+ * kv_backup calls take part in a stream's run of overlapped ops too.  A new op
+ * (backup or restore, same pool handle, same stream) may overlap the ops of
+ * the run whose fences are not yet complete when no byte that one of the two
+ * writes is touched by the other: a backup reads its source pages (every
+ * layer) and writes its host slots; a restore reads its host slots and writes
+ * its destination pages (its layer, or every layer).  So consecutive backups
+ * into disjoint slots overlap, and a backup of pages a restore is still
+ * writing does not.  Useful for streams of small ops, whose time is mostly
+ * latency; fences still complete in call order. */
+#define KV_CFG_OVERLAP_BACKUPS 8u
 
 /* Defaults: host-link moves (zero-copy backup / restore) run 16 CTAs of 1024
  * threads when pool and tier share a head order and 64 CTAs of 256 when the
@@ -658,9 +669,9 @@ KVB_API kv_status kv_config_set(const kv_config *cfg);
 KVB_API kv_status kv_layout_page_bytes(const kv_layout *layout, uint64_t *out);
 /* Number of kernels this library has launched in this process. */
 KVB_API uint64_t kv_launch_count(void);
-/* Number of restores this process issued overlapped with the previous one on
- * their stream (KV_CFG_OVERLAP_RESTORES): a way to check that the flag applies
- * to a caller's pattern of calls. */
+/* Number of ops this process issued overlapped with the previous one on their
+ * stream (KV_CFG_OVERLAP_RESTORES / KV_CFG_OVERLAP_BACKUPS): a way to check
+ * that the flags apply to a caller's pattern of calls. */
 KVB_API uint64_t kv_overlap_count(void);
 /* Message of the last failing call on this thread ("" if none). */
 KVB_API const char *kv_last_error(void);

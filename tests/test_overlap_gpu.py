@@ -112,9 +112,9 @@ def test_same_layer_disjoint_pages_overlap_and_shared_pages_do_not(overlap):
             # the third shares pages with the first, not with the second: it may
             # overlap only once the first's fence is complete, and must land after it
             f = kvb.kv_restore(rig.pool, rig.hostt, sl3, shared, layer, s.cuda_stream)
-            c3 = kvb.kv_overlap_count()
-            f4 = kvb.kv_restore(rig.pool, rig.hostt, sl1, shared, layer, s.cuda_stream)  # = 3rd's
-            assert kvb.kv_overlap_count() == c3
+            # the fourth writes the third's pages: it may overlap only once the third
+            # is done (whether it did depends on timing); the bytes must be the oracle's
+            f4 = kvb.kv_restore(rig.pool, rig.hostt, sl1, shared, layer, s.cuda_stream)
             kvb.kv_fence_wait(f4, WAIT)
             assert kvb.kv_fence_query(f) == kvb.KV_OK
             for sl, dd in ((sl1, a), (sl2, b), (sl3, shared), (sl1, shared)):
@@ -339,4 +339,85 @@ def test_ring_host_server_with_overlapped_restores(overlap):
         s.synchronize()
         kvb.kv_ring_close(srv)
         kvb.kv_ring_close(sub)
+        rig.close()
+
+
+def test_overlapped_backups_and_their_hazards(overlap):
+    """KV_CFG_OVERLAP_BACKUPS with KV_CFG_OVERLAP_RESTORES: backups into disjoint
+    slots overlap; a backup into a slot an unfinished backup writes, a restore
+    reading a slot an unfinished backup writes, and a backup of a page an
+    unfinished restore writes all wait.  Whole buffers against the oracle in
+    call order, repeated (a wrong overlap would show only as a race)."""
+    overlap(flags=kvb.KV_CFG_OVERLAP_RESTORES | kvb.KV_CFG_OVERLAP_BACKUPS)
+    g = GEOMS["llama8b"]
+    n = 8
+    r = np.random.default_rng(41)
+    rig = Rig(g, 6 * n, seed=42)
+    s = torch.cuda.Stream()
+    og = oracle_geom(g)
+    try:
+        for it in range(10):
+            want = rig.snapshot()
+            want = (want[0].copy(), want[1].copy())
+            pages = wl.distinct_pages(r, g.P, 4 * n)
+            slots = r.permutation(6 * n).astype(np.int32)
+            sa, sb, sc = slots[:n], slots[n:2 * n], slots[2 * n:3 * n]
+            p1, p2, p3 = pages[:n], pages[n:2 * n], pages[2 * n:3 * n]
+            ops = []
+            kvb.kv_backup(rig.pool, rig.hostt, p1, sa, s.cuda_stream)
+            ops.append(("b", p1, sa, -1))
+            c0 = kvb.kv_overlap_count()
+            kvb.kv_backup(rig.pool, rig.hostt, p2, sb, s.cuda_stream)      # disjoint slots
+            ops.append(("b", p2, sb, -1))
+            assert kvb.kv_overlap_count() - c0 == 1
+            # the next three each conflict with their unfinished predecessor and wait
+            # for it (or overlap once it is done: timing); the bytes must be the oracle's
+            shared = np.concatenate([sb[:n // 2], sc[:n - n // 2]])        # meets the 2nd
+            kvb.kv_backup(rig.pool, rig.hostt, p3, shared, s.cuda_stream)  # WAW on slots
+            ops.append(("b", p3, shared, -1))
+            kvb.kv_restore(rig.pool, rig.hostt, shared, p1, 2, s.cuda_stream)  # RAW on slots
+            ops.append(("r", p1, shared, 2))
+            kvb.kv_backup(rig.pool, rig.hostt, p1, sa, s.cuda_stream)      # reads pages the
+            ops.append(("b", p1, sa, -1))                                   # restore writes
+            f = kvb.kv_restore(rig.pool, rig.hostt, sc, p2, 5, s.cuda_stream)
+            ops.append(("r", p2, sc, 5))
+            kvb.kv_fence_wait(f, WAIT)
+            for kind, pg, sl, layer in ops:
+                if kind == "b":
+                    oracle.backup(og, want[0], want[1], pg, sl)
+                else:
+                    oracle.restore(og, want[0], want[1], sl, pg, layer=layer)
+            rig.assert_equal(want)
+    finally:
+        rig.close()
+
+
+def test_many_small_overlapped_backups(overlap):
+    """A stream of 400 small backups (8 pages each) into two alternating slot
+    sets, and restores out of them: the tier and pool equal the oracle's and
+    consecutive disjoint ops overlapped."""
+    overlap(flags=kvb.KV_CFG_OVERLAP_RESTORES | kvb.KV_CFG_OVERLAP_BACKUPS)
+    g = wl.TINY.geom.with_(P=64)
+    r = np.random.default_rng(43)
+    rig = Rig(g, 16, seed=44)
+    s = torch.cuda.Stream()
+    og = oracle_geom(g)
+    try:
+        want = rig.snapshot()
+        want = (want[0].copy(), want[1].copy())
+        c0 = kvb.kv_overlap_count()
+        f = None
+        for i in range(400):
+            sl = np.arange(8 * (i % 2), 8 * (i % 2) + 8, dtype=np.int32)
+            pg = r.permutation(g.P)[:8].astype(np.int32)
+            if i % 5 == 4:
+                f = kvb.kv_restore(rig.pool, rig.hostt, sl, pg, -1, s.cuda_stream)
+                oracle.restore(og, want[0], want[1], sl, pg)
+            else:
+                f = kvb.kv_backup(rig.pool, rig.hostt, pg, sl, s.cuda_stream)
+                oracle.backup(og, want[0], want[1], pg, sl)
+        kvb.kv_fence_wait(f, WAIT)
+        assert kvb.kv_overlap_count() - c0 > 100
+        rig.assert_equal(want)
+    finally:
         rig.close()

@@ -103,8 +103,9 @@ def test_overlapped_restores_from_four_threads_match_the_oracle():
     drawn from a small page range (so consecutive restores often share a page
     and layer, and must not overlap, and often do not, and may), mixed with
     whole-prefix restores, backups of pages just restored and progressive
-    restores, while the process-wide config flips KV_CFG_OVERLAP_RESTORES on and
-    off and the mode between zero-copy, STAGED and COPY_ENGINE.  The oracle
+    restores, while the process-wide config flips KV_CFG_OVERLAP_RESTORES and
+    KV_CFG_OVERLAP_BACKUPS on and off and the mode between zero-copy, STAGED and
+    COPY_ENGINE.  The oracle
     replays each thread's ops in order; the whole allocation and tier match."""
     P_T, S_T = 400, 400
     g = wl.Geometry(L=4, C=2, P=THREADS * P_T, T=16, H=4, B=64)
@@ -112,6 +113,7 @@ def test_overlapped_restores_from_four_threads_match_the_oracle():
     old = kvb.kv_config_get()
     r = np.random.default_rng(93)
     OV = kvb.KV_CFG_OVERLAP_RESTORES
+    OB = kvb.KV_CFG_OVERLAP_BACKUPS
 
     def plan(t):
         ops = []
@@ -123,7 +125,7 @@ def test_overlapped_restores_from_four_threads_match_the_oracle():
             slots = (t * S_T + r.permutation(S_T)[:n]).astype(np.int32)
             mode = [kvb.KV_MODE_ZERO_COPY] * 4 + [kvb.KV_MODE_STAGED, kvb.KV_MODE_COPY_ENGINE]
             ops.append((kind, pages, slots, int(r.integers(g.L)), int(r.choice(mode)),
-                        int(r.choice([OV, OV, OV, 0]))))
+                        int(r.choice([OV | OB, OV | OB, OV, OB, 0]))))
         return ops
 
     plans = [plan(t) for t in range(THREADS)]
