@@ -1525,6 +1525,19 @@ def small_ops(ctx, su):
         lat, rate = ring_loop(ctx, kind, f"/kvbbench_{os.getpid()}_{kind}", [tpool], ttier,
                               iters, 2_000_000_000, body)
         ring_lat[f"{kind}_served_descriptors_per_s"] = rate
+        if kind == "host":
+            # the same stream of descriptors with overlapped backups and restores
+            old = kvb.kv_config_get()
+            kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes,
+                              old.flags | kvb.KV_CFG_OVERLAP_RESTORES |
+                              kvb.KV_CFG_OVERLAP_BACKUPS, old.cta_threads)
+            try:
+                _, rate_ov = ring_loop(ctx, kind, f"/kvbbenchov_{os.getpid()}", [tpool], ttier,
+                                       iters, 2_000_000_000, body)
+            finally:
+                kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags,
+                                  old.cta_threads)
+            ring_lat["host_served_overlapped_descriptors_per_s"] = rate_ov
         ring_lat[f"{kind}_served_us_median"] = round(1e6 * statistics.median(lat), 1)
         ring_lat[f"{kind}_served_us_p99"] = round(1e6 * sorted(lat)[int(0.99 * len(lat))], 1)
     ring_lat["workload"] = ("tiny: 8 pages x 16 KiB (128 KiB) backup per descriptor, submit "
