@@ -122,12 +122,19 @@ def test_config_roundtrip_and_checks():
         assert (c.mode, c.max_ctas, c.staging_bytes) == (1, 64, 64 << 20)
         kvb.kv_config_set(kvb.KV_MODE_COPY_ENGINE)
         assert kvb.kv_config_get().mode == 2
-        for bad in [dict(mode=3), dict(mode=5), dict(max_ctas=1 << 20), dict(staging_bytes=1000)]:
+        for bad in [dict(mode=3), dict(mode=5), dict(max_ctas=1 << 20), dict(staging_bytes=1000),
+                    dict(flags=16), dict(flags=kvb.KV_CFG_OVERLAP_RESTORES | 32),
+                    dict(cta_threads=512)]:
             with pytest.raises(kvb.KvError) as e:
                 kvb.kv_config_set(**bad)
             assert e.value.status == kvb.KV_ERR_INVALID_ARG
+        every = (kvb.KV_CFG_NO_BULK | kvb.KV_CFG_NO_PDL | kvb.KV_CFG_OVERLAP_RESTORES |
+                 kvb.KV_CFG_OVERLAP_BACKUPS)
+        kvb.kv_config_set(kvb.KV_MODE_ZERO_COPY, 6, 0, every, 1024)
+        c = kvb.kv_config_get()
+        assert (c.mode, c.max_ctas, c.flags, c.cta_threads) == (0, 6, every, 1024)
     finally:
-        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes)
+        kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
 
 
 def test_handles_and_fences_without_gpu():
