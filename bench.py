@@ -577,6 +577,7 @@ class Setup:
             self.exporter = mpc.Process(target=_exporter, args=(q, self.done_ev, ctx.local,
                                                                 w.seed + 100 * rank,
                                                                 w.pool_offset))
+            self.exporter.daemon = True   # never outlives the benchmark, whatever happens
             self.exporter.start()
             self.pool = kvb.kv_pool_import(kvb.desc_from_bytes(q.get(timeout=900)))
             self.alloc = None
@@ -610,6 +611,9 @@ class Setup:
         if self.exporter is not None:
             self.done_ev.set()
             self.exporter.join(120)
+            if self.exporter.is_alive():
+                self.exporter.terminate()
+                self.exporter.join(10)
         self.alloc = self.host = None
         self.ctx.torch.cuda.empty_cache()
 
