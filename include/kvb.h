@@ -158,26 +158,27 @@ typedef enum { KV_MODE_ZERO_COPY = 0, KV_MODE_STAGED = 1, KV_MODE_COPY_ENGINE = 
 /* KV_CFG_OVERLAP_RESTORES (opt-in; needs programmatic dependent launch, so it
  * has no effect together with KV_CFG_NO_PDL).  A zero-copy kv_restore may start
  * moving bytes while the previous kernel on its stream is still finishing,
- * instead of after it, when the library can prove the two independent: that
- * kernel is the last kv_restore issued on the same stream (a created stream:
- * never the legacy default stream, cudaStreamLegacy or cudaStreamPerThread)
- * through this library, of the same pool handle, with no other call of this
- * library on that stream in between, and the two write disjoint bytes -- different layers
- * (both one-layer restores), or no destination page in common.  A restore
- * only reads the host tier, so nothing else of the two can conflict.  This is
- * the layer-by-layer restore of the PP prefetch PR (§PP Prefetch Ticket Path,
- * "Layer-wise H2D + forward"): consecutive one-layer restores keep the host
- * link busy across the boundary between calls instead of draining it.  The
- * overlapping restore must fit one launch (n <= 2,048 pages).  Fences still
- * complete in call order: the later restore publishes its fence only after the
- * earlier one's (a wait on the GPU, bounded at 2 s; if it ever gave up, every
- * later fence query reports KV_ERR_TIMEOUT).  Under this flag zero-copy
- * restores run, unless max_ctas / cta_threads say otherwise, on 6 CTAs of
- * 1,024 threads (6 whole SMs): overlapped, that reaches ~99% of the H2D link
- * and leaves the rest of the GPU to the forward pass.  Contract: the library cannot see
- * work that the caller itself puts on the stream between two restores; under
- * this flag such work must not write the host slots or pages the later restore
- * reads or writes, nor read the pages it writes. */
+ * instead of after it, when the library can prove them independent.  Per
+ * stream (a created stream: never the legacy default stream, cudaStreamLegacy
+ * or cudaStreamPerThread) it keeps the run of restores of one pool handle
+ * issued there since the last call that waited for its predecessor; any other
+ * call of this library on that stream ends the run.  A new restore of the same
+ * pool overlaps when it writes no byte that a restore of the run whose fence is
+ * not yet complete writes: another layer (both one-layer restores), or no
+ * destination page in common.  Restores only read the host tier, so nothing
+ * else can conflict.  This is the layer-by-layer restore of the PP prefetch PR
+ * (§PP Prefetch Ticket Path, "Layer-wise H2D + forward"): consecutive one-layer
+ * restores keep the host link busy across the boundary between calls instead
+ * of draining it.  The overlapping restore must fit one launch (n <= 2,048
+ * pages).  Fences still complete in call order: a restore publishes its fence
+ * only after its predecessor's (a wait on the GPU, bounded at 2 s; if it ever
+ * gave up, every later fence query reports KV_ERR_TIMEOUT).  Under this flag
+ * zero-copy restores run, unless max_ctas / cta_threads say otherwise, on 6
+ * CTAs of 1,024 threads (6 whole SMs): overlapped, that reaches ~99% of the H2D
+ * link and leaves the rest of the GPU to the forward pass.  Contract: the
+ * library cannot see work that the caller itself puts on the stream between
+ * two of its calls; under this flag such work must not write the host slots or
+ * pages a later restore reads or writes, nor read the pages it writes. */
 #define KV_CFG_OVERLAP_RESTORES 4u
 /* KV_CFG_OVERLAP_BACKUPS (opt-in, same mechanism and contract): zero-copy
  * kv_backup calls take part in a stream's run of overlapped ops too.  A new op
