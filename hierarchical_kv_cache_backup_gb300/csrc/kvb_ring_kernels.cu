@@ -25,8 +25,9 @@
 // through L2 (ld.global.cg) or with strong loads, never through the
 // non-coherent read-only path.  A descriptor is released with a gpu-scope
 // release after every writer's fence; a CTA arrives at a descriptor's end
-// after a system-scope fence of its stores, so the completion record the last
-// arriver stores (system scope, release) covers every byte of the operation.
+// after a device-scope fence of its stores, with an acq_rel count, so the
+// completion record the last arriver stores (system scope, release: cumulative
+// over what it acquired) covers every byte of the operation.
 #include "kvb_ring_internal.h"
 
 namespace kvb {
@@ -205,10 +206,12 @@ __device__ __forceinline__ void move_share(const RingKDesc &k, const RingPoolK &
 }
 
 // A mover CTA's arrival at the end of released descriptor number `rel`
-// (1-based): its stores are made visible system-wide, then counted; the last
-// of the movers' arrivals stores the ticket into the completion record.
+// (1-based): its stores are ordered device-wide, then counted (acq_rel at
+// device scope); the last of the movers' arrivals stores the ticket into the
+// completion record with a system-scope release, which is cumulative over
+// every mover's bytes, so the process that acquires the record sees them.
 __device__ __forceinline__ void arrive(const RingKDesc &k, uint32_t rel, uint64_t ticket) {
-    __threadfence_system();
+    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t prev;
@@ -216,10 +219,8 @@ __device__ __forceinline__ void arrive(const RingKDesc &k, uint32_t rel, uint64_
                      : "=r"(prev)
                      : "l"(&k.ctl->arrived)
                      : "memory");
-        if (prev + 1 == (gridDim.x - 1) * rel) {
-            __threadfence_system();
+        if (prev + 1 == (gridDim.x - 1) * rel)
             st_release_sys((unsigned long long *)&k.comp[(ticket - 1) % k.slots].done, ticket);
-        }
     }
 }
 
@@ -552,8 +553,7 @@ __global__ void kv_ring_mark_kernel(unsigned long long *done, unsigned long long
                      : "memory");
         st_relaxed_sys64(err_ticket, ticket);
     }
-    __threadfence_system();
-    st_release_sys(done, ticket);
+    st_release_sys(done, ticket);   // release: the error fields are visible first
 }
 
 }  // namespace
