@@ -1,0 +1,122 @@
+"""Fence visibility: once a fence reports an op complete, every byte the op
+wrote is visible to whoever observed the fence -- the host thread that waited
+on (or polled) it, reading the pinned host tier with no CUDA call in between,
+and a copy on another stream ordered after the op only by kv_fence_stream_wait.
+
+The fused completion orders each CTA's stores at device scope and publishes
+the fence with one system-scope release store; the copy-engine modes publish
+it with a marker kernel after their copies.  Every round below rewrites the
+source with a new value, so a byte left over from the previous round, or one
+still in flight when the fence was seen, shows up as a mismatch against the
+oracle (RFC "[HiCache] Out-of-process HiCache data plane", §Device IPC data
+path: the completion handle says the copy has landed)."""
+import time
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import oracle  # noqa: E402
+from gpu_rig import Rig, oracle_geom  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
+from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
+
+ROUNDS = 150
+WAIT_NS = 30_000_000_000
+MODES = {"zero_copy": kvb.KV_MODE_ZERO_COPY, "staged": kvb.KV_MODE_STAGED,
+         "copy_engine": kvb.KV_MODE_COPY_ENGINE}
+# 64 pages of 32 KiB (2 MiB): every CTA of the default grid takes segments
+GEOMS = {
+    "layer_first_nhd": wl.Geometry(L=2, C=2, P=64, T=16, H=4, B=128),
+    "page_first_hnd": wl.Geometry(L=2, C=2, P=64, T=16, H=4, B=128, order=wl.PAGE_FIRST,
+                                  dev_heads=wl.HND),
+}
+
+
+def _mismatch(name, got, want):
+    bad = np.flatnonzero(got != want)
+    return (f"{name}: {bad.size} bytes differ, first at {bad[0]} (got {got[bad[0]]}, "
+            f"want {want[bad[0]]})")
+
+
+@pytest.fixture
+def mode_config():
+    old = kvb.kv_config_get()
+    yield
+    kvb.kv_config_set(old.mode, old.max_ctas, old.staging_bytes, old.flags, old.cta_threads)
+
+
+@pytest.mark.parametrize("geom", sorted(GEOMS))
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_backup_bytes_are_on_the_host_when_its_fence_is(geom, mode, mode_config):
+    g = GEOMS[geom]
+    rig = Rig(g, g.P, pool_offset=4096 + 48, seed=301)
+    try:
+        kvb.kv_config_set(MODES[mode], 0, 1 << 20)
+        alloc0, _ = rig.snapshot()
+        off, nb = rig.offset, g.pool_bytes
+        base = rig.alloc[off:off + nb].clone()
+        base_np = alloc0[off:off + nb].copy()
+        host_view = rig.host.numpy()          # the pinned tier itself, no copy
+        r = np.random.default_rng(302)
+        s = torch.cuda.Stream()
+        og = oracle_geom(g)
+        for k in range(ROUNDS):
+            src = r.permutation(g.P).astype(np.int32)
+            slots = r.permutation(g.P).astype(np.int32)
+            with torch.cuda.stream(s):
+                torch.add(base, k + 1, out=rig.alloc[off:off + nb])   # wraps mod 256
+            f = kvb.kv_backup(rig.pool, rig.hostt, src, slots, s.cuda_stream)
+            if k % 2 == 0:
+                kvb.kv_fence_wait(f, WAIT_NS)
+            else:                              # poll instead of waiting
+                deadline = time.monotonic() + WAIT_NS / 1e9
+                while kvb.kv_fence_query(f) == kvb.KV_ERR_TIMEOUT:
+                    assert time.monotonic() < deadline, f"round {k}: fence never completed"
+                assert kvb.kv_fence_query(f) == kvb.KV_OK
+            got = host_view.copy()             # read right after the fence, nothing synced
+            pool_k = alloc0.copy()
+            pool_k[off:off + nb] = base_np + np.uint8(k + 1)
+            want = np.zeros_like(got)
+            oracle.backup(og, pool_k, want, src, slots, pool_offset=off, threads=4)
+            assert np.array_equal(got, want), f"round {k}: " + _mismatch("host tier", got, want)
+        torch.cuda.synchronize()
+    finally:
+        rig.close()
+
+
+@pytest.mark.parametrize("geom", sorted(GEOMS))
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_restored_pages_are_seen_by_a_stream_that_waits_on_the_fence(geom, mode, mode_config):
+    g = GEOMS[geom]
+    rig = Rig(g, g.P, pool_offset=4096 + 48, seed=311)
+    try:
+        kvb.kv_config_set(MODES[mode], 0, 1 << 20)
+        alloc_np, host0 = rig.snapshot()
+        host_view = rig.host.numpy()
+        out = torch.empty(rig.alloc.numel(), dtype=torch.uint8, pin_memory=True)
+        r = np.random.default_rng(312)
+        s, c = torch.cuda.Stream(), torch.cuda.Stream()
+        og = oracle_geom(g)
+        for k in range(ROUNDS):
+            host_view[:] = host0 + np.uint8(k + 1)    # the host rewrites its tier every round
+            slots = r.permutation(g.P).astype(np.int32)
+            dst = r.permutation(g.P).astype(np.int32)
+            f = kvb.kv_restore(rig.pool, rig.hostt, slots, dst, -1, s.cuda_stream)
+            kvb.kv_fence_stream_wait(f, c.cuda_stream)
+            with torch.cuda.stream(c):
+                out.copy_(rig.alloc, non_blocking=True)   # ordered after the op by the fence only
+            c.synchronize()
+            oracle.restore(og, alloc_np, host_view, slots, dst, pool_offset=rig.offset, threads=4)
+            got = out.numpy()
+            assert np.array_equal(got, alloc_np), f"round {k}: " + _mismatch("pool", got,
+                                                                             alloc_np)
+            s.synchronize()                    # before the host rewrites what the op read
+        torch.cuda.synchronize()
+    finally:
+        rig.close()
