@@ -5,7 +5,7 @@ and a copy on another stream ordered after the op only by kv_fence_stream_wait.
 
 The fused completion orders each CTA's stores at device scope and publishes
 the fence with one system-scope release store; the copy-engine modes publish
-it with a marker kernel after their copies.  Every round below rewrites the
+it with a marker kernel after their copies.  Each of 400 rounds below rewrites the
 source with a new value, so a byte left over from the previous round, or one
 still in flight when the fence was seen, shows up as a mismatch against the
 oracle (RFC "[HiCache] Out-of-process HiCache data plane", §Device IPC data
@@ -26,14 +26,15 @@ from gpu_rig import Rig, oracle_geom  # noqa: E402
 from hierarchical_kv_cache_backup_gb300 import kvb  # noqa: E402
 from hierarchical_kv_cache_backup_gb300 import workloads as wl  # noqa: E402
 
-ROUNDS = 150
+ROUNDS = 400
 WAIT_NS = 30_000_000_000
 MODES = {"zero_copy": kvb.KV_MODE_ZERO_COPY, "staged": kvb.KV_MODE_STAGED,
          "copy_engine": kvb.KV_MODE_COPY_ENGINE}
-# 64 pages of 32 KiB (2 MiB): every CTA of the default grid takes segments
+STAGING = 2 << 20      # the smallest: a 4 MiB STAGED op runs as 8 ping-pong chunks of 512 KiB
+# 128 pages of 32 KiB (4 MiB): every CTA of the default grid takes segments
 GEOMS = {
-    "layer_first_nhd": wl.Geometry(L=2, C=2, P=64, T=16, H=4, B=128),
-    "page_first_hnd": wl.Geometry(L=2, C=2, P=64, T=16, H=4, B=128, order=wl.PAGE_FIRST,
+    "layer_first_nhd": wl.Geometry(L=2, C=2, P=128, T=16, H=4, B=128),
+    "page_first_hnd": wl.Geometry(L=2, C=2, P=128, T=16, H=4, B=128, order=wl.PAGE_FIRST,
                                   dev_heads=wl.HND),
 }
 
@@ -57,7 +58,7 @@ def test_backup_bytes_are_on_the_host_when_its_fence_is(geom, mode, mode_config)
     g = GEOMS[geom]
     rig = Rig(g, g.P, pool_offset=4096 + 48, seed=301)
     try:
-        kvb.kv_config_set(MODES[mode], 0, 1 << 20)
+        kvb.kv_config_set(MODES[mode], 0, STAGING)
         alloc0, _ = rig.snapshot()
         off, nb = rig.offset, g.pool_bytes
         base = rig.alloc[off:off + nb].clone()
@@ -96,7 +97,7 @@ def test_restored_pages_are_seen_by_a_stream_that_waits_on_the_fence(geom, mode,
     g = GEOMS[geom]
     rig = Rig(g, g.P, pool_offset=4096 + 48, seed=311)
     try:
-        kvb.kv_config_set(MODES[mode], 0, 1 << 20)
+        kvb.kv_config_set(MODES[mode], 0, STAGING)
         alloc_np, host0 = rig.snapshot()
         host_view = rig.host.numpy()
         out = torch.empty(rig.alloc.numel(), dtype=torch.uint8, pin_memory=True)
