@@ -117,8 +117,8 @@ __device__ __forceinline__ void chain_wait(const MoveDesc &d) {
     if (d.err != nullptr) *(volatile uint32_t *)d.err = 3u;
 }
 
-// Completion of a grid, fused into its last CTA: every thread orders its own
-// stores device-wide, the CTA counts itself done (acq_rel at device scope: the
+// Completion of a grid, fused into its last CTA: every CTA's stores are
+// ordered device-wide, the CTA counts itself done (acq_rel at device scope: the
 // counting CTAs and the publisher all run on this GPU), and the CTA that
 // finishes last publishes the sequence number with a system-scope release
 // store (and resets the counter for the fence slot's next use).  A release is
@@ -131,27 +131,33 @@ __device__ __forceinline__ void chain_wait(const MoveDesc &d) {
 // overlapped restore first waits for its predecessor's fence (chain_wait).  A
 // ring descriptor's completion record (ext_word), when given, is stored right
 // after the fence.
+//
+// arrive_and_publish: one thread of the CTA, once the CTA's stores are ordered
+// (its own fence, or a barrier after every thread's fence).
+__device__ __forceinline__ void arrive_and_publish(const MoveDesc &d) {
+    unsigned int done;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(done)
+                 : "l"(d.fence_count)
+                 : "memory");
+    if (done == gridDim.x - 1) {
+        *d.fence_count = 0u;
+        if (d.chain_word != nullptr) chain_wait(d);
+        asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.fence_word),
+                     "l"(d.fence_seq)
+                     : "memory");
+        if (d.ext_word != nullptr)
+            asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.ext_word),
+                         "l"(d.ext_value)
+                         : "memory");
+    }
+}
+
+// Every thread of the CTA stored: each fences, the CTA meets, one arrives.
 __device__ __forceinline__ void complete_grid(const MoveDesc &d) {
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned int done;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                     : "=r"(done)
-                     : "l"(d.fence_count)
-                     : "memory");
-        if (done == gridDim.x - 1) {
-            *d.fence_count = 0u;
-            if (d.chain_word != nullptr) chain_wait(d);
-            asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.fence_word),
-                         "l"(d.fence_seq)
-                         : "memory");
-            if (d.ext_word != nullptr)
-                asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(d.ext_word),
-                             "l"(d.ext_value)
-                             : "memory");
-        }
-    }
+    if (threadIdx.x == 0) arrive_and_publish(d);
 }
 
 // Progressive layers: called by lane 0 of a warp once its `count` segments of
@@ -485,8 +491,15 @@ __global__ void __launch_bounds__(kBulkThreads)
         }
         asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // every store complete
         asm volatile("fence.proxy.async.global;" ::: "memory");
+        // Lane 0 issued every copy of this CTA, so it completes alone; the other
+        // lanes have left already.  Parked at a barrier while lane 0 ran the
+        // pipeline, they slowed it: back-to-back 1 GiB gathers ran at 6,363-6,370
+        // GB/s that way and at 6,402-6,419 with lane 0 completing alone.
+        if (d.fence_word != nullptr) {
+            __threadfence();
+            arrive_and_publish(d);
+        }
     }
-    if (d.fence_word != nullptr) complete_grid(d);
 }
 
 // ------------------------------------------------- transposing bulk path

@@ -68,10 +68,11 @@ def test_backup_bytes_are_on_the_host_when_its_fence_is(geom, mode, mode_config)
         s = torch.cuda.Stream()
         og = oracle_geom(g)
         for k in range(ROUNDS):
+            v = k % 255 + 1                    # a new, nonzero offset every round
             src = r.permutation(g.P).astype(np.int32)
             slots = r.permutation(g.P).astype(np.int32)
             with torch.cuda.stream(s):
-                torch.add(base, k + 1, out=rig.alloc[off:off + nb])   # wraps mod 256
+                torch.add(base, v, out=rig.alloc[off:off + nb])   # wraps mod 256
             f = kvb.kv_backup(rig.pool, rig.hostt, src, slots, s.cuda_stream)
             if k % 2 == 0:
                 kvb.kv_fence_wait(f, WAIT_NS)
@@ -82,7 +83,7 @@ def test_backup_bytes_are_on_the_host_when_its_fence_is(geom, mode, mode_config)
                 assert kvb.kv_fence_query(f) == kvb.KV_OK
             got = host_view.copy()             # read right after the fence, nothing synced
             pool_k = alloc0.copy()
-            pool_k[off:off + nb] = base_np + np.uint8(k + 1)
+            pool_k[off:off + nb] = base_np + np.uint8(v)
             want = np.zeros_like(got)
             oracle.backup(og, pool_k, want, src, slots, pool_offset=off, threads=4)
             assert np.array_equal(got, want), f"round {k}: " + _mismatch("host tier", got, want)
@@ -105,7 +106,7 @@ def test_restored_pages_are_seen_by_a_stream_that_waits_on_the_fence(geom, mode,
         s, c = torch.cuda.Stream(), torch.cuda.Stream()
         og = oracle_geom(g)
         for k in range(ROUNDS):
-            host_view[:] = host0 + np.uint8(k + 1)    # the host rewrites its tier every round
+            host_view[:] = host0 + np.uint8(k % 255 + 1)   # the host rewrites its tier
             slots = r.permutation(g.P).astype(np.int32)
             dst = r.permutation(g.P).astype(np.int32)
             f = kvb.kv_restore(rig.pool, rig.hostt, slots, dst, -1, s.cuda_stream)
