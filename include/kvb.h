@@ -649,7 +649,11 @@ KVB_API kv_status kv_l3_get(kv_l3 store, void *host, uint64_t host_slots,
 /* DeviceSyncIPC wait/query ([RFC] §Device IPC data path).  A fence completes
  * when every byte of its operation is in place.  Completion is a sequence
  * number the GPU stores into a mapped pinned word after the operation, so
- * the host learns of it without a CUDA call.
+ * the host learns of it without a CUDA call.  The word is stored with a
+ * system-scope release that orders every byte of the operation: a host
+ * thread that sees the fence complete may read a backup's host slots at once,
+ * and work on a stream that waited with kv_fence_stream_wait sees a restore's
+ * pages.
  * kv_fence_query: OK when complete, TIMEOUT when not yet, ABORTED when the
  * operation completed by giving up (kv_backup_when_ready whose ready fence
  * never arrived), INVALID_ARG for a fence never issued.  kv_fence_wait: polls
