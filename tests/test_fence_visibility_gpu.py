@@ -5,11 +5,13 @@ and a copy on another stream ordered after the op only by kv_fence_stream_wait.
 
 The fused completion orders each CTA's stores at device scope and publishes
 the fence with one system-scope release store; the copy-engine modes publish
-it with a marker kernel after their copies.  Each of 400 rounds below rewrites the
-source with a new value, so a byte left over from the previous round, or one
-still in flight when the fence was seen, shows up as a mismatch against the
-oracle (RFC "[HiCache] Out-of-process HiCache data plane", §Device IPC data
-path: the completion handle says the copy has landed)."""
+it with a marker kernel after their copies; overlapped ops (the overlap flags)
+publish in call order after waiting for their predecessor's fence.  Every
+round below rewrites the source with a new value, so a byte left over from the
+previous round, or one still in flight when the fence was seen, shows up as a
+mismatch against the oracle (RFC "[HiCache] Out-of-process HiCache data
+plane", §Device IPC data path: the completion handle says the copy has
+landed)."""
 import time
 
 import numpy as np
