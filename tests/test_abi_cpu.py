@@ -275,3 +275,20 @@ def test_id_lists_are_refused_rather_than_wrapped():
     lay = kvb.make_layout(2, 2, 64, 16, 2, 128)
     with pytest.raises(ValueError):                         # before the C call
         kvb.kv_op_validate(lay, 16, 0, [2**32 + 3], [0], -1)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """The binding has no fallback: a copy of it next to no built library
+    refuses to import, naming the missing file."""
+    import shutil
+    import subprocess
+    import sys
+
+    pkg = tmp_path / "unbuilt_pkg"
+    pkg.mkdir()
+    shutil.copy(kvb.__file__, pkg / "kvb.py")
+    (pkg / "__init__.py").write_text("")
+    r = subprocess.run([sys.executable, "-c", "import unbuilt_pkg.kvb"], cwd=tmp_path,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libkvb.so is missing" in r.stderr
