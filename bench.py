@@ -1376,13 +1376,25 @@ def write_through(ctx, su):
     t_b = wt_timed(wt_backup)
     t_last = wt_timed(lambda i: wt_backup(i, True))
     t_p = wt_timed(wt_pipelined)
+    # the SM budget of the backups: k CTAs of 1,024 threads (k whole SMs) each
+    budget = []
+    if not ctx.args.max_ctas and not ctx.args.cta_threads:
+        for k in (4, 6, 8):
+            ctx.set_config(max_ctas=k, cta_threads=1024)
+            tb_k, tp_k = wt_timed(wt_backup), wt_timed(wt_pipelined)
+            budget.append({"sms": k, "backup_only_ms": round(tb_k, 3),
+                           "backup_gbs": round(w.n * su.g.page_bytes / (tb_k / 1e3) / GB, 1),
+                           "pipelined_ms": round(tp_k, 3),
+                           "exposed_backup_ms": round(tp_k - t_c, 3)})
+        ctx.set_config()
     del A, Bm, Cm
     return {"forward_stand_in": f"bf16 GEMM {M}^3 x {per_chunk} per chunk on a compute stream",
             "chunks": chunks, "pages_per_chunk": cp,
             "compute_only_ms": round(t_c, 3), "backup_only_ms": round(t_b, 3),
             "pipelined_ms": round(t_p, 3), "exposed_backup_ms": round(t_p - t_c, 3),
             "last_chunk_backup_ms": round(t_last, 3),
-            "exposed_beyond_last_chunk_ms": round(t_p - t_c - t_last, 3)}
+            "exposed_beyond_last_chunk_ms": round(t_p - t_c - t_last, 3),
+            "sm_budget": budget or None}
 
 
 def l3_hop(ctx, su):
