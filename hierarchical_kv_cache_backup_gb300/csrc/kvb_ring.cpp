@@ -108,13 +108,13 @@ double now_ns() {
     return ts.tv_sec * 1e9 + ts.tv_nsec;
 }
 
-// Busy for the first 50 us of a wait, then yield until 2 ms, then sleep.
+// Busy for the first 50 us of a wait, then yield until 20 ms, then sleep.
 void backoff(int &spins) {
     static thread_local double t0;
     if (spins++ == 0) t0 = now_ns();
     const double t = now_ns() - t0;
     if (t < 50e3) return;
-    if (t < 2e6) {
+    if (t < 20e6) {
         sched_yield();
     } else {
         timespec ts{0, 10000};

@@ -657,7 +657,10 @@ KVB_API kv_status kv_l3_get(kv_l3 store, void *host, uint64_t host_slots,
  * kv_fence_query: OK when complete, TIMEOUT when not yet, ABORTED when the
  * operation completed by giving up (kv_backup_when_ready whose ready fence
  * never arrived), INVALID_ARG for a fence never issued.  kv_fence_wait: polls
- * until complete or until timeout_ns has passed (TIMEOUT).  kv_fence_stream_wait: makes `stream` wait
+ * until complete or until timeout_ns has passed (TIMEOUT): spinning for the
+ * first 50 us, then yielding the core between polls up to 20 ms (the calling
+ * thread stays runnable, so it sees the fence within microseconds), then
+ * sleeping between polls.  kv_fence_stream_wait: makes `stream` wait
  * for the fence on the GPU (the compute stream of a layer-wise restore): the
  * stream waits for the fence's word itself (a 64-bit stream wait-value) where
  * the driver supports it, else for the fence's event. */
